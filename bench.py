@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""bench.py -- DDPM core fused forward+backward throughput on one GB300.
+
+One step = one ddpm_forward plus one ddpm_backward (fused generator + dynamic
+dilated depthwise filter, then dX / dY / dW / dbias with recomputed taps) over
+one batch of the synthetic workload B=1, C=64, K=3, 256x256, bf16, inputs
+resident in HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU FP64 oracle (the plain C restatement of the
+method under oracle/) on the host cores, on a bounded sample of the same
+workload: the operator has no other runnable reference here.
+
+Timing: CUDA events on the launching stream around each step, a 256 MiB
+write between steps flushes the 129 MB L2 (outside the events), W untimed
+warm-up steps, barrier + synchronize on both sides, max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "DDPM fused fwd+bwd Mpixel/s (C=64,K=3,256² bf16, 1 GB300); % of roofline"
+UNIT = "Mpixel/s"
+DEFAULT_WORKLOAD = "b1_c64_256x256_k3"
+FLUSH_BYTES = 256 << 20
+
+# Nominal GB300 unit counts used for the CUDA-core (FFMA) ceiling.
+NUM_SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def load_peaks():
+    """Measured HBM / bf16 peaks (driver-written), else the stated fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "sm_max_mhz": float(m.get("sm_max_mhz", 2070.0)), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def fp32_alu_tflops(peaks) -> float:
+    """FFMA ceiling: SMs x FP32 lanes x 2 flops x max SM clock."""
+    return NUM_SMS * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+
+
+def kernel_work(name: str, p, es: int, splits: int):
+    """Algorithmic work of one launch of a kernel: (bound, amount, unit-kind).
+
+    flops count the contractions the kernel performs (2 per multiply-add);
+    bytes count each input read once and each output written once.
+    """
+    P = p.B * p.H * p.W
+    O = p.O
+    C = p.C
+    gemm = 2.0 * O * C * P
+    if name == "filter_pregenerated_simt":
+        return "hbm", P * (O + C + 4 * C) * es, "bytes"
+    if name in ("forward_simt", "bwd_dx_simt", "bwd_dy_simt"):
+        return "alu", gemm, "flops"
+    if name == "bwd_dw_partial_simt":
+        return "alu", 2.0 * O * (C + 1) * P, "flops"
+    if name == "bwd_dw_reduce":
+        return "hbm", splits * O * (C + 1) * 4 + O * (C + 1) * es, "bytes"
+    if name in ("forward_tc", "bwd_dx_tc"):
+        return "tensor", gemm, "flops"
+    if name == "bwd_dydw_tc":
+        return "tensor", 2 * gemm, "flops"
+    return "unknown", 0.0, "flops"
+
+
+def step_roofline_us(p, es: int, peaks) -> dict:
+    """Roofline of one fwd+bwd step: max(GEMM flops at the bf16 tensor peak,
+    minimum bytes at the HBM peak).  Four contractions of 2*O*C flops per pixel
+    (generator, generator recompute for dX, dY, dW); bytes: x, y, weight, bias
+    and grad read once, out / dx / dy / dW / dbias written once."""
+    P = p.B * p.H * p.W
+    flops = 4 * 2.0 * p.O * p.C * P
+    fwd_bytes = P * (2 * p.C + 4 * p.C) * es
+    bwd_bytes = P * (4 * p.C + 2 * p.C + 2 * p.C) * es
+    w_bytes = 2 * (p.O * p.C + p.O) * es * 2
+    nbytes = fwd_bytes + bwd_bytes + w_bytes
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    return {"flops": flops, "bytes": nbytes, "tensor_us": t_tc, "hbm_us": t_hbm, "roofline_us": max(t_tc, t_hbm)}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.out = os.path.join("/tmp", f"ddpm_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.2)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not os.path.exists(self.out):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.out) as f:
+            for line in f:
+                cols = [c.strip() for c in line.split(",")]
+                if len(cols) < 9:
+                    continue
+                try:
+                    sm.append(float(cols[1]))
+                    smax.append(float(cols[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, cols[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.out)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_digest() -> str:
+    """Digest of the CUDA sources (to invalidate stored ncu traffic figures)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dynamic_dilated_depthwise_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, or None if the
+    kernels changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_digest") != kernel_source_digest():
+        return None
+    k = t.get("kernels", {}).get(kernel)
+    if not k or k.get("workload") != workload:
+        return None
+    return k.get("dram_bytes_per_launch")
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(p, dtype: str, target_s: float = 10.0) -> dict:
+    """The oracle as it stands, on the host cores: fwd+bwd of the full image,
+    repeated until about target_s of CPU time (at most 3 repetitions)."""
+    import oracle
+    from dynamic_dilated_depthwise_gb300.inputs import Problem, SEEDS, make_inputs
+    one = Problem(1, p.C, p.H, p.W, p.K, p.dilations)
+    h = make_inputs(one, SEEDS.get(p.name, 1000), dtype)
+    h = {k: v.double().numpy() for k, v in h.items()}
+    bf = dtype == "bfloat16"
+    oracle.build()
+    reps, t_total = 0, 0.0
+    while reps < 3 and (reps == 0 or t_total < target_s):
+        t0 = time.perf_counter()
+        oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
+        oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    px = reps * one.pixels
+    return {"value": px / t_total / 1e6, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{reps} x fwd+bwd of one {p.H}x{p.W} image (C={p.C}, K={p.K}, {dtype}-valued inputs, FP64 math)",
+            "seconds": round(t_total, 3)}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from dynamic_dilated_depthwise_gb300 import binding, build
+    from dynamic_dilated_depthwise_gb300.inputs import SEEDS, WORKLOADS, make_inputs
+
+    build.build()
+    lib = binding.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    p = WORKLOADS[args.workload]
+    dtype = args.dtype
+    es = 2 if dtype == "bfloat16" else 4
+    h = make_inputs(p, SEEDS[p.name] + rank, dtype)
+    d = {k: v.to(dev) for k, v in h.items()}
+    flags = binding.DDPM_FLAG_TF32_BACKWARD
+    prob = binding.make_problem(p.B, p.C, p.H, p.W, p.K, p.dilations,
+                                binding.DDPM_BFLOAT16 if dtype == "bfloat16" else binding.DDPM_FLOAT32, flags)
+    out = torch.empty((p.B, 4 * p.C, p.H, p.W), dtype=d["x"].dtype, device=dev)
+    dx, dy = torch.empty_like(d["x"]), torch.empty_like(d["y"])
+    dw, db = torch.empty_like(d["weight"]), torch.empty_like(d["bias"])
+    ws_bytes = binding.ddpm_backward_workspace_size(prob)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    ptr = {k: v.data_ptr() for k, v in d.items()}
+    import ctypes
+    pref = ctypes.byref(prob)
+
+    def step():
+        s1 = lib.ddpm_forward(pref, ptr["x"], ptr["y"], ptr["weight"], ptr["bias"], out.data_ptr(), sh)
+        s2 = lib.ddpm_backward(pref, ptr["grad_out"], ptr["x"], ptr["y"], ptr["weight"], ptr["bias"],
+                               dx.data_ptr(), dy.data_ptr(), dw.data_ptr(), db.data_ptr(), ws.data_ptr(),
+                               ws.numel(), sh)
+        if s1 or s2:
+            raise RuntimeError(f"library error {binding.status_string(s1 or s2)}")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert binding.ddpm_get_device_error() == 0
+
+    # ---- timed loop (value) ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        barrier(world)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(world, sum(step_ms))
+    ms_per_step = total_ms / args.steps
+    value = world * p.pixels / (ms_per_step * 1e-3) / 1e6
+
+    # ---- traced loop: per-kernel device time on the launching stream ----
+    binding.ddpm_trace_read()
+    binding.ddpm_trace_enable(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    binding.ddpm_trace_enable(False)
+    recs = binding.ddpm_trace_read()
+    per_kernel = {}
+    for name, ms in recs:
+        per_kernel.setdefault(name, []).append(ms)
+    launches_per_step = len(recs) / args.steps
+    peaks = load_peaks()
+    splits = ws_bytes // (4 * p.O * (p.C + 1)) if ws_bytes else 1
+    dominant = max(per_kernel, key=lambda k: sum(per_kernel[k]))
+    avg_ms = sum(per_kernel[dominant]) / len(per_kernel[dominant])
+    bound, amount, kind = kernel_work(dominant, p, es, splits)
+    if bound == "hbm":
+        achieved, peak, unit = amount / (avg_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    elif bound == "tensor":
+        achieved, peak, unit = amount / (avg_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = amount / (avg_ms * 1e-3) / 1e12, fp32_alu_tflops(peaks), "TFLOP/s"
+    roof = {"bound": bound, "kernel": dominant, "achieved": round(achieved, 3), "peak": round(peak, 1),
+            "unit": unit, "frac": round(achieved / peak, 4),
+            "traffic": stored_traffic(dominant, p.name),
+            "peak_source": peaks["source"] if bound != "alu" else "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock",
+            "avg_launch_us": round(avg_ms * 1e3, 3),
+            "work_per_launch": amount, "work_unit": kind}
+    kernels = {k: {"launches_per_step": len(v) / args.steps, "avg_us": round(sum(v) / len(v) * 1e3, 3),
+                   "share": round(sum(v) / sum(sum(x) for x in per_kernel.values()), 4)}
+               for k, v in per_kernel.items()}
+    sr = step_roofline_us(p, es, peaks)
+    step_roof = {"roofline_us": round(sr["roofline_us"], 3), "tensor_us": round(sr["tensor_us"], 3),
+                 "hbm_us": round(sr["hbm_us"], 3), "measured_us": round(ms_per_step * 1e3, 3),
+                 "frac": round(sr["roofline_us"] / (ms_per_step * 1e3), 4)}
+
+    # ---- end to end through the C ABI: pinned host inputs in, results out ----
+    e2e_steps = min(args.steps, 20)
+    hin = {k: v.pin_memory() for k, v in h.items()}
+    hout = {"out": torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+            "dx": torch.empty(dx.shape, dtype=dx.dtype).pin_memory(),
+            "dy": torch.empty(dy.shape, dtype=dy.dtype).pin_memory(),
+            "dw": torch.empty(dw.shape, dtype=dw.dtype).pin_memory(),
+            "db": torch.empty(db.shape, dtype=db.dtype).pin_memory()}
+    dres = {"out": out, "dx": dx, "dy": dy, "dw": dw, "db": db}
+    bi = sum(v.numel() * v.element_size() for v in hin.values())
+    bo = sum(v.numel() * v.element_size() for v in hout.values())
+    es_, ee_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(e2e_steps + 2):
+        flush.zero_()
+        es_.record(stream)
+        for k in hin:
+            d[k].copy_(hin[k], non_blocking=True)
+        step()
+        for k in hout:
+            hout[k].copy_(dres[k], non_blocking=True)
+        ee_.record(stream)
+        ee_.synchronize()
+        if i >= 2:
+            e2e_ms += es_.elapsed_time(ee_)
+    e2e_ms = max_over_ranks(world, e2e_ms) / e2e_steps
+    e2e = {"value": round(world * p.pixels / (e2e_ms * 1e-3) / 1e6, 3), "unit": UNIT,
+           "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 4)}
+    assert binding.ddpm_get_device_error() == 0
+
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dtype == "bfloat16" else "f32",
+            "data": "synthetic (seeded N(0,1) x, y, grad; weight N(0,1/C); bias N(0,0.01))",
+            "config": {"workload": p.name, "B": p.B, "C": p.C, "H": p.H, "W": p.W, "K": p.K,
+                       "dilations": list(p.dilations), "dtype": dtype,
+                       "step": "ddpm_forward + ddpm_backward (dx, dy, dweight, dbias)",
+                       "l2": "flushed: 256 MiB write before each step, outside the timed events",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "e2e": e2e, "wall_s_timed_loop": round(t_wall, 4)}
+    line["clocks"] = clk.summary()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(p, dtype)
+    return line
+
+
+def run_reference(args, world, rank):
+    """The CPU FP64 oracle on the host cores, timed as the reference arm."""
+    if rank != 0:
+        return None
+    import oracle
+    from dynamic_dilated_depthwise_gb300.inputs import Problem, SEEDS, WORKLOADS, make_inputs
+    p = WORKLOADS[args.workload]
+    rows = 16
+    sample = Problem(1, p.C, rows, p.W, p.K, p.dilations)
+    h = make_inputs(sample, SEEDS[p.name], args.dtype)
+    h = {k: v.double().numpy() for k, v in h.items()}
+    bf = args.dtype == "bfloat16"
+    oracle.build()
+
+    def step():
+        oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
+        oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    ms = t / args.steps * 1e3
+    value = sample.pixels / (ms * 1e-3) / 1e6
+    desc = f"fwd+bwd of a {rows}x{p.W} band (B=1, C={p.C}, K={p.K}) per step, FP64, {args.dtype}-valued inputs"
+    return {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": p.name, "B": p.B, "C": p.C, "H": p.H, "W": p.W, "K": p.K,
+                       "dilations": list(p.dilations), "dtype": args.dtype, "sample_rows": rows},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[1])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--dtype", choices=("bfloat16", "float32"), default="bfloat16")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (faster runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

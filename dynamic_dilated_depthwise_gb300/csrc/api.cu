@@ -1,0 +1,187 @@
+// api.cu -- the C ABI of libddpm_gb300.so (declared in include/ddpm.h).
+//
+// Host-side validation, kernel selection and launch on the caller's stream.
+// The library never allocates device memory, never synchronises (except in
+// ddpm_get_device_error) and never throws across the boundary.
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/ddpm.h"
+#include "launch.h"
+
+namespace ddpm {
+
+// Device-side error word: kernels with bounded waits set a nonzero code here
+// when a wait expires, instead of trapping.  Passed to kernels by address.
+__device__ unsigned int g_device_error = 0;
+
+unsigned int* device_error_word() {
+    static std::mutex mu;
+    static unsigned int* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned int*>(p);
+    }
+    return addr[dev];
+}
+
+}  // namespace ddpm
+
+namespace {
+
+using ddpm::Dims;
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+size_t elem_size(int dtype) { return dtype == DDPM_BFLOAT16 ? 2 : 4; }
+
+ddpm_status validate(const ddpm_problem* p, Dims* d) {
+    if (p == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
+    if (p->B < 1 || p->C < 1 || p->H < 1 || p->W < 1) return DDPM_ERR_INVALID_ARGUMENT;
+    if (p->K < 1 || p->K % 2 == 0) return DDPM_ERR_INVALID_ARGUMENT;
+    if (p->dtype != DDPM_FLOAT32 && p->dtype != DDPM_BFLOAT16) return DDPM_ERR_INVALID_ARGUMENT;
+    for (int i = 0; i < 3; ++i)
+        if (p->dilations[i] < 1) return DDPM_ERR_INVALID_ARGUMENT;
+    if ((p->flags & ~DDPM_FLAG_TF32_BACKWARD) != 0) return DDPM_ERR_INVALID_ARGUMENT;
+    if (p->K > 7) return DDPM_ERR_UNSUPPORTED;
+    // grid-dimension and index-width limits of this build
+    if (p->B > 65535 || p->C > 65535) return DDPM_ERR_UNSUPPORTED;
+    for (int i = 0; i < 3; ++i)
+        if (p->dilations[i] > (1 << 20)) return DDPM_ERR_UNSUPPORTED;
+    const long long HW = (long long)p->H * p->W;
+    if (HW > INT_MAX) return DDPM_ERR_UNSUPPORTED;
+    const long long O = 3LL * p->C * p->K * p->K;
+    // largest tensor: taps [B, O, H, W]; keep every flat index inside int64 with margin
+    if ((double)p->B * (double)O * (double)HW > 4.0e18) return DDPM_ERR_UNSUPPORTED;
+    // shared-memory staging of the CUDA-core kernels
+    const long long K2 = (long long)p->K * p->K;
+    const long long KP = (K2 + 3) / 4 * 4;
+    if ((size_t)p->C * KP * sizeof(float) > kMaxSmem) return DDPM_ERR_UNSUPPORTED;
+    if ((size_t)p->C * 8 * sizeof(float) > kMaxSmem) return DDPM_ERR_UNSUPPORTED;
+    d->B = p->B; d->C = p->C; d->H = p->H; d->W = p->W; d->K = p->K; d->r = p->K / 2;
+    for (int i = 0; i < 3; ++i) d->dil[i] = p->dilations[i];
+    d->dtype = p->dtype;
+    d->flags = p->flags;
+    d->HW = HW;
+    d->O = O;
+    return DDPM_OK;
+}
+
+ddpm_status check_ptr(const void* ptr, size_t align, bool nullable) {
+    if (ptr == nullptr) return nullable ? DDPM_OK : DDPM_ERR_INVALID_ARGUMENT;
+    if ((uintptr_t)ptr % align != 0) return DDPM_ERR_MISALIGNED;
+    return DDPM_OK;
+}
+
+#define DDPM_TRY(expr)                         \
+    do {                                       \
+        const ddpm_status s_ = (expr);         \
+        if (s_ != DDPM_OK) return s_;          \
+    } while (0)
+
+ddpm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DDPM_OK : DDPM_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+ddpm_status ddpm_forward(const ddpm_problem* problem, const void* x, const void* y, const void* weight,
+                         const void* bias, void* out, ddpm_stream_t stream) {
+    Dims d;
+    DDPM_TRY(validate(problem, &d));
+    const size_t es = elem_size(d.dtype);
+    DDPM_TRY(check_ptr(x, es, false));
+    DDPM_TRY(check_ptr(y, es, false));
+    DDPM_TRY(check_ptr(weight, es, false));
+    DDPM_TRY(check_ptr(bias, es, true));
+    DDPM_TRY(check_ptr(out, es, false));
+    try {
+        return from_cuda(ddpm::launch_forward_simt(d, x, y, weight, bias, out, (cudaStream_t)stream));
+    } catch (...) {
+        return DDPM_ERR_CUDA;
+    }
+}
+
+ddpm_status ddpm_filter_pregenerated(const ddpm_problem* problem, const void* x, const void* taps, void* out,
+                                     ddpm_stream_t stream) {
+    Dims d;
+    DDPM_TRY(validate(problem, &d));
+    const size_t es = elem_size(d.dtype);
+    DDPM_TRY(check_ptr(x, es, false));
+    DDPM_TRY(check_ptr(taps, es, false));
+    DDPM_TRY(check_ptr(out, es, false));
+    try {
+        return from_cuda(ddpm::launch_filter_simt(d, x, taps, out, (cudaStream_t)stream));
+    } catch (...) {
+        return DDPM_ERR_CUDA;
+    }
+}
+
+ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* bytes) {
+    Dims d;
+    DDPM_TRY(validate(problem, &d));
+    if (bytes == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
+    *bytes = ddpm::backward_simt_workspace(d);
+    return DDPM_OK;
+}
+
+ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, const void* x, const void* y,
+                          const void* weight, const void* bias, void* dx, void* dy, void* dweight,
+                          void* dbias, void* workspace, size_t workspace_bytes, ddpm_stream_t stream) {
+    Dims d;
+    DDPM_TRY(validate(problem, &d));
+    const size_t es = elem_size(d.dtype);
+    DDPM_TRY(check_ptr(grad_out, es, false));
+    DDPM_TRY(check_ptr(x, es, false));
+    DDPM_TRY(check_ptr(y, es, false));
+    DDPM_TRY(check_ptr(weight, es, false));
+    DDPM_TRY(check_ptr(bias, es, true));
+    DDPM_TRY(check_ptr(dx, es, false));
+    DDPM_TRY(check_ptr(dy, es, false));
+    DDPM_TRY(check_ptr(dweight, es, false));
+    DDPM_TRY(check_ptr(dbias, es, true));
+    DDPM_TRY(check_ptr(workspace, 16, false));
+    if (workspace_bytes < ddpm::backward_simt_workspace(d)) return DDPM_ERR_WORKSPACE_TOO_SMALL;
+    try {
+        return from_cuda(ddpm::launch_backward_simt(d, grad_out, x, y, weight, bias, dx, dy, dweight, dbias,
+                                                    workspace, (cudaStream_t)stream));
+    } catch (...) {
+        return DDPM_ERR_CUDA;
+    }
+}
+
+ddpm_status ddpm_get_device_error(ddpm_stream_t stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DDPM_ERR_CUDA;
+    unsigned int* word = ddpm::device_error_word();
+    if (word == nullptr) return DDPM_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DDPM_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return DDPM_ERR_CUDA;
+        return DDPM_ERR_DEVICE_TIMEOUT;
+    }
+    return DDPM_OK;
+}
+
+const char* ddpm_status_string(ddpm_status status) {
+    switch (status) {
+        case DDPM_OK: return "DDPM_OK";
+        case DDPM_ERR_INVALID_ARGUMENT: return "DDPM_ERR_INVALID_ARGUMENT: invalid argument";
+        case DDPM_ERR_UNSUPPORTED: return "DDPM_ERR_UNSUPPORTED: problem outside what this build implements";
+        case DDPM_ERR_MISALIGNED: return "DDPM_ERR_MISALIGNED: pointer not aligned to its element size";
+        case DDPM_ERR_WORKSPACE_TOO_SMALL: return "DDPM_ERR_WORKSPACE_TOO_SMALL: workspace below the queried size";
+        case DDPM_ERR_CUDA: return "DDPM_ERR_CUDA: a CUDA call or kernel launch failed";
+        case DDPM_ERR_DEVICE_TIMEOUT: return "DDPM_ERR_DEVICE_TIMEOUT: a kernel's bounded wait expired";
+    }
+    return "DDPM: unknown status";
+}
+
+int ddpm_version(void) { return 100; }
+
+}  // extern "C"

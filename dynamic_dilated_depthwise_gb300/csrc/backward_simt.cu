@@ -1,0 +1,389 @@
+// backward_simt.cu -- DDPM core backward on CUDA cores (any dtype and shape).
+//
+// README "lartpang/DynamicConvolutionOperator", section "CUDA Flash 式融合训练":
+//   dX     : recompute the dynamic taps and gather each dilation's contribution;
+//   dY     : form dK = shifted(x) * grad on chip and multiply it by the generator
+//            weight straight away;
+//   dW/db  : form dK on chip and reduce over space -- the tokens are split into
+//            at most 16 FP32 partials and a second short kernel sums them.
+// Taps are recomputed, never written out.  In bf16 problems the tap rounding
+// is straight-through: dx multiplies grad by the rounded taps.
+//
+// Four kernels: dx_kernel, dy_kernel, dw_partial_kernel, dw_reduce_kernel.
+// The partial sums are summed in a fixed order, so results are reproducible
+// bit for bit from run to run.
+#include "launch.h"
+
+namespace ddpm {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kCG = 8;          // dx: channels per block
+constexpr int kJC = 64;         // dy: j per register chunk
+constexpr int kMaxSplits = 16;  // "最多 16 个 FP32 partial"
+
+// ---------------------------------------------------------------- dX --
+// dx[b,c,q] = g[b,c,q] + sum_{di,ky,kx} Tq[b,o,q-off] * g[b,(1+di)C+c,q-off]
+// One thread per pixel q, CG channels per block.  For each tap (di,k) the
+// block stages the CG generator rows {o(di, c0+cc, k)} as Ws[j][cc]; each
+// thread evaluates the taps of its CG channels at the neighbour p = q - off
+// (one y load feeds CG FMAs) and accumulates tap * grad there.
+template <typename T, int K>
+__global__ void __launch_bounds__(kThreads) dx_kernel(Dims d, const T* __restrict__ g,
+                                                      const T* __restrict__ y, const T* __restrict__ wgt,
+                                                      const T* __restrict__ bias, T* __restrict__ dx) {
+    constexpr int K2 = K * K;
+    extern __shared__ __align__(16) float Ws[];  // [C][kCG]
+    __shared__ float bs[kCG];
+    const int r = K / 2;
+    const int C = d.C;
+    const int b = blockIdx.z;
+    const int c0 = blockIdx.y * kCG;
+    const long long q = (long long)blockIdx.x * kThreads + threadIdx.x;
+    const bool active = q < d.HW;
+    const int h = active ? (int)(q / d.W) : 0;
+    const int w = active ? (int)(q % d.W) : 0;
+    const T* yb = y + (long long)b * C * d.HW;
+    const T* gb = g + (long long)b * 4 * C * d.HW;
+
+    float acc[kCG];
+#pragma unroll
+    for (int cc = 0; cc < kCG; ++cc)
+        acc[cc] = (active && c0 + cc < C) ? to_f(gb[(long long)(c0 + cc) * d.HW + q]) : 0.0f;
+
+#pragma unroll 1
+    for (int di = 0; di < 3; ++di) {
+        const int dil = dil_of(d, di);
+#pragma unroll 1
+        for (int k = 0; k < K2; ++k) {
+            __syncthreads();
+            for (int i = threadIdx.x; i < C * kCG; i += kThreads) {
+                const int j = i / kCG, cc = i % kCG;
+                const int c = c0 + cc;
+                Ws[i] = c < C ? to_f(wgt[((long long)(di * C + c) * K2 + k) * C + j]) : 0.0f;
+            }
+            if (threadIdx.x < kCG) {
+                const int c = c0 + threadIdx.x;
+                bs[threadIdx.x] = (c < C && bias != nullptr) ? to_f(bias[(long long)(di * C + c) * K2 + k]) : 0.0f;
+            }
+            __syncthreads();
+            const int ky = k / K, kx = k % K;
+            const int hs = h - (ky - r) * dil, ws = w - (kx - r) * dil;
+            if (!active || hs < 0 || hs >= d.H || ws < 0 || ws >= d.W) continue;
+            const long long ps = (long long)hs * d.W + ws;
+            float t[kCG];
+#pragma unroll
+            for (int cc = 0; cc < kCG; ++cc) t[cc] = bs[cc];
+            for (int j = 0; j < C; ++j) {
+                const float yv = ldg_f(yb + (long long)j * d.HW + ps);
+                const float4 w0 = reinterpret_cast<const float4*>(Ws + j * kCG)[0];
+                const float4 w1 = reinterpret_cast<const float4*>(Ws + j * kCG)[1];
+                t[0] = fmaf(w0.x, yv, t[0]); t[1] = fmaf(w0.y, yv, t[1]);
+                t[2] = fmaf(w0.z, yv, t[2]); t[3] = fmaf(w0.w, yv, t[3]);
+                t[4] = fmaf(w1.x, yv, t[4]); t[5] = fmaf(w1.y, yv, t[5]);
+                t[6] = fmaf(w1.z, yv, t[6]); t[7] = fmaf(w1.w, yv, t[7]);
+            }
+#pragma unroll
+            for (int cc = 0; cc < kCG; ++cc) {
+                if (c0 + cc < C) {
+                    const float gv = to_f(gb[(long long)((1 + di) * C + c0 + cc) * d.HW + ps]);
+                    acc[cc] = fmaf(quantise_tap<T>(t[cc]), gv, acc[cc]);
+                }
+            }
+        }
+    }
+    if (active) {
+#pragma unroll
+        for (int cc = 0; cc < kCG; ++cc)
+            if (c0 + cc < C) dx[((long long)b * C + c0 + cc) * d.HW + q] = from_f<T>(acc[cc]);
+    }
+}
+
+// ---------------------------------------------------------------- dY --
+// dy[b,j,p] = sum_o W[o,j] * dK[b,o,p],  dK = g[b,(1+di)C+c,p] * x[b,c,p+off].
+// One thread per pixel keeps kJC accumulators; per channel c the block stages
+// the 3*K*K generator rows of c (Ws[(di*K2+k)][jj]) and each thread forms the
+// dK of its pixel and applies it to the kJC weights (16-byte broadcasts).
+template <typename T, int K>
+__global__ void __launch_bounds__(kThreads) dy_kernel(Dims d, const T* __restrict__ g,
+                                                      const T* __restrict__ x, const T* __restrict__ wgt,
+                                                      T* __restrict__ dy) {
+    constexpr int K2 = K * K;
+    __shared__ __align__(16) float Ws[3 * K2 * kJC];
+    const int r = K / 2;
+    const int C = d.C;
+    const int b = blockIdx.z;
+    const int j0 = blockIdx.y * kJC;
+    const long long p = (long long)blockIdx.x * kThreads + threadIdx.x;
+    const bool active = p < d.HW;
+    const int h = active ? (int)(p / d.W) : 0;
+    const int w = active ? (int)(p % d.W) : 0;
+    const T* gb = g + (long long)b * 4 * C * d.HW;
+
+    float acc[kJC];
+#pragma unroll
+    for (int jj = 0; jj < kJC; ++jj) acc[jj] = 0.0f;
+
+#pragma unroll 1
+    for (int c = 0; c < C; ++c) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < 3 * K2 * kJC; i += kThreads) {
+            const int row = i / kJC, jj = i % kJC;  // row = di*K2 + k
+            const int di = row / K2, k = row % K2;
+            Ws[i] = (j0 + jj < C) ? to_f(wgt[((long long)(di * C + c) * K2 + k) * C + j0 + jj]) : 0.0f;
+        }
+        __syncthreads();
+        if (!active) continue;
+        const T* xp = x + ((long long)b * C + c) * d.HW;
+#pragma unroll 1
+        for (int di = 0; di < 3; ++di) {
+            const int dil = dil_of(d, di);
+            const float gv = to_f(gb[(long long)((1 + di) * C + c) * d.HW + p]);
+#pragma unroll
+            for (int k = 0; k < K2; ++k) {
+                const int ky = k / K, kx = k % K;
+                const float dk = gv * x_at(xp, d.H, d.W, h + (ky - r) * dil, w + (kx - r) * dil);
+                const float4* wr = reinterpret_cast<const float4*>(Ws + (di * K2 + k) * kJC);
+#pragma unroll
+                for (int q4 = 0; q4 < kJC / 4; ++q4) {
+                    const float4 w4 = wr[q4];
+                    acc[4 * q4 + 0] = fmaf(w4.x, dk, acc[4 * q4 + 0]);
+                    acc[4 * q4 + 1] = fmaf(w4.y, dk, acc[4 * q4 + 1]);
+                    acc[4 * q4 + 2] = fmaf(w4.z, dk, acc[4 * q4 + 2]);
+                    acc[4 * q4 + 3] = fmaf(w4.w, dk, acc[4 * q4 + 3]);
+                }
+            }
+        }
+    }
+    if (active) {
+#pragma unroll
+        for (int jj = 0; jj < kJC; ++jj)
+            if (j0 + jj < C) dy[((long long)b * C + j0 + jj) * d.HW + p] = from_f<T>(acc[jj]);
+    }
+}
+
+// ------------------------------------------------------------- dW, db --
+// Partial sums over split s of the flattened pixels (b, p):
+//   ws[s][o][j] = sum_{(b,p) in s} dK[b,o,p] * y[b,j,p]   (j < C)
+//   ws[s][o][C] = sum_{(b,p) in s} dK[b,o,p]               (the dbias column)
+// Block (c, di*JT + jt, s): the K*K taps of (di, c) x 64 columns of j (tile jt)
+// plus a column of ones that yields dbias.  Each pixel tile of kPT pixels is
+// staged as dK_s[k][pp] and y_s[jj][pp]; threads own 4x4 output micro-tiles and
+// a strided subset of the tile's pixel quads (register tiling, 16-byte shared
+// loads), and the lanes sharing a micro-tile are summed in a fixed order.
+constexpr int kPT = 64;
+constexpr int kNJ = 68;  // 64 j columns + ones column + 3 zero columns
+constexpr int kDwThreads = 256;
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kDwThreads) dw_partial_kernel(Dims d, const T* __restrict__ g,
+                                                                const T* __restrict__ x,
+                                                                const T* __restrict__ y,
+                                                                float* __restrict__ ws, long long chunk) {
+    constexpr int K2 = K * K;
+    constexpr int KP = (K2 + 3) / 4 * 4;
+    constexpr int NM = (KP / 4) * (kNJ / 4);
+    constexpr int L = (kDwThreads / NM) > 0 ? (kDwThreads / NM) : 1;
+    static_assert(NM * L <= kDwThreads, "micro-tiles must fit the block");
+    __shared__ __align__(16) float dK_s[KP * kPT];
+    __shared__ __align__(16) float y_s[kNJ * kPT];
+    __shared__ float red[NM * 16 * L];
+
+    const int r = K / 2;
+    const int C = d.C;
+    const int c = blockIdx.x;
+    const int JT = (C + 63) / 64;
+    const int di = blockIdx.y / JT;
+    const int jt = blockIdx.y % JT;
+    const int j0 = jt * 64;
+    const int s = blockIdx.z;
+    const int dil = dil_of(d, di);
+    const long long NP = (long long)d.B * d.HW;
+    const long long P0 = (long long)s * chunk;
+    const long long P1 = P0 + chunk < NP ? P0 + chunk : NP;
+    const int tid = threadIdx.x;
+    const int m = tid / L, lane = tid % L;
+    const bool computes = tid < NM * L;
+    const int mr = m / (kNJ / 4), mc = m % (kNJ / 4);
+
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+
+    for (long long base = P0; base < P1; base += kPT) {
+        __syncthreads();
+        for (int i = tid; i < KP * kPT; i += kDwThreads) {
+            const int k = i / kPT, pp = i % kPT;
+            const long long P = base + pp;
+            float v = 0.0f;
+            if (k < K2 && P < P1) {
+                const int b = (int)(P / d.HW);
+                const long long p = P % d.HW;
+                const int h = (int)(p / d.W), w = (int)(p % d.W);
+                const int ky = k / K, kx = k % K;
+                const float gv = to_f(g[((long long)b * 4 * C + (1 + di) * C + c) * d.HW + p]);
+                v = gv * x_at(x + ((long long)b * C + c) * d.HW, d.H, d.W, h + (ky - r) * dil, w + (kx - r) * dil);
+            }
+            dK_s[i] = v;
+        }
+        for (int i = tid; i < kNJ * kPT; i += kDwThreads) {
+            const int jj = i / kPT, pp = i % kPT;
+            const long long P = base + pp;
+            float v = 0.0f;
+            if (P < P1) {
+                if (jj < 64) {
+                    if (j0 + jj < C) {
+                        const int b = (int)(P / d.HW);
+                        const long long p = P % d.HW;
+                        v = to_f(y[((long long)b * C + j0 + jj) * d.HW + p]);
+                    }
+                } else if (jj == 64 && jt == 0) {
+                    v = 1.0f;
+                }
+            }
+            y_s[i] = v;
+        }
+        __syncthreads();
+        if (computes) {
+            for (int qd = lane; qd < kPT / 4; qd += L) {
+                float4 a[4], bq[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[i] = reinterpret_cast<const float4*>(dK_s + (4 * mr + i) * kPT)[qd];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) bq[j] = reinterpret_cast<const float4*>(y_s + (4 * mc + j) * kPT)[qd];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[i][j] = fmaf(a[i].x, bq[j].x, acc[i][j]);
+                        acc[i][j] = fmaf(a[i].y, bq[j].y, acc[i][j]);
+                        acc[i][j] = fmaf(a[i].z, bq[j].z, acc[i][j]);
+                        acc[i][j] = fmaf(a[i].w, bq[j].w, acc[i][j]);
+                    }
+            }
+        }
+    }
+    __syncthreads();
+    if (computes) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) red[(m * 16 + i * 4 + j) * L + lane] = acc[i][j];
+    }
+    __syncthreads();
+    float* wsb = ws + (long long)s * d.O * (C + 1);
+    for (int e = tid; e < NM * 16; e += kDwThreads) {
+        const int mm = e / 16, i = (e / 4) % 4, j = e % 4;
+        float v = 0.0f;
+        for (int l = 0; l < L; ++l) v += red[e * L + l];
+        const int k = 4 * (mm / (kNJ / 4)) + i;
+        const int jj = 4 * (mm % (kNJ / 4)) + j;
+        if (k >= K2) continue;
+        const long long o = (long long)(di * C + c) * K2 + k;
+        if (jj < 64) {
+            if (j0 + jj < C) wsb[o * (C + 1) + j0 + jj] = v;
+        } else if (jj == 64 && jt == 0) {
+            wsb[o * (C + 1) + C] = v;
+        }
+    }
+}
+
+// Sum the partials in split order; cast to the gradient dtype.
+template <typename T>
+__global__ void __launch_bounds__(256) dw_reduce_kernel(Dims d, const float* __restrict__ ws, int S,
+                                                        T* __restrict__ dw, T* __restrict__ db) {
+    const long long n = d.O * (d.C + 1);
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (long long)gridDim.x * blockDim.x) {
+        float v = 0.0f;
+        for (int s = 0; s < S; ++s) v += ws[(long long)s * n + e];
+        const long long o = e / (d.C + 1);
+        const int j = (int)(e % (d.C + 1));
+        if (j < d.C) dw[o * d.C + j] = from_f<T>(v);
+        else if (db != nullptr) db[o] = from_f<T>(v);
+    }
+}
+
+long long split_chunk(const Dims& d, int S) {
+    const long long NP = (long long)d.B * d.HW;
+    long long chunk = (NP + S - 1) / S;
+    return (chunk + kPT - 1) / kPT * kPT;
+}
+
+template <typename T, int K>
+cudaError_t launch_k(const Dims& d, const void* g, const void* x, const void* y, const void* w,
+                     const void* bias, void* dx, void* dy, void* dw, void* db, void* ws, cudaStream_t s) {
+    const unsigned pix_blocks = (unsigned)((d.HW + kThreads - 1) / kThreads);
+    {
+        const size_t smem = sizeof(float) * (size_t)d.C * kCG;
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(dx_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        dim3 grid(pix_blocks, (unsigned)((d.C + kCG - 1) / kCG), (unsigned)d.B);
+        trace_begin(s, kKBwdDxSimt);
+        dx_kernel<T, K><<<grid, kThreads, smem, s>>>(d, (const T*)g, (const T*)y, (const T*)w, (const T*)bias, (T*)dx);
+        trace_end(s);
+    }
+    {
+        dim3 grid(pix_blocks, (unsigned)((d.C + kJC - 1) / kJC), (unsigned)d.B);
+        trace_begin(s, kKBwdDySimt);
+        dy_kernel<T, K><<<grid, kThreads, 0, s>>>(d, (const T*)g, (const T*)x, (const T*)w, (T*)dy);
+        trace_end(s);
+    }
+    const int S = backward_num_splits(d);
+    {
+        const int JT = (d.C + 63) / 64;
+        dim3 grid((unsigned)d.C, (unsigned)(3 * JT), (unsigned)S);
+        trace_begin(s, kKBwdDwPartialSimt);
+        dw_partial_kernel<T, K><<<grid, kDwThreads, 0, s>>>(d, (const T*)g, (const T*)x, (const T*)y, (float*)ws,
+                                                            split_chunk(d, S));
+        trace_end(s);
+    }
+    {
+        const long long n = d.O * (d.C + 1);
+        long long blocks = (n + 255) / 256;
+        if (blocks > 152 * 32) blocks = 152 * 32;
+        trace_begin(s, kKBwdDwReduce);
+        dw_reduce_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(d, (const float*)ws, S, (T*)dw, (T*)db);
+        trace_end(s);
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(const Dims& d, const void* g, const void* x, const void* y, const void* w,
+                     const void* bias, void* dx, void* dy, void* dw, void* db, void* ws, cudaStream_t s) {
+    switch (d.K) {
+        case 1: return launch_k<T, 1>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
+        case 3: return launch_k<T, 3>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
+        case 5: return launch_k<T, 5>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
+        case 7: return launch_k<T, 7>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+int backward_num_splits(const Dims& d) {
+    const long long NP = (long long)d.B * d.HW;
+    long long S = (NP + 2047) / 2048;
+    if (S < 1) S = 1;
+    if (S > kMaxSplits) S = kMaxSplits;
+    return (int)S;
+}
+
+size_t backward_simt_workspace(const Dims& d) {
+    return sizeof(float) * (size_t)backward_num_splits(d) * (size_t)d.O * (size_t)(d.C + 1);
+}
+
+cudaError_t launch_backward_simt(const Dims& d, const void* g, const void* x, const void* y, const void* w,
+                                 const void* bias, void* dx, void* dy, void* dw, void* db, void* ws,
+                                 cudaStream_t s) {
+    if (d.dtype == 1) return launch_t<__nv_bfloat16>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
+    return launch_t<float>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
+}
+
+}  // namespace ddpm

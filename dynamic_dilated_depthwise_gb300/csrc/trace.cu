@@ -1,0 +1,106 @@
+// trace.cu -- optional per-kernel device timing (ddpm_trace_enable / ddpm_trace_read).
+//
+// While tracing is on, each launch site calls trace_begin / trace_end, which
+// record a pair of CUDA events on the launching stream.  Events come from a
+// pool that is reused across reads, so steady-state tracing creates nothing.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/ddpm.h"
+#include "launch.h"
+
+namespace ddpm {
+namespace {
+
+struct Record {
+    int id;
+    cudaEvent_t start, stop;
+};
+
+constexpr size_t kMaxRecords = 65536;
+
+std::atomic<bool> g_enabled{false};
+std::mutex g_mu;
+std::vector<Record> g_records;
+std::vector<cudaEvent_t> g_pool;
+bool g_open = false;  // a begin without its end yet
+
+cudaEvent_t take_event() {
+    if (!g_pool.empty()) {
+        cudaEvent_t e = g_pool.back();
+        g_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+const char* const kNames[kKNumKernels] = {
+    "filter_pregenerated_simt", "forward_simt", "forward_tc", "bwd_dx_simt", "bwd_dy_simt",
+    "bwd_dw_partial_simt", "bwd_dw_reduce", "bwd_dx_tc", "bwd_dydw_tc",
+};
+
+}  // namespace
+
+void trace_begin(cudaStream_t s, int kernel_id) {
+    if (!g_enabled.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_open = false;
+    if (g_records.size() >= kMaxRecords) return;
+    Record r{kernel_id, take_event(), take_event()};
+    if (r.start == nullptr || r.stop == nullptr || cudaEventRecord(r.start, s) != cudaSuccess) {
+        if (r.start) g_pool.push_back(r.start);
+        if (r.stop) g_pool.push_back(r.stop);
+        return;
+    }
+    g_records.push_back(r);
+    g_open = true;
+}
+
+void trace_end(cudaStream_t s) {
+    if (!g_enabled.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_open || g_records.empty()) return;
+    cudaEventRecord(g_records.back().stop, s);
+    g_open = false;
+}
+
+}  // namespace ddpm
+
+extern "C" {
+
+ddpm_status ddpm_trace_enable(int enable) {
+    ddpm::g_enabled.store(enable != 0);
+    return DDPM_OK;
+}
+
+int ddpm_trace_read(int* kernel_ids, float* milliseconds, int max_records) {
+    using namespace ddpm;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int n = 0;
+    int rc = 0;
+    for (const Record& r : g_records) {
+        float ms = -1.0f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+            rc = -1;
+        if (n < max_records && kernel_ids != nullptr && milliseconds != nullptr) {
+            kernel_ids[n] = r.id;
+            milliseconds[n] = ms;
+            ++n;
+        }
+        g_pool.push_back(r.start);
+        g_pool.push_back(r.stop);
+    }
+    g_records.clear();
+    g_open = false;
+    return rc < 0 ? -1 : n;
+}
+
+const char* ddpm_kernel_name(int kernel_id) {
+    if (kernel_id < 0 || kernel_id >= ddpm::kKNumKernels) return "unknown";
+    return ddpm::kNames[kernel_id];
+}
+
+}  // extern "C"

@@ -1,0 +1,169 @@
+/*
+ * ddpm.h -- C ABI of the GB300 (sm_103a) DDPM core library, libddpm_gb300.so.
+ *
+ * The Dynamic Dilated Pyramid Module core of HDFNet (ECCV 2020), as described
+ * in the "lartpang/DynamicConvolutionOperator" README:
+ *
+ *   taps  T[b,o,h,w] = bias[o] + sum_j weight[o,j] * y[b,j,h,w]      (1x1 generator)
+ *         with o = (di*C + c)*K*K + ky*K + kx, di indexing the three dilations;
+ *   out   [B,4C,H,W] = [x, d1, d3, d5], where
+ *         out[b,(1+di)*C+c,h,w] = sum_{ky,kx} T[b,o,h,w] * x[b,c,h+(ky-r)d,w+(kx-r)d],
+ *         r = K/2, d = dilations[di], x = 0 outside the image (Unfold semantics).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are dense, contiguous, NCHW (weight [O, C], bias [O]) with
+ *     O = 3*C*K*K, and all share the problem's dtype.
+ *   - Every pointer is a DEVICE pointer owned by the caller.  The library never
+ *     allocates, frees or synchronises; it enqueues kernels on `stream` (NULL =
+ *     the legacy default stream) and returns.  Inputs are read-only; outputs are
+ *     fully overwritten (no accumulation into them).  Outputs must not alias
+ *     inputs.
+ *   - Pointers must be aligned to the element size; 16-byte alignment enables
+ *     the vectorised paths but is not required.
+ *   - Arguments are validated on the host before anything is enqueued; on any
+ *     error nothing is enqueued.  A launch failure maps to DDPM_ERR_CUDA.
+ *     No C++ exception crosses this boundary.
+ *   - Reductions accumulate in FP32.  FP32 problems compute the forward with
+ *     IEEE FP32 FMA; BF16 problems round each generated tap to bf16 (round to
+ *     nearest even) before the filter uses it, as the page's precision policy
+ *     states (section "CUDA Flash 式融合训练", last paragraph).
+ */
+#ifndef DDPM_GB300_H
+#define DDPM_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__) || defined(__clang__)
+#define DDPM_API __attribute__((visibility("default")))
+#else
+#define DDPM_API
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t / CUstream; NULL selects the legacy default stream. */
+typedef struct CUstream_st* ddpm_stream_t;
+
+typedef enum {
+    DDPM_OK = 0,
+    DDPM_ERR_INVALID_ARGUMENT = 1,    /* bad shape, NULL pointer, even K, dilation < 1 ... */
+    DDPM_ERR_UNSUPPORTED = 2,         /* valid but outside what this build implements */
+    DDPM_ERR_MISALIGNED = 3,          /* a pointer is not aligned to its element size */
+    DDPM_ERR_WORKSPACE_TOO_SMALL = 4, /* ddpm_backward workspace below the queried size */
+    DDPM_ERR_CUDA = 5,                /* a CUDA runtime call or a launch failed */
+    DDPM_ERR_DEVICE_TIMEOUT = 6       /* a kernel's bounded wait expired (ddpm_get_device_error) */
+} ddpm_status;
+
+typedef enum { DDPM_FLOAT32 = 0, DDPM_BFLOAT16 = 1 } ddpm_dtype;
+
+/* Flags for ddpm_problem.flags.
+ * DDPM_FLAG_TF32_BACKWARD: FP32 problems may run the backward contractions on
+ *   TF32 tensor cores (the page allows TF32 for FP32 backward reductions and
+ *   recompute, never for the forward).  Ignored for BF16. */
+#define DDPM_FLAG_TF32_BACKWARD 0x1u
+
+typedef struct {
+    int B, C, H, W;    /* batch, channels, height, width: all >= 1 */
+    int K;             /* kernel size: odd, 1 <= K <= 7 */
+    int dilations[3];  /* the three pyramid dilations, each >= 1; (1,3,5) in the method */
+    int dtype;         /* a ddpm_dtype */
+    unsigned flags;    /* DDPM_FLAG_* bits */
+} ddpm_problem;
+
+/*
+ * ddpm_forward -- fused generator + dynamic dilated depthwise filter.
+ * Source: README section "CUDA 融合生成器推理" (fused generator inference:
+ * y tile -> dot(weight, y) -> dynamic taps -> consume with shifted x -> output;
+ * taps live only on chip) and "CUDA 动态过滤" (output [x, d1, d3, d5]).
+ *   x, y    [B, C, H, W]   inputs
+ *   weight  [O, C]         generator weight, O = 3*C*K*K
+ *   bias    [O] or NULL    generator bias (NULL = zero bias)
+ *   out     [B, 4C, H, W]  output; out[:, :C] is a bit-exact copy of x
+ * The taps are never written to global memory.
+ */
+DDPM_API ddpm_status ddpm_forward(const ddpm_problem* problem, const void* x, const void* y,
+                         const void* weight, const void* bias, void* out, ddpm_stream_t stream);
+
+/*
+ * ddpm_filter_pregenerated -- the dynamic filter alone, taps given.
+ * Source: README section "CUDA 动态过滤" (with the dynamic kernels already
+ * generated, one kernel handles dilations (1,3,5), reads the neighbourhood per
+ * spatial tile, accumulates in FP32 and writes [x, d1, d3, d5] without Unfold).
+ *   x     [B, C, H, W]
+ *   taps  [B, O, H, W]    channel o = (di*C + c)*K*K + ky*K + kx; used as given
+ *   out   [B, 4C, H, W]
+ */
+DDPM_API ddpm_status ddpm_filter_pregenerated(const ddpm_problem* problem, const void* x, const void* taps,
+                                     void* out, ddpm_stream_t stream);
+
+/*
+ * ddpm_backward_workspace_size -- bytes of device workspace ddpm_backward needs.
+ * Host only; enqueues nothing.  The workspace holds at most 16 FP32 partial
+ * sums of [O, C+1] (dW and dbias), per README section "CUDA Flash 式融合训练"
+ * (dWeight/dbias: split tokens into at most 16 FP32 partials, reduce them in a
+ * second short kernel) -- a few MiB, independent of the image size.
+ */
+DDPM_API ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* bytes);
+
+/*
+ * ddpm_backward -- gradients of L = <grad_out, out> for ddpm_forward.
+ * Source: README section "CUDA Flash 式融合训练":
+ *   dX : recompute the taps and gather each dilation's contribution
+ *        dx[b,c,q] = grad[b,c,q] + sum_{di,ky,kx} T[b,o,q-off] * grad[b,(1+di)C+c,q-off];
+ *   dY : form dK = shifted(x) * grad on chip and contract with the weight,
+ *        dy[b,j,p] = sum_o weight[o,j] * dK[b,o,p];
+ *   dW, dbias : spatial reductions of dK, dW[o,j] = sum_{b,p} dK[b,o,p] y[b,j,p],
+ *        dbias[o] = sum_{b,p} dK[b,o,p], via <= 16 FP32 partials + a reduce kernel.
+ * Taps are recomputed, never materialised.  In BF16 the tap rounding is
+ * straight-through (dx uses the rounded taps).
+ *   grad_out  [B, 4C, H, W]
+ *   x, y      [B, C, H, W];  weight [O, C];  bias [O] or NULL
+ *   dx, dy    [B, C, H, W]   outputs
+ *   dweight   [O, C]         output
+ *   dbias     [O] or NULL    output (NULL: not computed)
+ *   workspace device buffer of at least ddpm_backward_workspace_size() bytes,
+ *             16-byte aligned; its contents on entry do not matter
+ */
+DDPM_API ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, const void* x,
+                          const void* y, const void* weight, const void* bias, void* dx, void* dy,
+                          void* dweight, void* dbias, void* workspace, size_t workspace_bytes,
+                          ddpm_stream_t stream);
+
+/*
+ * ddpm_get_device_error -- synchronise `stream`, then report (and clear) the
+ * device-side error word that kernels set when a bounded wait expires.
+ * Returns DDPM_OK, DDPM_ERR_DEVICE_TIMEOUT or DDPM_ERR_CUDA.
+ */
+DDPM_API ddpm_status ddpm_get_device_error(ddpm_stream_t stream);
+
+/*
+ * Kernel tracing (profiling aid; off by default).
+ * While enabled, every kernel an entry point launches is bracketed by a pair of
+ * CUDA events recorded on the caller's stream, so per-kernel device time can be
+ * read back without a profiler.  Enabling creates CUDA events lazily (no device
+ * memory is allocated); at most 65536 records are kept, later ones are dropped.
+ *   ddpm_trace_enable(1|0)      switch tracing on or off (returns DDPM_OK)
+ *   ddpm_trace_read(ids, ms, n) wait for the recorded kernels, copy up to n
+ *                               (kernel id, milliseconds) pairs in launch order,
+ *                               clear the list; returns the number copied, or
+ *                               -1 on a CUDA error
+ *   ddpm_kernel_name(id)        name of a kernel id (never NULL)
+ */
+DDPM_API ddpm_status ddpm_trace_enable(int enable);
+DDPM_API int ddpm_trace_read(int* kernel_ids, float* milliseconds, int max_records);
+DDPM_API const char* ddpm_kernel_name(int kernel_id);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+DDPM_API const char* ddpm_status_string(ddpm_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+DDPM_API int ddpm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDPM_GB300_H */

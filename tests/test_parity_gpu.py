@@ -1,0 +1,233 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU FP64 oracle.
+
+Same seeded inputs on both sides (dynamic_dilated_depthwise_gb300.inputs).
+Small problems are compared element by element over whole tensors; the five
+workloads at full size are compared on sampled elements that the oracle
+evaluates one by one.  Integer-valued inputs make every intermediate exact,
+so addressing (tap order, offset signs, zero padding, tile tails) is checked
+bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dynamic_dilated_depthwise_gb300 import binding, build
+from dynamic_dilated_depthwise_gb300.inputs import (SEEDS, WORKLOADS, Problem, make_inputs,
+                                                    make_integer_inputs)
+from parity import assert_forward_close, assert_grad_close, sample_indices, to64
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["float32", "bfloat16"]
+
+SMALL = [
+    Problem(2, 24, 15, 17, 3),               # the regression shape: non-pow2 C, odd borders
+    Problem(1, 16, 9, 130, 3),               # rows wider than one 128-pixel tile, ragged
+    Problem(2, 40, 37, 45, 3),               # several tiles and a ragged tail, C % 16 != 0
+    Problem(1, 64, 32, 32, 3),               # C = 64 as in the main workloads
+    Problem(1, 8, 12, 11, 5),                # K = 5
+    Problem(2, 5, 6, 7, 1),                  # K = 1
+    Problem(1, 6, 13, 9, 7),                 # K = 7
+    Problem(1, 12, 20, 19, 3, (2, 2, 4)),    # other dilations
+    Problem(1, 3, 1, 1, 3),                  # 1x1 image: every neighbour is padding
+    Problem(3, 4, 2, 33, 3),                 # image thinner than the halo
+]
+
+
+def _id(p):
+    return f"B{p.B}C{p.C}_{p.H}x{p.W}_K{p.K}_d{''.join(map(str, p.dilations))}"
+
+
+@pytest.fixture(scope="session", autouse=True)
+def library():
+    build.build()
+    binding.load()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.init()
+
+
+def _dev(t):
+    return {k: v.cuda() for k, v in t.items()}
+
+
+def run_forward(d, p):
+    return binding.forward(d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations)
+
+
+def run_backward(d, p, flags=0):
+    return binding.backward(d["grad_out"], d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations, flags=flags)
+
+
+# ------------------------------------------------------------ small, full --
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", SMALL, ids=_id)
+def test_forward_matches_oracle(p, dtype):
+    h = make_inputs(p, 100, dtype)
+    d = _dev(h)
+    out = run_forward(d, p)
+    torch.cuda.synchronize()
+    ref = oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=dtype == "bfloat16")
+    assert_forward_close(out, ref, dtype)
+    assert torch.equal(out[:, :p.C].cpu(), h["x"]), "passthrough channels must be a bit-exact copy of x"
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", SMALL, ids=_id)
+def test_filter_pregenerated_matches_oracle(p, dtype):
+    h = make_inputs(p, 200, dtype, grad=False, taps=True)
+    d = _dev(h)
+    out = binding.filter_pregenerated(d["x"], d["taps"], p.K, p.dilations)
+    torch.cuda.synchronize()
+    ref = oracle.filter_pregenerated(h["x"], h["taps"], p.K, p.dilations)
+    assert_forward_close(out, ref, dtype)
+    assert torch.equal(out[:, :p.C].cpu(), h["x"])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", SMALL, ids=_id)
+def test_backward_matches_oracle(p, dtype):
+    h = make_inputs(p, 300, dtype)
+    d = _dev(h)
+    dx, dy, dw, db = run_backward(d, p, flags=binding.DDPM_FLAG_TF32_BACKWARD)
+    torch.cuda.synchronize()
+    ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations,
+                          bf16=dtype == "bfloat16")
+    for name, got, want in zip(("dx", "dy", "dW", "dbias"), (dx, dy, dw, db), ref):
+        assert_grad_close(got, want, dtype, name)
+
+
+# ----------------------------------------------------- integer, bit-exact --
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", [Problem(2, 24, 15, 17, 3), Problem(1, 16, 9, 130, 3), Problem(1, 8, 12, 11, 5),
+                               Problem(1, 12, 20, 19, 3, (2, 2, 4)), Problem(2, 5, 6, 7, 1),
+                               Problem(1, 64, 16, 24, 3)], ids=_id)
+def test_integer_inputs_bit_exact(p, dtype):
+    h = make_integer_inputs(p, 7, dtype, taps=True)
+    d = _dev(h)
+    bf = dtype == "bfloat16"
+    out = run_forward(d, p)
+    filt = binding.filter_pregenerated(d["x"], d["taps"], p.K, p.dilations)
+    dx, dy, dw, db = run_backward(d, p, flags=binding.DDPM_FLAG_TF32_BACKWARD)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to64(out), oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K,
+                                                            p.dilations, bf16=bf))
+    np.testing.assert_array_equal(to64(filt), oracle.filter_pregenerated(h["x"], h["taps"], p.K, p.dilations))
+    rdx, rdy, rdw, rdb = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K,
+                                         p.dilations, bf16=bf)
+    np.testing.assert_array_equal(to64(dx), rdx)
+    np.testing.assert_array_equal(to64(dy), rdy)
+    if not bf or p.B * p.H * p.W <= 256:   # bf16 holds every integer sum only up to 256
+        np.testing.assert_array_equal(to64(dw), rdw)
+        np.testing.assert_array_equal(to64(db), rdb)
+
+
+def test_integer_bf16_weight_grads_bit_exact_small_image():
+    p = Problem(1, 24, 15, 17, 3)             # 255 pixels: every dW / dbias sum stays <= 255
+    h = make_integer_inputs(p, 8, "bfloat16")
+    dx, dy, dw, db = run_backward(_dev(h), p)
+    torch.cuda.synchronize()
+    _, _, rdw, rdb = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations,
+                                     bf16=True)
+    np.testing.assert_array_equal(to64(dw), rdw)
+    np.testing.assert_array_equal(to64(db), rdb)
+
+
+# ------------------------------------------------------------ edge cases --
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_no_bias(dtype):
+    p = Problem(2, 24, 15, 17, 3)
+    h = make_inputs(p, 400, dtype)
+    d = _dev(h)
+    out = binding.forward(d["x"], d["y"], d["weight"], None, p.K, p.dilations)
+    dx, dy, dw, db = binding.backward(d["grad_out"], d["x"], d["y"], d["weight"], None, p.K, p.dilations,
+                                      with_dbias=False)
+    torch.cuda.synchronize()
+    bf = dtype == "bfloat16"
+    assert db is None
+    assert_forward_close(out, oracle.forward(h["x"], h["y"], h["weight"], None, p.K, p.dilations, bf16=bf), dtype)
+    ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], None, p.K, p.dilations, bf16=bf)
+    for name, got, want in zip(("dx", "dy", "dW"), (dx, dy, dw), ref[:3]):
+        assert_grad_close(got, want, dtype, name)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_backward_deterministic(dtype):
+    p = Problem(1, 64, 64, 64, 3)
+    d = _dev(make_inputs(p, 500, dtype))
+    a = run_backward(d, p)
+    b = run_backward(d, p)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v), "backward must be bit-reproducible run to run"
+
+
+def test_autograd_wrapper():
+    p = Problem(1, 8, 10, 12, 3)
+    h = make_inputs(p, 600, "float32")
+    d = {k: v.cuda().requires_grad_(k in ("x", "y", "weight", "bias")) for k, v in h.items()}
+    out = binding.DDPMCoreFunction.apply(d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations)
+    out.backward(d["grad_out"])
+    ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations)
+    for name, t, want in zip(("dx", "dy", "dW", "dbias"), ("x", "y", "weight", "bias"), ref):
+        assert_grad_close(d[t].grad, want, "float32", name)
+
+
+def test_device_error_word_is_clear():
+    p = Problem(1, 16, 8, 8, 3)
+    run_forward(_dev(make_inputs(p, 1, "bfloat16", grad=False)), p)
+    assert binding.ddpm_get_device_error() == 0
+
+
+# ------------------------------------------------ full-size, sampled checks --
+
+def _sampled_forward(p, h, out, dtype, fused=True):
+    idx = sample_indices(out.shape, 3000, 11)
+    bf = dtype == "bfloat16"
+    if fused:
+        ref = oracle.forward_points(h["x"], h["y"], h["weight"], h["bias"], p.K, idx, p.dilations, bf16=bf)
+    else:
+        ref = oracle.filter_points(h["x"], h["taps"], p.K, idx, p.dilations)
+    got = to64(out).reshape(-1)[idx]
+    assert_forward_close(got, ref, dtype)
+
+
+def _sampled_backward(p, h, grads, dtype):
+    bf = dtype == "bfloat16"
+    counts = {"dx": 1500, "dy": 1500, "dW": 150, "dbias": 100}
+    for (name, n), got in zip(counts.items(), grads):
+        arr = to64(got)
+        idx = sample_indices(arr.shape, n, 13, include_borders=name in ("dx", "dy"))
+        ref = oracle.backward_points(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, name, idx,
+                                     p.dilations, bf16=bf)
+        assert_grad_close(arr.reshape(-1)[idx], ref, dtype, name)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("name", ["b1_c64_128x128_k3", "b1_c64_128x128_k5"])
+def test_full_size_forward_and_filter(name, dtype):
+    p = WORKLOADS[name]
+    h = make_inputs(p, SEEDS[name], dtype, grad=False, taps=True)
+    d = _dev(h)
+    out = run_forward(d, p)
+    filt = binding.filter_pregenerated(d["x"], d["taps"], p.K, p.dilations)
+    torch.cuda.synchronize()
+    _sampled_forward(p, h, out, dtype, fused=True)
+    _sampled_forward(p, h, filt, dtype, fused=False)
+    assert torch.equal(out[:, :p.C].cpu(), h["x"])
+
+
+@pytest.mark.parametrize("name,dtype", [("b1_c64_256x256_k3", "bfloat16"), ("b1_c64_256x256_k3", "float32"),
+                                        ("b8_c64_256x256_k3", "bfloat16")])
+def test_full_size_training(name, dtype):
+    p = WORKLOADS[name]
+    h = make_inputs(p, SEEDS[name], dtype)
+    d = _dev(h)
+    out = run_forward(d, p)
+    grads = run_backward(d, p, flags=binding.DDPM_FLAG_TF32_BACKWARD)
+    torch.cuda.synchronize()
+    _sampled_forward(p, h, out, dtype)
+    _sampled_backward(p, h, grads, dtype)
