@@ -29,7 +29,7 @@ STATUS = {
 }
 EXPORTED = ("ddpm_forward", "ddpm_filter_pregenerated", "ddpm_backward_workspace_size", "ddpm_backward",
             "ddpm_get_device_error", "ddpm_status_string", "ddpm_version", "ddpm_trace_enable",
-            "ddpm_trace_read", "ddpm_kernel_name")
+            "ddpm_trace_read", "ddpm_kernel_name", "ddpm_backward_noalloc")
 
 
 class ddpm_problem(ctypes.Structure):
@@ -64,6 +64,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ddpm_backward_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
         lib.ddpm_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.ddpm_get_device_error.argtypes = [vp]
+        lib.ddpm_backward_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.ddpm_backward_noalloc.restype = ctypes.c_int
         lib.ddpm_status_string.argtypes = [ctypes.c_int]
         lib.ddpm_status_string.restype = ctypes.c_char_p
         lib.ddpm_version.argtypes = []
@@ -140,6 +142,14 @@ def ddpm_backward(problem, grad_out, x, y, weight, bias, dx, dy, dweight, dbias,
     _check(load().ddpm_backward(ctypes.byref(problem), _p(grad_out), _p(x), _p(y), _p(weight), _p(bias), _p(dx),
                                 _p(dy), _p(dweight), _p(dbias), _p(workspace), int(workspace_bytes),
                                 _stream(stream)), "ddpm_backward")
+
+
+def ddpm_backward_noalloc(problem, grad_out, x, y, weight, bias, dx, dy, dweight, dbias, stream=None) -> None:
+    """ddpm_backward with the library's own fixed scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/ddpm.h)."""
+    _check(load().ddpm_backward_noalloc(ctypes.byref(problem), _p(grad_out), _p(x), _p(y), _p(weight), _p(bias),
+                                        _p(dx), _p(dy), _p(dweight), _p(dbias), _stream(stream)),
+           "ddpm_backward_noalloc")
 
 
 def ddpm_get_device_error(stream=None) -> int:

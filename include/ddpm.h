@@ -132,6 +132,35 @@ DDPM_API ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad
                           void* dweight, void* dbias, void* workspace, size_t workspace_bytes,
                           ddpm_stream_t stream);
 
+/* Bytes of device scratch that ddpm_backward_noalloc keeps inside the library. */
+#define DDPM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * ddpm_backward_noalloc -- ddpm_backward without a caller-supplied workspace.
+ * The paper has no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory when they call the backward -- for example a
+ * plugin running inside an application that owns every device allocation, a
+ * real-time loop that forbids allocation after start-up, or a C caller with no
+ * allocator for temporary buffers.
+ *   Arguments and results are those of ddpm_backward, minus the workspace.
+ *   The FP32 dW/dbias partial sums live in a fixed device array of
+ *   DDPM_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library; every GPU that loads
+ *   the library holds it until the process exits.  Problems whose partials
+ *   need more (ddpm_backward_workspace_size() > DDPM_NOALLOC_SCRATCH_BYTES,
+ *   e.g. C=64 with K=5) are rejected with DDPM_ERR_UNSUPPORTED before anything
+ *   is enqueued; C=64, K=3 needs 7.2 MB at any image size.
+ *   No device memory is allocated or freed.  The first call on each device looks
+ *   up the array's device address (cudaGetSymbolAddress with that device
+ *   current); make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents (no
+ *   slot needs to start at zero: each call overwrites every slot it reads).
+ *   Calls that overlap on the GPU -- on different streams or from different
+ *   host threads on one device -- race on the array and give wrong results.
+ */
+DDPM_API ddpm_status ddpm_backward_noalloc(const ddpm_problem* problem, const void* grad_out, const void* x,
+                                          const void* y, const void* weight, const void* bias, void* dx,
+                                          void* dy, void* dweight, void* dbias, ddpm_stream_t stream);
+
 /*
  * ddpm_get_device_error -- synchronise `stream`, then report (and clear) the
  * device-side error word that kernels set when a bounded wait expires.
