@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libddpm_gb300.so")
 DDPM_FLOAT32 = 0
 DDPM_BFLOAT16 = 1
 DDPM_FLAG_TF32_BACKWARD = 0x1
+DDPM_FLAG_CUDA_CORES = 0x2
 
 STATUS = {
     0: "DDPM_OK", 1: "DDPM_ERR_INVALID_ARGUMENT", 2: "DDPM_ERR_UNSUPPORTED", 3: "DDPM_ERR_MISALIGNED",
@@ -200,13 +201,13 @@ def _same(x, *ts):
             raise ValueError("tensors must be contiguous and on the same CUDA device")
 
 
-def forward(x, y, weight, bias, K, dilations=(1, 3, 5), out=None, stream=None):
+def forward(x, y, weight, bias, K, dilations=(1, 3, 5), out=None, stream=None, flags=0):
     """[x, d1, d3, d5] = DDPM core forward; returns out [B, 4C, H, W]."""
     _same(x, y, weight, bias)
     B, C, H, W = x.shape
     if out is None:
         out = torch.empty((B, 4 * C, H, W), dtype=x.dtype, device=x.device)
-    ddpm_forward(_problem_of(x, K, dilations), x, y, weight, bias, out, stream)
+    ddpm_forward(_problem_of(x, K, dilations, flags), x, y, weight, bias, out, stream)
     return out
 
 

@@ -30,6 +30,20 @@ unsigned int* device_error_word() {
     return addr[dev];
 }
 
+int num_sms() {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 }  // namespace ddpm
 
 namespace {
@@ -47,7 +61,7 @@ ddpm_status validate(const ddpm_problem* p, Dims* d) {
     if (p->dtype != DDPM_FLOAT32 && p->dtype != DDPM_BFLOAT16) return DDPM_ERR_INVALID_ARGUMENT;
     for (int i = 0; i < 3; ++i)
         if (p->dilations[i] < 1) return DDPM_ERR_INVALID_ARGUMENT;
-    if ((p->flags & ~DDPM_FLAG_TF32_BACKWARD) != 0) return DDPM_ERR_INVALID_ARGUMENT;
+    if ((p->flags & ~(DDPM_FLAG_TF32_BACKWARD | DDPM_FLAG_CUDA_CORES)) != 0) return DDPM_ERR_INVALID_ARGUMENT;
     if (p->K > 7) return DDPM_ERR_UNSUPPORTED;
     // grid-dimension and index-width limits of this build
     if (p->B > 65535 || p->C > 65535) return DDPM_ERR_UNSUPPORTED;
@@ -101,6 +115,8 @@ ddpm_status ddpm_forward(const ddpm_problem* problem, const void* x, const void*
     DDPM_TRY(check_ptr(bias, es, true));
     DDPM_TRY(check_ptr(out, es, false));
     try {
+        if (ddpm::forward_tc_eligible(d, y, weight))
+            return from_cuda(ddpm::launch_forward_tc(d, x, y, weight, bias, out, (cudaStream_t)stream));
         return from_cuda(ddpm::launch_forward_simt(d, x, y, weight, bias, out, (cudaStream_t)stream));
     } catch (...) {
         return DDPM_ERR_CUDA;

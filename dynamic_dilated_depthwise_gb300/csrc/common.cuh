@@ -19,6 +19,12 @@ struct Dims {
     unsigned flags;
     long long HW;            // H * W
     long long O;             // 3 * C * K * K
+
+    __host__ __device__ int R() const {  // halo radius: largest dilation * (K / 2)
+        int m = dil[0] > dil[1] ? dil[0] : dil[1];
+        m = m > dil[2] ? m : dil[2];
+        return m * r;
+    }
 };
 
 // ---- element conversions -------------------------------------------------

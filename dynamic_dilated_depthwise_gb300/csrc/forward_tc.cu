@@ -1,0 +1,423 @@
+// forward_tc.cu -- fused generator + dynamic filter on tcgen05 tensor cores (bf16).
+//
+// README "lartpang/DynamicConvolutionOperator", section "CUDA 融合生成器推理":
+//   y tile -> dot(weight, y) -> dynamic taps -> consume with shifted x -> output,
+// with the taps living only on chip; BF16 taps are rounded to bf16 before use.
+//
+// GB300 design.  A persistent CTA owns one group of 16 output channels and
+// walks pixel tiles of 128 pixels (one row segment, or several whole rows when
+// W < 128).  Per tile and dilation d the generator GEMM is
+//   D[p, n] = sum_j y[j, p] * W[o_n, j] + bias[o_n],  n = c_local*9 + k  (144 columns)
+// issued as tcgen05.mma (M = 128 pixels, N = 144, K = 64 in four K=16 steps,
+// plus one K=16 step that adds the bias through a ones column) into TMEM:
+// TMEM lane = pixel, so each epilogue thread owns every tap of its pixel and
+// filters without any cross-thread reduction.
+//
+//   warp 0      TMA producer: W slice of the group (once), y tiles (2 stages)
+//   warp 1      TMEM owner + MMA issuer (one elected lane)
+//   warps 2..9  epilogue: stage the x window (fp32, position-major), read the
+//               taps from TMEM, round to bf16, multiply by shifted x, store.
+// Three TMEM regions (one per dilation, 144 columns each) form the pipeline:
+// the MMA of tile i+1 / dilation d starts as soon as the epilogue has drained
+// region d of tile i.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "tc.cuh"
+
+namespace ddpm {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kCG = 16;                  // output channels per CTA group
+constexpr int kTaps = 9;                 // K = 3
+constexpr int kN = kCG * kTaps;          // 144 MMA columns per dilation
+constexpr int kTile = 128;               // pixels per tile (MMA M)
+constexpr int kKPad = 64;                // generator K (channels of y), zero padded
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kWinMax = 1536;            // x window positions (fits R = 5 at TW = 128)
+
+// shared-memory carve-up (bytes, from a 1024-aligned base).  The two 128-byte
+// swizzled operands come first so that every swizzle atom starts on 1024 B.
+constexpr int kSW = 0;                                 // W slice, 3 x [144 x 128 B], SW128 K-major
+constexpr int kSWBytes = 3 * kN * 128;                 // 55296 = 54 KiB
+constexpr int kSY = kSW + kSWBytes;                    // y tiles, 2 x [64 j x 128 px] SW128 MN-major
+constexpr int kSYBytes = 2 * kTile * kKPad * 2;        // 32768
+constexpr int kSBias = kSY + kSYBytes;                 // bias B operand, 3 x [144 x 16] no swizzle
+constexpr int kSBiasBytes = 3 * kN * 32;               // 13824
+constexpr int kSOnes = kSBias + kSBiasBytes;           // ones A operand [128 x 16] no swizzle
+constexpr int kSOnesBytes = kTile * 32;                // 4096
+constexpr int kSX = kSOnes + kSOnesBytes;              // x window, [pos][16] fp32
+constexpr int kSXBytes = kWinMax * kCG * 4;            // 98304
+constexpr int kSmemBytes = kSX + kSXBytes + 1024;      // + alignment slack
+static_assert(kSW % 1024 == 0 && kSY % 1024 == 0 && (kSY + kSYBytes / 2) % 1024 == 0, "SW128 atoms need 1 KiB");
+static_assert(kSBias % 16 == 0 && kSOnes % 16 == 0 && kSX % 16 == 0, "16-byte aligned operands");
+
+struct FwdTcParams {
+    Dims d;
+    int TH, TW;            // tile rows / columns (TH * TW <= 128)
+    int tiles_per_row;     // W >= 128: ceil(W / 128); else 1
+    int tiles_per_img;
+    int n_tiles;           // B * tiles_per_img
+    int n_groups;          // ceil(C / 16)
+    int ctas_per_group;
+    int R;                 // halo radius = max dilation * (K / 2)
+    int WH, WW;            // x window rows / columns
+    const bf16* x;
+    const bf16* bias;      // may be null
+    bf16* out;
+    unsigned int* err;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
+
+// x window slot of (position, float4 group j): the group index is rotated by
+// (pos >> 1) & 3 so that 8 consecutive positions hit 8 distinct bank quads.
+__device__ __forceinline__ int xw_index(int pos, int j) { return pos * kCG + (((j + (pos >> 1)) & 3) << 2); }
+
+struct TileCoord {
+    int b, h0, w0, nvalid;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const FwdTcParams& P, int t) {
+    TileCoord c;
+    c.b = t / P.tiles_per_img;
+    const int ti = t % P.tiles_per_img;
+    if (P.TH == 1) {
+        c.h0 = ti / P.tiles_per_row;
+        c.w0 = (ti % P.tiles_per_row) * P.TW;
+        c.nvalid = min(P.TW, P.d.W - c.w0);
+    } else {
+        c.h0 = ti * P.TH;
+        c.w0 = 0;
+        c.nvalid = P.TW * min(P.TH, P.d.H - c.h0);
+    }
+    return c;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    forward_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmW,
+                      const FwdTcParams P) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* sX = reinterpret_cast<float*>(sm + kSX);
+    __shared__ uint64_t bar_w, bar_y_full[2], bar_y_empty[2], bar_acc_full[3], bar_acc_empty[3], bar_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = blockIdx.x % P.n_groups;
+    const int cta_in_group = blockIdx.x / P.n_groups;
+    const int c0 = group * kCG;
+    const int C = P.d.C;
+    const long long HW = P.d.HW;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar_w, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar_y_full[s], 1);
+            mbar_init(&bar_y_empty[s], 1);
+        }
+        for (int dd = 0; dd < 3; ++dd) {
+            mbar_init(&bar_acc_full[dd], 1);
+            mbar_init(&bar_acc_empty[dd], kEpiWarps);
+        }
+        mbar_init(&bar_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_slot, 512);
+    if (warp >= 2) {
+        // constant MMA operands: a ones column (A) and the bias column (B), K = 16, no swizzle
+        const int et = threadIdx.x - 64;
+        for (int i = et; i < kTile * 16; i += 32 * kEpiWarps) {
+            const int m = i / 16, k = i % 16;
+            *reinterpret_cast<bf16*>(sm + kSOnes + (m / 8) * 256 + (k / 8) * 128 + (m % 8) * 16 + (k % 8) * 2) =
+                __float2bfloat16(k == 0 ? 1.0f : 0.0f);
+        }
+        for (int i = et; i < 3 * kN * 16; i += 32 * kEpiWarps) {
+            const int dd = i / (kN * 16), rem = i % (kN * 16), n = rem / 16, k = rem % 16;
+            const long long o = (long long)(dd * C + c0) * kTaps + n;
+            bf16 v = __float2bfloat16(0.0f);
+            if (k == 0 && P.bias != nullptr && o < P.d.O) v = P.bias[o];
+            *reinterpret_cast<bf16*>(sm + kSBias + dd * kN * 32 + (n / 8) * 256 + (k / 8) * 128 + (n % 8) * 16 +
+                                     (k % 8) * 2) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const int n_my = cta_in_group < P.n_tiles ? (P.n_tiles - 1 - cta_in_group) / P.ctas_per_group + 1 : 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmY);
+            prefetch_tmap(&tmW);
+            mbar_arrive_expect_tx(&bar_w, 3 * kN * 128);
+            for (int dd = 0; dd < 3; ++dd)
+                tma_load_2d(sm + kSW + dd * kN * 128, &tmW, &bar_w, 0, (dd * C + c0) * kTaps);
+            int issued = 0;
+            for (int i = 0; i < n_my; ++i) {
+                const int s = i & 1, ph = (i >> 1) & 1;
+                if (!mbar_wait(&bar_y_empty[s], ph ^ 1, P.err, abort_v)) break;
+                const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
+                const int pb = tcd.h0 * P.d.W + tcd.w0;
+                mbar_arrive_expect_tx(&bar_y_full[s], kTile * kKPad * 2);
+                tma_load_3d(sm + kSY + s * 16384, &tmY, &bar_y_full[s], pb, 0, tcd.b);
+                tma_load_3d(sm + kSY + s * 16384 + 8192, &tmY, &bar_y_full[s], pb + 64, 0, tcd.b);
+                issued = i + 1;
+            }
+            // drain: every copy this CTA started must land before its shared memory is released
+            int never = 0;
+            mbar_wait(&bar_w, 0, P.err, &never);
+            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+                mbar_wait(&bar_y_full[i & 1], (i >> 1) & 1, P.err, &never);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(&bar_w, 0, P.err, abort_v);
+            const uint32_t idesc = instr_desc(1, 1, 0, kTile, kN);     // A (y) MN-major, B (W) K-major
+            const uint32_t idesc_b = instr_desc(1, 0, 0, kTile, kN);   // ones x bias, both K-major
+            const uint64_t d_ones = smem_desc(smem_u32(sm + kSOnes), 128, 256, kSwizzleNone);
+            for (int i = 0; ok && i < n_my; ++i) {
+                const int s = i & 1, ph = (i >> 1) & 1;
+                if (!mbar_wait(&bar_y_full[s], ph, P.err, abort_v)) break;
+                tc_fence_after();
+                const uint32_t ya = smem_u32(sm + kSY + s * 16384);
+                for (int dd = 0; dd < 3 && ok; ++dd) {
+                    if (!mbar_wait(&bar_acc_empty[dd], (i & 1) ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t dt = tmem + dd * kN;
+                    const uint32_t wa = smem_u32(sm + kSW + dd * kN * 128);
+#pragma unroll
+                    for (int kk = 0; kk < kKPad / 16; ++kk)
+                        mma_f16(dt, smem_desc(ya + kk * 2048, 8192, 1024, kSwizzle128B),
+                                smem_desc(wa + kk * 32, 16, 1024, kSwizzle128B), idesc, kk > 0);
+                    mma_f16(dt, d_ones, smem_desc(smem_u32(sm + kSBias + dd * kN * 32), 128, 256, kSwizzleNone),
+                            idesc_b, 1);
+                    mma_commit(&bar_acc_full[dd]);
+                }
+                if (!ok) break;
+                mma_commit(&bar_y_empty[s]);
+            }
+            // all issued MMAs must retire before TMEM is released
+            mma_commit(&bar_done);
+            int never = 0;
+            mbar_wait(&bar_done, 0, P.err, &never);
+        }
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int ew = warp - 2;
+        const int q = warp & 3;          // TMEM lane quadrant this warp may access
+        const int g = ew >> 2;           // channel half: c_local in [8g, 8g+8)
+        const int s = q * 32 + lane;     // pixel slot == TMEM lane
+        const int et = threadIdx.x - 64;
+        const bool slot_in_tile = s < P.TH * P.TW;
+        const int rr = slot_in_tile ? s / P.TW : 0;
+        const int cc = slot_in_tile ? s % P.TW : 0;
+        const int R = P.R, WW = P.WW;
+        const int npos = P.WH * P.WW;
+        for (int i = 0; i < n_my; ++i) {
+            const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
+            epi_bar();  // the previous tile's window is no longer read
+            const bf16* xb = P.x + ((long long)tcd.b * C + c0) * HW;
+            for (int pos = et; pos < npos; pos += 32 * kEpiWarps) {
+                const int wr = pos / WW, wc = pos % WW;
+                const int h = tcd.h0 - R + wr, w = tcd.w0 - R + wc;
+                const bool inside = h >= 0 && h < P.d.H && w >= 0 && w < P.d.W;
+                float v[kCG];
+#pragma unroll
+                for (int c = 0; c < kCG; ++c)
+                    v[c] = (inside && c0 + c < C) ? __bfloat162float(xb[(long long)c * HW + (long long)h * P.d.W + w])
+                                                  : 0.0f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<float4*>(sX + xw_index(pos, j)) =
+                        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+            epi_bar();  // window ready
+            const bool valid = s < tcd.nvalid;
+            const long long p = (long long)(tcd.h0 + rr) * P.d.W + tcd.w0 + cc;
+            bf16* ob = P.out + (long long)tcd.b * 4 * C * HW;
+            if (valid) {
+                const int cpos = (rr + R) * WW + cc + R;
+#pragma unroll
+                for (int cl = 0; cl < 8; ++cl) {
+                    const int c = 8 * g + cl;
+                    if (c0 + c < C)
+                        ob[(long long)(c0 + c) * HW + p] =
+                            __float2bfloat16(sX[xw_index(cpos, c >> 2) + (c & 3)]);
+                }
+            }
+            for (int dd = 0; dd < 3; ++dd) {
+                if (!mbar_wait(&bar_acc_full[dd], i & 1, P.err, abort_v)) goto epilogue_done;
+                tc_fence_after();
+                uint32_t t[72];
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + dd * kN + g * 72;
+                DDPM_TMEM_LD_X16(ta, (t + 0));
+                DDPM_TMEM_LD_X16(ta + 16, (t + 16));
+                DDPM_TMEM_LD_X16(ta + 32, (t + 32));
+                DDPM_TMEM_LD_X16(ta + 48, (t + 48));
+                DDPM_TMEM_LD_X8(ta + 64, (t + 64));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_acc_empty[dd]);
+                if (valid) {
+                    const int dil = dil_of(P.d, dd);
+                    float acc[8];
+#pragma unroll
+                    for (int cl = 0; cl < 8; ++cl) acc[cl] = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < kTaps; ++k) {
+                        const int ky = k / 3, kx = k % 3;
+                        const int pos = (rr + R + (ky - 1) * dil) * WW + cc + R + (kx - 1) * dil;
+                        const float4 xa = *reinterpret_cast<const float4*>(sX + xw_index(pos, 2 * g));
+                        const float4 xc = *reinterpret_cast<const float4*>(sX + xw_index(pos, 2 * g + 1));
+                        const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
+#pragma unroll
+                        for (int cl = 0; cl < 8; ++cl) {
+                            const float tq = __bfloat162float(__float2bfloat16_rn(__uint_as_float(t[cl * kTaps + k])));
+                            acc[cl] = fmaf(tq, xv[cl], acc[cl]);
+                        }
+                    }
+#pragma unroll
+                    for (int cl = 0; cl < 8; ++cl) {
+                        const int c = c0 + 8 * g + cl;
+                        if (c < C) ob[(long long)((1 + dd) * C + c) * HW + p] = __float2bfloat16_rn(acc[cl]);
+                    }
+                }
+            }
+        }
+    epilogue_done:;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+struct Tiling {
+    int TH, TW, tiles_per_row, tiles_per_img, R, WH, WW;
+};
+
+Tiling tiling_of(const Dims& d) {
+    Tiling t;
+    if (d.W >= kTile) {
+        t.TW = kTile;
+        t.TH = 1;
+        t.tiles_per_row = (d.W + kTile - 1) / kTile;
+        t.tiles_per_img = d.H * t.tiles_per_row;
+    } else {
+        t.TW = d.W;
+        t.TH = kTile / d.W < d.H ? kTile / d.W : d.H;
+        t.tiles_per_row = 1;
+        t.tiles_per_img = (d.H + t.TH - 1) / t.TH;
+    }
+    const int maxdil = d.dil[0] > d.dil[1] ? (d.dil[0] > d.dil[2] ? d.dil[0] : d.dil[2])
+                                           : (d.dil[1] > d.dil[2] ? d.dil[1] : d.dil[2]);
+    t.R = maxdil * (d.K / 2);
+    t.WH = t.TH + 2 * t.R;
+    t.WW = t.TW + 2 * t.R;
+    return t;
+}
+
+}  // namespace
+
+bool forward_tc_eligible(const Dims& d, const void* y, const void* w) {
+    if (d.dtype != 1 || d.K != 3 || (d.flags & kFlagCudaCores)) return false;
+    if (d.C % 8 != 0 || d.C > kKPad) return false;      // TMA row stride of W; one 64-wide K block
+    if (d.W % 8 != 0) return false;                     // every tile start is a 16-byte TMA coordinate
+    if ((uintptr_t)y % 16 != 0 || (uintptr_t)w % 16 != 0) return false;
+    if (d.R() > 1024) return false;
+    const Tiling t = tiling_of(d);
+    if ((long long)t.WH * t.WW > kWinMax) return false;
+    const long long tiles = (long long)d.B * t.tiles_per_img;
+    if (tiles > (1LL << 30) || d.O > (1LL << 30) || d.HW > (1LL << 31) - 1024) return false;
+    return encode_fn() != nullptr;
+}
+
+cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const void* w, const void* bias,
+                              void* out, cudaStream_t s) {
+    static int attr_done = 0;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(forward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = 1;
+    }
+    auto enc = encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    CUtensorMap tmY, tmW;
+    const cuuint64_t dimY[3] = {(cuuint64_t)d.HW, (cuuint64_t)d.C, (cuuint64_t)d.B};
+    const cuuint64_t strY[2] = {(cuuint64_t)d.HW * 2, (cuuint64_t)d.HW * d.C * 2};
+    const cuuint32_t boxY[3] = {64, (cuuint32_t)kKPad, 1};
+    const cuuint32_t one3[3] = {1, 1, 1};
+    if (enc(&tmY, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(y), dimY, strY, boxY, one3,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const cuuint64_t dimW[2] = {(cuuint64_t)d.C, (cuuint64_t)d.O};
+    const cuuint64_t strW[1] = {(cuuint64_t)d.C * 2};
+    const cuuint32_t boxW[2] = {(cuuint32_t)kKPad, (cuuint32_t)kN};
+    const cuuint32_t one2[2] = {1, 1};
+    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dimW, strW, boxW, one2,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    const Tiling t = tiling_of(d);
+    FwdTcParams P;
+    P.d = d;
+    P.TH = t.TH;
+    P.TW = t.TW;
+    P.tiles_per_row = t.tiles_per_row;
+    P.tiles_per_img = t.tiles_per_img;
+    P.n_tiles = d.B * t.tiles_per_img;
+    P.n_groups = (d.C + kCG - 1) / kCG;
+    const int sms = num_sms();
+    int cpg = sms / P.n_groups;
+    if (cpg < 1) cpg = 1;
+    if (cpg > P.n_tiles) cpg = P.n_tiles;
+    P.ctas_per_group = cpg;
+    P.R = t.R;
+    P.WH = t.WH;
+    P.WW = t.WW;
+    P.x = static_cast<const bf16*>(x);
+    P.bias = static_cast<const bf16*>(bias);
+    P.out = static_cast<bf16*>(out);
+    P.err = device_error_word();
+    if (P.err == nullptr) return cudaErrorUnknown;
+    trace_begin(s, kKForwardTc);
+    forward_tc_kernel<<<P.n_groups * cpg, kThreads, kSmemBytes, s>>>(tmY, tmW, P);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace ddpm

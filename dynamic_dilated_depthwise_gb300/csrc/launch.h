@@ -27,6 +27,12 @@ enum KernelId : int {
 void trace_begin(cudaStream_t s, int kernel_id);
 void trace_end(cudaStream_t s);
 
+// ddpm_problem.flags bit that forces the CUDA-core kernels (DDPM_FLAG_CUDA_CORES).
+constexpr unsigned kFlagCudaCores = 0x2u;
+
+// Multiprocessor count of the current device (cached per device).
+int num_sms();
+
 // Device address of the library's error word (set by kernels whose bounded
 // waits expire).
 unsigned int* device_error_word();
@@ -38,6 +44,11 @@ cudaError_t launch_filter_simt(const Dims& d, const void* x, const void* taps, v
 // Fused generator + filter on CUDA cores (IEEE FP32 FMA; also any dtype/shape).
 cudaError_t launch_forward_simt(const Dims& d, const void* x, const void* y, const void* w,
                                 const void* bias, void* out, cudaStream_t s);
+
+// Fused generator + filter on tcgen05 tensor cores (bf16, K = 3, C <= 64).
+bool forward_tc_eligible(const Dims& d, const void* y, const void* w);
+cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const void* w,
+                              const void* bias, void* out, cudaStream_t s);
 
 // Backward on CUDA cores: dX gather, dY, dW/dbias split partials + reduce.
 size_t backward_simt_workspace(const Dims& d);

@@ -64,6 +64,9 @@ typedef enum { DDPM_FLOAT32 = 0, DDPM_BFLOAT16 = 1 } ddpm_dtype;
  *   TF32 tensor cores (the page allows TF32 for FP32 backward reductions and
  *   recompute, never for the forward).  Ignored for BF16. */
 #define DDPM_FLAG_TF32_BACKWARD 0x1u
+/* DDPM_FLAG_CUDA_CORES: run the CUDA-core (FFMA) kernels even where a
+ *   tensor-core kernel exists for the problem (BF16 forward / backward). */
+#define DDPM_FLAG_CUDA_CORES 0x2u
 
 typedef struct {
     int B, C, H, W;    /* batch, channels, height, width: all >= 1 */

@@ -35,6 +35,19 @@ SMALL = [
 ]
 
 
+# Shapes the tensor-core forward takes (bf16, K = 3, C % 8 == 0, C <= 64, W % 8 == 0):
+# ragged row tiles, partial channel groups, several rows per tile, H below the tile height.
+TC_SHAPES = [
+    Problem(1, 16, 5, 136, 3),               # W = 136: one full and one 8-pixel tile per row
+    Problem(2, 24, 10, 24, 3),               # C = 24: partial second channel group; 5 rows per tile
+    Problem(1, 48, 12, 256, 3),              # two tiles per row, three channel groups
+    Problem(1, 8, 3, 40, 3, (2, 2, 4)),      # C = 8, other dilations, image shorter than a tile
+    Problem(2, 64, 7, 200, 3),               # second tile of each row holds 72 pixels
+    Problem(1, 32, 1, 8, 3),                 # a single 8-pixel row
+    Problem(3, 64, 40, 40, 3),               # several images, 3 rows per tile
+]
+
+
 def _id(p):
     return f"B{p.B}C{p.C}_{p.H}x{p.W}_K{p.K}_d{''.join(map(str, p.dilations))}"
 
@@ -96,6 +109,64 @@ def test_backward_matches_oracle(p, dtype):
                           bf16=dtype == "bfloat16")
     for name, got, want in zip(("dx", "dy", "dW", "dbias"), (dx, dy, dw, db), ref):
         assert_grad_close(got, want, dtype, name)
+
+
+# ------------------------------------------------- tensor-core forward path --
+
+def _traced_kernels(fn):
+    binding.ddpm_trace_read()
+    binding.ddpm_trace_enable(True)
+    try:
+        fn()
+        torch.cuda.synchronize()
+    finally:
+        binding.ddpm_trace_enable(False)
+    return [name for name, _ in binding.ddpm_trace_read()]
+
+
+@pytest.mark.parametrize("p", TC_SHAPES, ids=_id)
+def test_tc_forward_matches_oracle_and_cuda_cores(p):
+    h = make_inputs(p, 700, "bfloat16", grad=False)
+    d = _dev(h)
+    names = _traced_kernels(lambda: run_forward(d, p))
+    assert names == ["forward_tc"], f"expected the tensor-core forward, got {names}"
+    out = run_forward(d, p)
+    simt = binding.forward(d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations,
+                           flags=binding.DDPM_FLAG_CUDA_CORES)
+    torch.cuda.synchronize()
+    ref = oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=True)
+    assert_forward_close(out, ref, "bfloat16")
+    assert_forward_close(simt, ref, "bfloat16")
+    assert torch.equal(out[:, :p.C].cpu(), h["x"])
+
+
+@pytest.mark.parametrize("p", TC_SHAPES[:5], ids=_id)
+def test_tc_forward_integer_bit_exact(p):
+    h = make_integer_inputs(p, 9, "bfloat16", grad=False)
+    out = run_forward(_dev(h), p)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to64(out), oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K,
+                                                            p.dilations, bf16=True))
+
+
+def test_tc_forward_without_bias():
+    p = Problem(1, 24, 6, 64, 3)
+    h = make_inputs(p, 701, "bfloat16", grad=False)
+    d = _dev(h)
+    out = binding.forward(d["x"], d["y"], d["weight"], None, p.K, p.dilations)
+    torch.cuda.synchronize()
+    assert_forward_close(out, oracle.forward(h["x"], h["y"], h["weight"], None, p.K, p.dilations, bf16=True),
+                         "bfloat16")
+
+
+def test_tc_forward_repeated_calls_identical():
+    p = Problem(1, 64, 64, 128, 3)
+    d = _dev(make_inputs(p, 702, "bfloat16", grad=False))
+    a = run_forward(d, p)
+    b = run_forward(d, p)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert binding.ddpm_get_device_error() == 0
 
 
 # ----------------------------------------------------- integer, bit-exact --
