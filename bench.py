@@ -78,10 +78,8 @@ def kernel_work(name: str, p, es: int, splits: int):
         return "alu", 2.0 * O * (C + 1) * P, "flops"
     if name == "bwd_dw_reduce":
         return "hbm", splits * O * (C + 1) * 4 + O * (C + 1) * es, "bytes"
-    if name in ("forward_tc", "bwd_dx_tc"):
+    if name in ("forward_tc", "bwd_dx_tc", "bwd_dy_tc", "bwd_dw_tc"):
         return "tensor", gemm, "flops"
-    if name == "bwd_dydw_tc":
-        return "tensor", 2 * gemm, "flops"
     return "unknown", 0.0, "flops"
 
 

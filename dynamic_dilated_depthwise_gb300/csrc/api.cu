@@ -164,8 +164,28 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
     DDPM_TRY(check_ptr(workspace, 16, false));
     if (workspace_bytes < ddpm::backward_simt_workspace(d)) return DDPM_ERR_WORKSPACE_TOO_SMALL;
     try {
-        return from_cuda(ddpm::launch_backward_simt(d, grad_out, x, y, weight, bias, dx, dy, dweight, dbias,
-                                                    workspace, (cudaStream_t)stream));
+        const cudaStream_t s = (cudaStream_t)stream;
+        // each piece runs on the tensor-core kernel where one exists for the problem
+        cudaError_t e = ddpm::launch_bwd_dx_simt(d, grad_out, y, weight, bias, dx, s);
+        if (e == cudaSuccess) {
+            if (ddpm::bwd_dy_tc_eligible(d, grad_out, x, weight))
+                e = ddpm::launch_bwd_dy_tc(d, grad_out, x, weight, dy, s);
+            else
+                e = ddpm::launch_bwd_dy_simt(d, grad_out, x, weight, dy, s);
+        }
+        if (e == cudaSuccess) {
+            if (ddpm::bwd_dw_tc_eligible(d, grad_out, x, y)) {
+                const int S = ddpm::bwd_dw_tc_splits(d, workspace_bytes);
+                e = ddpm::launch_bwd_dw_tc(d, grad_out, x, y, (float*)workspace, S, s);
+                if (e == cudaSuccess) e = ddpm::launch_bwd_reduce(d, (const float*)workspace, S, dweight, dbias, s);
+            } else {
+                e = ddpm::launch_bwd_dw_partial_simt(d, grad_out, x, y, workspace, s);
+                if (e == cudaSuccess)
+                    e = ddpm::launch_bwd_reduce(d, (const float*)workspace, ddpm::backward_num_splits(d), dweight,
+                                                dbias, s);
+            }
+        }
+        return from_cuda(e);
     } catch (...) {
         return DDPM_ERR_CUDA;
     }

@@ -313,54 +313,84 @@ long long split_chunk(const Dims& d, int S) {
 }
 
 template <typename T, int K>
-cudaError_t launch_k(const Dims& d, const void* g, const void* x, const void* y, const void* w,
-                     const void* bias, void* dx, void* dy, void* dw, void* db, void* ws, cudaStream_t s) {
+cudaError_t launch_dx_k(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
+                        cudaStream_t s) {
     const unsigned pix_blocks = (unsigned)((d.HW + kThreads - 1) / kThreads);
-    {
-        const size_t smem = sizeof(float) * (size_t)d.C * kCG;
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(dx_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-        }
-        dim3 grid(pix_blocks, (unsigned)((d.C + kCG - 1) / kCG), (unsigned)d.B);
-        trace_begin(s, kKBwdDxSimt);
-        dx_kernel<T, K><<<grid, kThreads, smem, s>>>(d, (const T*)g, (const T*)y, (const T*)w, (const T*)bias, (T*)dx);
-        trace_end(s);
+    const size_t smem = sizeof(float) * (size_t)d.C * kCG;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(dx_kernel<T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
     }
-    {
-        dim3 grid(pix_blocks, (unsigned)((d.C + kJC - 1) / kJC), (unsigned)d.B);
-        trace_begin(s, kKBwdDySimt);
-        dy_kernel<T, K><<<grid, kThreads, 0, s>>>(d, (const T*)g, (const T*)x, (const T*)w, (T*)dy);
-        trace_end(s);
-    }
+    dim3 grid(pix_blocks, (unsigned)((d.C + kCG - 1) / kCG), (unsigned)d.B);
+    trace_begin(s, kKBwdDxSimt);
+    dx_kernel<T, K><<<grid, kThreads, smem, s>>>(d, (const T*)g, (const T*)y, (const T*)w, (const T*)bias, (T*)dx);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+template <typename T, int K>
+cudaError_t launch_dy_k(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
+    const unsigned pix_blocks = (unsigned)((d.HW + kThreads - 1) / kThreads);
+    dim3 grid(pix_blocks, (unsigned)((d.C + kJC - 1) / kJC), (unsigned)d.B);
+    trace_begin(s, kKBwdDySimt);
+    dy_kernel<T, K><<<grid, kThreads, 0, s>>>(d, (const T*)g, (const T*)x, (const T*)w, (T*)dy);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+template <typename T, int K>
+cudaError_t launch_dw_k(const Dims& d, const void* g, const void* x, const void* y, void* ws, cudaStream_t s) {
     const int S = backward_num_splits(d);
-    {
-        const int JT = (d.C + 63) / 64;
-        dim3 grid((unsigned)d.C, (unsigned)(3 * JT), (unsigned)S);
-        trace_begin(s, kKBwdDwPartialSimt);
-        dw_partial_kernel<T, K><<<grid, kDwThreads, 0, s>>>(d, (const T*)g, (const T*)x, (const T*)y, (float*)ws,
-                                                            split_chunk(d, S));
-        trace_end(s);
-    }
-    {
-        const long long n = d.O * (d.C + 1);
-        long long blocks = (n + 255) / 256;
-        if (blocks > 152 * 32) blocks = 152 * 32;
-        trace_begin(s, kKBwdDwReduce);
-        dw_reduce_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(d, (const float*)ws, S, (T*)dw, (T*)db);
-        trace_end(s);
-    }
+    const int JT = (d.C + 63) / 64;
+    dim3 grid((unsigned)d.C, (unsigned)(3 * JT), (unsigned)S);
+    trace_begin(s, kKBwdDwPartialSimt);
+    dw_partial_kernel<T, K><<<grid, kDwThreads, 0, s>>>(d, (const T*)g, (const T*)x, (const T*)y, (float*)ws,
+                                                        split_chunk(d, S));
+    trace_end(s);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_t(const Dims& d, const void* g, const void* x, const void* y, const void* w,
-                     const void* bias, void* dx, void* dy, void* dw, void* db, void* ws, cudaStream_t s) {
+cudaError_t reduce_t(const Dims& d, const float* ws, int S, void* dw, void* db, cudaStream_t s) {
+    const long long n = d.O * (d.C + 1);
+    long long blocks = (n + 255) / 256;
+    if (blocks > 152 * 32) blocks = 152 * 32;
+    trace_begin(s, kKBwdDwReduce);
+    dw_reduce_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(d, ws, S, (T*)dw, (T*)db);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dx_t(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
+                 cudaStream_t s) {
     switch (d.K) {
-        case 1: return launch_k<T, 1>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
-        case 3: return launch_k<T, 3>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
-        case 5: return launch_k<T, 5>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
-        case 7: return launch_k<T, 7>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
+        case 1: return launch_dx_k<T, 1>(d, g, y, w, bias, dx, s);
+        case 3: return launch_dx_k<T, 3>(d, g, y, w, bias, dx, s);
+        case 5: return launch_dx_k<T, 5>(d, g, y, w, bias, dx, s);
+        case 7: return launch_dx_k<T, 7>(d, g, y, w, bias, dx, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t dy_t(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
+    switch (d.K) {
+        case 1: return launch_dy_k<T, 1>(d, g, x, w, dy, s);
+        case 3: return launch_dy_k<T, 3>(d, g, x, w, dy, s);
+        case 5: return launch_dy_k<T, 5>(d, g, x, w, dy, s);
+        case 7: return launch_dy_k<T, 7>(d, g, x, w, dy, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t dw_t(const Dims& d, const void* g, const void* x, const void* y, void* ws, cudaStream_t s) {
+    switch (d.K) {
+        case 1: return launch_dw_k<T, 1>(d, g, x, y, ws, s);
+        case 3: return launch_dw_k<T, 3>(d, g, x, y, ws, s);
+        case 5: return launch_dw_k<T, 5>(d, g, x, y, ws, s);
+        case 7: return launch_dw_k<T, 7>(d, g, x, y, ws, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -379,11 +409,38 @@ size_t backward_simt_workspace(const Dims& d) {
     return sizeof(float) * (size_t)backward_num_splits(d) * (size_t)d.O * (size_t)(d.C + 1);
 }
 
+cudaError_t launch_bwd_dx_simt(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
+                               cudaStream_t s) {
+    if (d.dtype == 1) return dx_t<__nv_bfloat16>(d, g, y, w, bias, dx, s);
+    return dx_t<float>(d, g, y, w, bias, dx, s);
+}
+
+cudaError_t launch_bwd_dy_simt(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
+    if (d.dtype == 1) return dy_t<__nv_bfloat16>(d, g, x, w, dy, s);
+    return dy_t<float>(d, g, x, w, dy, s);
+}
+
+cudaError_t launch_bwd_dw_partial_simt(const Dims& d, const void* g, const void* x, const void* y, void* ws,
+                                       cudaStream_t s) {
+    if (d.dtype == 1) return dw_t<__nv_bfloat16>(d, g, x, y, ws, s);
+    return dw_t<float>(d, g, x, y, ws, s);
+}
+
+cudaError_t launch_bwd_reduce(const Dims& d, const float* ws, int S, void* dw, void* db, cudaStream_t s) {
+    if (d.dtype == 1) return reduce_t<__nv_bfloat16>(d, ws, S, dw, db, s);
+    return reduce_t<float>(d, ws, S, dw, db, s);
+}
+
 cudaError_t launch_backward_simt(const Dims& d, const void* g, const void* x, const void* y, const void* w,
                                  const void* bias, void* dx, void* dy, void* dw, void* db, void* ws,
                                  cudaStream_t s) {
-    if (d.dtype == 1) return launch_t<__nv_bfloat16>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
-    return launch_t<float>(d, g, x, y, w, bias, dx, dy, dw, db, ws, s);
+    cudaError_t e = launch_bwd_dx_simt(d, g, y, w, bias, dx, s);
+    if (e != cudaSuccess) return e;
+    e = launch_bwd_dy_simt(d, g, x, w, dy, s);
+    if (e != cudaSuccess) return e;
+    e = launch_bwd_dw_partial_simt(d, g, x, y, ws, s);
+    if (e != cudaSuccess) return e;
+    return launch_bwd_reduce(d, (const float*)ws, backward_num_splits(d), dw, db, s);
 }
 
 }  // namespace ddpm

@@ -1,0 +1,283 @@
+// bwd_dw_tc.cu -- dW / dbias split partials on tcgen05 tensor cores (bf16).
+//
+// README "lartpang/DynamicConvolutionOperator", section "CUDA Flash 式融合训练":
+// dWeight/dbias form dK = shifted(x) * grad on chip and reduce it over space;
+// the tokens are split into at most 16 FP32 partials that a second short
+// kernel sums (dw_reduce_kernel in backward_simt.cu, fixed order).
+//
+//   ws[s][o][j] = sum_{pixels p of split s} dK[o, p] * y[j, p]     (j < C)
+//   ws[s][o][C] = sum_p dK[o, p]                                    (dbias)
+//
+// GB300 design.  A CTA owns a block of taps -- 14 channels of one dilation,
+// 126 taps, padded to the MMA M of 128 -- and one pixel split.  Per 2x64
+// pixel tile:
+//   - TMA brings y [64 j x 128 px] (one 128-byte row per channel and tile row,
+//     128B-swizzled: a K-major operand), the block's 14 grad planes [16 x 128
+//     px] and the matching x windows [(2+2R) x 80 px], zero-filled outside the
+//     image;
+//   - eight warps form dK^T[o, px] (bwdtc::form_dk_tile) into a 128B-swizzled
+//     K-major operand;
+//   - one thread issues D[o, n] += dK^T[o, px] * Y[n, px] with N = 80 rows: the
+//     64 y channels plus a constant ones row (row 64) that yields dbias.
+// The accumulator stays in TMEM for the whole split and is written once.
+#include "bwd_tc_common.cuh"
+#include "tc.cuh"
+
+namespace ddpm {
+namespace {
+
+using namespace bwdtc;
+
+constexpr int kNY = 80;           // MMA N: 64 y channels + ones row + 15 zero rows
+constexpr int kFormWarps = 8;
+constexpr int kThreads = 32 * (2 + kFormWarps);
+constexpr int kWinRowsMax = kTH + 2 * kMaxR;   // 18
+
+// shared memory (bytes from a 1024-aligned base)
+constexpr int kDK = 0;                               // 2 x dK^T tiles
+constexpr int kYS = kDK + 2 * kDKBytes;              // 2 stages x 2 halves x [80 rows x 128 B]
+constexpr int kYHalf = kNY * 128;                    // 10240
+constexpr int kYStage = 2 * kYHalf;                  // 20480
+constexpr int kGS = kYS + 2 * kYStage;               // 2 stages x [16 slots x 128 px] bf16
+constexpr int kGStage = kSlots * kPx * 2;            // 4096
+constexpr int kXS = kGS + 2 * kGStage;               // 2 stages x [16 slots x rows x 80] bf16
+constexpr int kXStage = kSlots * kWinRowsMax * kWinCols * 2;  // 46080
+constexpr int kSmemBytes = kXS + 2 * kXStage + 1024;
+static_assert(kYS % 1024 == 0 && kYStage % 1024 == 0 && kYHalf % 1024 == 0, "SW128 atoms need 1 KiB");
+static_assert(kGS % 128 == 0 && kXS % 128 == 0 && kGStage % 128 == 0 && kXStage % 128 == 0, "TMA dst 128 B");
+
+struct DwTcParams {
+    Dims d;
+    int tiles_w, tiles_per_img, n_tiles;
+    int n_cblk;        // ceil(C / 14) blocks of channels per dilation
+    int n_oblk;        // 3 * n_cblk
+    int tiles_per_split;
+    int R, WHx;        // halo radius, window rows (2 + 2R)
+    int xslot_bytes;   // WHx * 80 * 2
+    float* ws;         // [S][O][C+1]
+    unsigned int* err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dw_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmG,
+                     const __grid_constant__ CUtensorMap tmX, const DwTcParams P) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t in_full[2], in_empty[2], dk_full[2], dk_empty[2], acc_done, mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = P.d.C;
+    const long long O = P.d.O;
+    const int ob = blockIdx.x % P.n_oblk;
+    const int split = blockIdx.x / P.n_oblk;
+    const int t_begin = split * P.tiles_per_split;
+    const int t_end = min(t_begin + P.tiles_per_split, P.n_tiles);
+    const int n_my = max(0, t_end - t_begin);
+
+    // this block of taps: dilation dd, channels [c_first, c_first + nc)
+    const int dd = ob / P.n_cblk;
+    const int c_first = (ob % P.n_cblk) * kCB;
+    const int nc = min(kCB, C - c_first);
+    const int nrows = nc * 9;
+    const int dil = dil_of(P.d, dd);
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&in_full[s], 1);
+            mbar_init(&in_empty[s], kFormWarps + 1);
+            mbar_init(&dk_full[s], kFormWarps);
+            mbar_init(&dk_empty[s], 1);
+        }
+        mbar_init(&acc_done, 1);
+        mbar_init(&mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_slot, 128);
+    if (warp >= 2) {
+        // rows 64..79 of both y stages / halves: a row of ones (dbias) and 15 zero rows
+        const int et = threadIdx.x - 64;
+        for (int i = et; i < 2 * 2 * 16 * 32; i += 32 * kFormWarps) {
+            const int word = i % 32, row = (i / 32) % 16, half = (i / 512) % 2, st = i / 1024;
+            const uint32_t v = row == 0 ? 0x3F803F80u : 0u;  // bf16 pair (1.0, 1.0)
+            reinterpret_cast<uint32_t*>(sm + kYS + st * kYStage + half * kYHalf + (64 + row) * 128)[word] = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmY);
+            prefetch_tmap(&tmG);
+            prefetch_tmap(&tmX);
+            const uint32_t bytes = 2 * 8192 + kGStage + kSlots * P.xslot_bytes;
+            int issued = 0;
+            for (int i = 0; i < n_my; ++i) {
+                const int s = i & 1, ph = (i >> 1) & 1;
+                if (!mbar_wait(&in_empty[s], ph ^ 1, P.err, abort_v)) break;
+                const int t = t_begin + i;
+                const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
+                const int h0 = (ti / P.tiles_w) * kTH, w0 = (ti % P.tiles_w) * kTW;
+                uint8_t* ys = sm + kYS + s * kYStage;
+                mbar_arrive_expect_tx(&in_full[s], bytes);
+                tma_load_4d(ys, &tmY, &in_full[s], w0, h0, 0, b);
+                tma_load_4d(ys + kYHalf, &tmY, &in_full[s], w0, h0 + 1, 0, b);
+                tma_load_4d(sm + kGS + s * kGStage, &tmG, &in_full[s], w0, h0, (1 + dd) * C + c_first, b);
+                tma_load_4d(sm + kXS + s * kXStage, &tmX, &in_full[s], w0 - 8, h0 - P.R, c_first, b);
+                issued = i + 1;
+            }
+            // drain: every copy this CTA started lands before its shared memory is released
+            int never = 0;
+            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+                mbar_wait(&in_full[i & 1], (i >> 1) & 1, P.err, &never);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0 && n_my > 0) {
+            const uint32_t idesc = instr_desc(1, 0, 0, kBlockRows, kNY);   // both operands K-major
+            bool ok = true;
+            for (int i = 0; i < n_my && ok; ++i) {
+                const int s = i & 1, ph = (i >> 1) & 1;
+                if (!mbar_wait(&dk_full[s], ph, P.err, abort_v) || !mbar_wait(&in_full[s], ph, P.err, abort_v)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t da = smem_u32(sm + kDK + s * kDKBytes);
+                const uint32_t ya = smem_u32(sm + kYS + s * kYStage);
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16(tmem, smem_desc(da + half * 16384 + kk * 32, 16, 1024, kSwizzle128B),
+                                smem_desc(ya + half * kYHalf + kk * 32, 16, 1024, kSwizzle128B), idesc,
+                                (i > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&dk_empty[s]);
+                mma_commit(&in_empty[s]);
+            }
+            if (ok) mma_commit(&acc_done);
+            mma_commit(&mma_done);
+            int never = 0;
+            mbar_wait(&mma_done, 0, P.err, &never);
+        }
+    } else {
+        // ------------------------------------------------------- dK formers + epilogue
+        const int et = threadIdx.x - 64;
+        const int slot_elems = P.xslot_bytes / 2;
+        bool ok = true;
+        for (int i = 0; i < n_my && ok; ++i) {
+            const int s = i & 1, ph = (i >> 1) & 1;
+            if (!mbar_wait(&in_full[s], ph, P.err, abort_v) || !mbar_wait(&dk_empty[s], ph ^ 1, P.err, abort_v)) {
+                ok = false;
+                break;
+            }
+            form_dk_tile(sm + kDK + s * kDKBytes, reinterpret_cast<const uint32_t*>(sm + kXS + s * kXStage),
+                         reinterpret_cast<const bf16*>(sm + kGS + s * kGStage), nrows, slot_elems, P.R, dil, 0, et,
+                         32 * kFormWarps);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&dk_full[s]);
+                mbar_arrive(&in_empty[s]);
+            }
+        }
+        // epilogue: this split's partial sums for the block of taps
+        const int q = warp & 3, hc = (warp - 2) >> 2;
+        const int row = q * 32 + lane;
+        const int rc = row / 9;
+        const long long o = (long long)(dd * C + c_first + rc) * 9 + (row - rc * 9);
+        float* wsrow = P.ws + ((long long)split * O + o) * (C + 1);
+        uint32_t v[40];
+        if (n_my > 0) {
+            if (ok && mbar_wait(&acc_done, 0, P.err, abort_v)) {
+                tc_fence_after();
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + hc * 40;
+                DDPM_TMEM_LD_X16(ta, (v + 0));
+                DDPM_TMEM_LD_X16(ta + 16, (v + 16));
+                DDPM_TMEM_LD_X8(ta + 32, (v + 32));
+                tmem_ld_wait();
+            } else {
+                ok = false;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 40; ++j) v[j] = 0u;
+        }
+        if (ok && row < nrows) {
+#pragma unroll
+            for (int jj = 0; jj < 40; ++jj) {
+                const int j = hc * 40 + jj;
+                if (j < C) wsrow[j] = __uint_as_float(v[jj]);
+                else if (j == 64) wsrow[C] = __uint_as_float(v[jj]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+}  // namespace
+
+bool bwd_dw_tc_eligible(const Dims& d, const void* g, const void* x, const void* y) {
+    return bwdtc::eligible(d, g, x, y);
+}
+
+int bwd_dw_tc_splits(const Dims& d, size_t workspace_bytes) {
+    const int n_oblk = 3 * ((d.C + kCB - 1) / kCB);
+    const long long n_tiles = (long long)d.B * ((d.H + kTH - 1) / kTH) * ((d.W + kTW - 1) / kTW);
+    int S = num_sms() / n_oblk;
+    if (S < 1) S = 1;
+    if (S > 16) S = 16;
+    if (S > n_tiles) S = (int)n_tiles;
+    const long long cap = (long long)(workspace_bytes / (sizeof(float) * (size_t)d.O * (size_t)(d.C + 1)));
+    if (S > cap) S = (int)cap;
+    return S < 1 ? 1 : S;
+}
+
+cudaError_t launch_bwd_dw_tc(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S,
+                             cudaStream_t s) {
+    static int attr_done = 0;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_dw_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = 1;
+    }
+    DwTcParams P;
+    P.d = d;
+    P.tiles_w = (d.W + kTW - 1) / kTW;
+    P.tiles_per_img = ((d.H + kTH - 1) / kTH) * P.tiles_w;
+    P.n_tiles = d.B * P.tiles_per_img;
+    P.n_cblk = (d.C + kCB - 1) / kCB;
+    P.n_oblk = 3 * P.n_cblk;
+    P.tiles_per_split = (P.n_tiles + S - 1) / S;
+    P.R = d.R();
+    P.WHx = kTH + 2 * P.R;
+    P.xslot_bytes = P.WHx * kWinCols * 2;
+    P.ws = ws;
+    P.err = device_error_word();
+    if (P.err == nullptr) return cudaErrorUnknown;
+    CUtensorMap tmY, tmG, tmX;
+    if (!encode_nchw(&tmY, y, d, d.C, kTW, 1, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_nchw(&tmG, g, d, 4 * d.C, kTW, kTH, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_nchw(&tmX, x, d, d.C, kWinCols, (uint32_t)P.WHx, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    trace_begin(s, kKBwdDwTc);
+    bwd_dw_tc_kernel<<<P.n_oblk * S, kThreads, kSmemBytes, s>>>(tmY, tmG, tmX, P);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace ddpm

@@ -1,0 +1,261 @@
+// bwd_dy_tc.cu -- dY on tcgen05 tensor cores (bf16).
+//
+// README "lartpang/DynamicConvolutionOperator", section "CUDA Flash 式融合训练":
+// dY forms dK = shifted(x) * grad on chip and multiplies it by the generator
+// weight straight away:
+//   dy[b, j, p] = sum_o W[o, j] * dK[b, o, p].
+//
+// GB300 design.  Persistent CTAs walk 2x64 pixel tiles.  For each tile the
+// CTA visits every block of taps (14 channels of one dilation, 126 taps):
+//   - TMA brings the block's grad planes, x windows and W rows [128 o x 64 j];
+//   - eight warps form the dK^T tile (bwdtc::form_dk_tile);
+//   - one thread issues D[px, j] += dK[px, o] * W[o, j] (M = 128 pixels read
+//     MN-major from the dK^T tile, N = 64, K = 128 taps in eight K=16 steps).
+// The accumulator [128 px x 64 j] fp32 is double-buffered in TMEM so that
+// four epilogue warps store tile i while tile i+1 accumulates.
+#include "bwd_tc_common.cuh"
+#include "tc.cuh"
+
+namespace ddpm {
+namespace {
+
+using namespace bwdtc;
+
+constexpr int kN = 64;            // MMA N: output channels j (zero padded beyond C)
+constexpr int kFormWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (2 + kFormWarps + kEpiWarps);
+constexpr int kWinRowsMax = kTH + 2 * kMaxR;   // 18
+
+// shared memory (bytes from a 1024-aligned base)
+constexpr int kDK = 0;                               // 2 x dK^T tiles
+constexpr int kWS = kDK + 2 * kDKBytes;              // 2 stages x W block [128 o x 128 B] SW128
+constexpr int kWStage = kBlockRows * 128;            // 16384
+constexpr int kGS = kWS + 2 * kWStage;               // 2 stages x [16 slots x 128 px] bf16
+constexpr int kGStage = kSlots * kPx * 2;            // 4096
+constexpr int kXS = kGS + 2 * kGStage;               // 2 stages x [16 slots x rows x 80] bf16
+constexpr int kXStage = kSlots * kWinRowsMax * kWinCols * 2;  // 46080
+constexpr int kSmemBytes = kXS + 2 * kXStage + 1024;
+static_assert(kWS % 1024 == 0 && kWStage % 1024 == 0, "SW128 atoms need 1 KiB");
+static_assert(kGS % 128 == 0 && kXS % 128 == 0 && kXStage % 128 == 0, "TMA dst 128 B");
+
+struct DyTcParams {
+    Dims d;
+    int tiles_w, tiles_per_img, n_tiles;
+    int n_cblk, n_oblk;
+    int R, WHx, xslot_bytes;
+    bf16* dy;
+    unsigned int* err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dy_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
+                     const __grid_constant__ CUtensorMap tmX, const DyTcParams P) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t in_full[2], in_empty[2], dk_full[2], dk_empty[2], acc_full[2], acc_empty[2], mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = P.d.C;
+    const int n_my = blockIdx.x < P.n_tiles ? (P.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int NB = P.n_oblk;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&in_full[s], 1);
+            mbar_init(&in_empty[s], kFormWarps + 1);
+            mbar_init(&dk_full[s], kFormWarps);
+            mbar_init(&dk_empty[s], 1);
+            mbar_init(&acc_full[s], 1);
+            mbar_init(&acc_empty[s], kEpiWarps);
+        }
+        mbar_init(&mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_slot, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmG);
+            prefetch_tmap(&tmX);
+            const uint32_t bytes = kWStage + kGStage + kSlots * P.xslot_bytes;
+            int issued = 0;
+            bool ok = true;
+            for (int tl = 0; tl < n_my && ok; ++tl) {
+                const int t = blockIdx.x + tl * gridDim.x;
+                const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
+                const int h0 = (ti / P.tiles_w) * kTH, w0 = (ti % P.tiles_w) * kTW;
+                for (int ob = 0; ob < NB; ++ob) {
+                    const int i = tl * NB + ob, s = i & 1, ph = (i >> 1) & 1;
+                    if (!mbar_wait(&in_empty[s], ph ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    const int dd = ob / P.n_cblk, c_first = (ob % P.n_cblk) * kCB;
+                    mbar_arrive_expect_tx(&in_full[s], bytes);
+                    tma_load_2d(sm + kWS + s * kWStage, &tmW, &in_full[s], 0, (dd * C + c_first) * 9);
+                    tma_load_4d(sm + kGS + s * kGStage, &tmG, &in_full[s], w0, h0, (1 + dd) * C + c_first, b);
+                    tma_load_4d(sm + kXS + s * kXStage, &tmX, &in_full[s], w0 - 8, h0 - P.R, c_first, b);
+                    issued = i + 1;
+                }
+            }
+            int never = 0;
+            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+                mbar_wait(&in_full[i & 1], (i >> 1) & 1, P.err, &never);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0 && n_my > 0) {
+            const uint32_t idesc = instr_desc(1, 1, 1, kPx, kN);   // A (dK) and B (W) MN-major
+            bool ok = true;
+            for (int tl = 0; tl < n_my && ok; ++tl) {
+                const int tb = tl & 1, tph = (tl >> 1) & 1;
+                if (!mbar_wait(&acc_empty[tb], tph ^ 1, P.err, abort_v)) break;
+                tc_fence_after();
+                const uint32_t dt = tmem + tb * kN;
+                for (int ob = 0; ob < NB; ++ob) {
+                    const int i = tl * NB + ob, s = i & 1, ph = (i >> 1) & 1;
+                    if (!mbar_wait(&dk_full[s], ph, P.err, abort_v) || !mbar_wait(&in_full[s], ph, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t da = smem_u32(sm + kDK + s * kDKBytes);
+                    const uint32_t wa = smem_u32(sm + kWS + s * kWStage);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockRows / 16; ++kk)
+                        mma_f16(dt, smem_desc(da + kk * 2048, 16384, 1024, kSwizzle128B),
+                                smem_desc(wa + kk * 2048, 8192, 1024, kSwizzle128B), idesc,
+                                (ob > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&dk_empty[s]);
+                    mma_commit(&in_empty[s]);
+                }
+                if (ok) mma_commit(&acc_full[tb]);
+            }
+            mma_commit(&mma_done);
+            int never = 0;
+            mbar_wait(&mma_done, 0, P.err, &never);
+        }
+    } else if (warp < 2 + kFormWarps) {
+        // ------------------------------------------------------- dK formers
+        const int et = threadIdx.x - 64;
+        const int slot_elems = P.xslot_bytes / 2;
+        bool ok = true;
+        for (int tl = 0; tl < n_my && ok; ++tl) {
+            for (int ob = 0; ob < NB; ++ob) {
+                const int i = tl * NB + ob, s = i & 1, ph = (i >> 1) & 1;
+                if (!mbar_wait(&in_full[s], ph, P.err, abort_v) || !mbar_wait(&dk_empty[s], ph ^ 1, P.err, abort_v)) {
+                    ok = false;
+                    break;
+                }
+                const int dd = ob / P.n_cblk, c_first = (ob % P.n_cblk) * kCB;
+                const int nrows = min(kCB, C - c_first) * 9;
+                form_dk_tile(sm + kDK + s * kDKBytes, reinterpret_cast<const uint32_t*>(sm + kXS + s * kXStage),
+                             reinterpret_cast<const bf16*>(sm + kGS + s * kGStage), nrows, slot_elems, P.R,
+                             dil_of(P.d, dd), 0, et, 32 * kFormWarps);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&dk_full[s]);
+                    mbar_arrive(&in_empty[s]);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------- epilogue: dy stores
+        const int q = warp & 3;
+        const int m = q * 32 + lane;              // pixel slot == TMEM lane
+        const int tr = m / kTW, tc_ = m % kTW;
+        for (int tl = 0; tl < n_my; ++tl) {
+            const int tb = tl & 1, tph = (tl >> 1) & 1;
+            if (!mbar_wait(&acc_full[tb], tph, P.err, abort_v)) break;
+            tc_fence_after();
+            uint32_t v[64];
+            const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * kN;
+            DDPM_TMEM_LD_X16(ta, (v + 0));
+            DDPM_TMEM_LD_X16(ta + 16, (v + 16));
+            DDPM_TMEM_LD_X16(ta + 32, (v + 32));
+            DDPM_TMEM_LD_X16(ta + 48, (v + 48));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[tb]);
+            const int t = blockIdx.x + tl * gridDim.x;
+            const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
+            const int h = (ti / P.tiles_w) * kTH + tr, w = (ti % P.tiles_w) * kTW + tc_;
+            if (h < P.d.H && w < P.d.W) {
+                bf16* out = P.dy + (long long)b * C * P.d.HW + (long long)h * P.d.W + w;
+#pragma unroll
+                for (int j = 0; j < kN; ++j)
+                    if (j < C) out[(long long)j * P.d.HW] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+}  // namespace
+
+bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w) {
+    return bwdtc::eligible(d, g, x, w);
+}
+
+cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
+    static int attr_done = 0;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_dy_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = 1;
+    }
+    DyTcParams P;
+    P.d = d;
+    P.tiles_w = (d.W + kTW - 1) / kTW;
+    P.tiles_per_img = ((d.H + kTH - 1) / kTH) * P.tiles_w;
+    P.n_tiles = d.B * P.tiles_per_img;
+    P.n_cblk = (d.C + kCB - 1) / kCB;
+    P.n_oblk = 3 * P.n_cblk;
+    P.R = d.R();
+    P.WHx = kTH + 2 * P.R;
+    P.xslot_bytes = P.WHx * kWinCols * 2;
+    P.dy = static_cast<bf16*>(dy);
+    P.err = device_error_word();
+    if (P.err == nullptr) return cudaErrorUnknown;
+    CUtensorMap tmW, tmG, tmX;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)d.C, (cuuint64_t)d.O};
+        const cuuint64_t str[1] = {(cuuint64_t)d.C * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)kBlockRows};
+        const cuuint32_t es[2] = {1, 1};
+        if (encode_fn()(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dims, str, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    if (!encode_nchw(&tmG, g, d, 4 * d.C, kTW, kTH, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_nchw(&tmX, x, d, d.C, kWinCols, (uint32_t)P.WHx, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    int grid = num_sms();
+    if (grid > P.n_tiles) grid = P.n_tiles;
+    trace_begin(s, kKBwdDyTc);
+    bwd_dy_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmW, tmG, tmX, P);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace ddpm

@@ -19,8 +19,9 @@ enum KernelId : int {
     kKBwdDwPartialSimt = 5,
     kKBwdDwReduce = 6,
     kKBwdDxTc = 7,
-    kKBwdDyDwTc = 8,
-    kKNumKernels = 9
+    kKBwdDyTc = 8,
+    kKBwdDwTc = 9,
+    kKNumKernels = 10
 };
 
 // Tracing hooks around each launch (cheap no-ops while tracing is off).
@@ -58,5 +59,24 @@ cudaError_t launch_backward_simt(const Dims& d, const void* g, const void* x, co
 
 // Number of fp32 partial slices used for dW / dbias (at most 16).
 int backward_num_splits(const Dims& d);
+
+// The backward's pieces, launched separately so that each can run on the
+// kernel that suits the problem.
+cudaError_t launch_bwd_dx_simt(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
+                               cudaStream_t s);
+cudaError_t launch_bwd_dy_simt(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s);
+cudaError_t launch_bwd_dw_partial_simt(const Dims& d, const void* g, const void* x, const void* y, void* ws,
+                                       cudaStream_t s);
+cudaError_t launch_bwd_reduce(const Dims& d, const float* ws, int S, void* dw, void* db, cudaStream_t s);
+
+// dW / dbias split partials on tcgen05 tensor cores (bf16, K = 3, 16 <= C <= 64).
+bool bwd_dw_tc_eligible(const Dims& d, const void* g, const void* x, const void* y);
+int bwd_dw_tc_splits(const Dims& d, size_t workspace_bytes);
+cudaError_t launch_bwd_dw_tc(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S,
+                             cudaStream_t s);
+
+// dY on tcgen05 tensor cores (same shapes as the dW kernel).
+bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w);
+cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s);
 
 }  // namespace ddpm

@@ -169,6 +169,43 @@ def test_tc_forward_repeated_calls_identical():
     assert binding.ddpm_get_device_error() == 0
 
 
+# ------------------------------------------------ tensor-core backward path --
+
+TC_BWD_SHAPES = list(TC_SHAPES)
+
+
+@pytest.mark.parametrize("p", TC_BWD_SHAPES, ids=_id)
+def test_tc_backward_matches_oracle_and_cuda_cores(p):
+    h = make_inputs(p, 800, "bfloat16")
+    d = _dev(h)
+    names = _traced_kernels(lambda: run_backward(d, p))
+    assert "bwd_dw_tc" in names and "bwd_dy_tc" in names, f"expected the tensor-core dY/dW kernels, got {names}"
+    got = run_backward(d, p)
+    simt = run_backward(d, p, flags=binding.DDPM_FLAG_CUDA_CORES)
+    torch.cuda.synchronize()
+    ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=True)
+    for name, a, b, want in zip(("dx", "dy", "dW", "dbias"), got, simt, ref):
+        assert_grad_close(a, want, "bfloat16", name)
+        assert_grad_close(b, want, "bfloat16", name + " (cuda cores)")
+
+
+@pytest.mark.parametrize("p", [Problem(1, 16, 8, 16, 3), Problem(1, 24, 4, 24, 3, (2, 2, 4)), Problem(2, 64, 4, 16, 3)],
+                         ids=_id)
+def test_tc_backward_integer_bit_exact(p):
+    """Integer inputs with at most 256 pixels: every dW / dbias sum is exact in bf16."""
+    h = make_integer_inputs(p, 11, "bfloat16")
+    d = _dev(h)
+    assert "bwd_dw_tc" in _traced_kernels(lambda: run_backward(d, p))
+    dx, dy, dw, db = run_backward(d, p)
+    torch.cuda.synchronize()
+    rdx, rdy, rdw, rdb = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations,
+                                         bf16=True)
+    np.testing.assert_array_equal(to64(dx), rdx)
+    np.testing.assert_array_equal(to64(dy), rdy)
+    np.testing.assert_array_equal(to64(dw), rdw)
+    np.testing.assert_array_equal(to64(db), rdb)
+
+
 # ----------------------------------------------------- integer, bit-exact --
 
 @pytest.mark.parametrize("dtype", DTYPES)
