@@ -166,7 +166,9 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
     try {
         const cudaStream_t s = (cudaStream_t)stream;
         // each piece runs on the tensor-core kernel where one exists for the problem
-        cudaError_t e = ddpm::launch_bwd_dx_simt(d, grad_out, y, weight, bias, dx, s);
+        cudaError_t e = ddpm::bwd_dx_tc_eligible(d, grad_out, y, weight)
+                            ? ddpm::launch_bwd_dx_tc(d, grad_out, y, weight, bias, dx, s)
+                            : ddpm::launch_bwd_dx_simt(d, grad_out, y, weight, bias, dx, s);
         if (e == cudaSuccess) {
             if (ddpm::bwd_dy_tc_eligible(d, grad_out, x, weight))
                 e = ddpm::launch_bwd_dy_tc(d, grad_out, x, weight, dy, s);

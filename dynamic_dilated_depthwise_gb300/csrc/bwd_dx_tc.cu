@@ -1,0 +1,362 @@
+// bwd_dx_tc.cu -- dX on tcgen05 tensor cores (bf16).
+//
+// README "lartpang/DynamicConvolutionOperator", section "CUDA Flash 式融合训练":
+// dX recomputes the dynamic taps and gathers each dilation's contribution:
+//   dx[b,c,q] = grad[b,c,q] + sum_{d,ky,kx} Tq[b,o,q-off] * grad[b,(1+d)C+c,q-off],
+//   Tq = bf16(bias[o] + sum_j W[o,j] y[b,j,q-off]),  o = (d*C + c)*9 + ky*3 + kx.
+//
+// GB300 design: one shifted GEMM per tap, so the taps are recomputed exactly
+// once per (pixel, tap) with no halo recompute.  A CTA owns a 16x8 pixel tile
+// (MMA M = 128, slot s = r*8 + c) and all 64 channels (N = 64):
+//   - the y window of the tile, (16+2R) x (8+2R) positions, is staged once as
+//     unswizzled K-major core matrices [8-channel chunk][position][8]: eight
+//     consecutive slots are eight consecutive positions of one window row, so
+//     the A operand of tap (dy, dx) is the same window at a start offset of
+//     ((R-dy)*WW + (R-dx)) * 16 bytes (row-group stride WW * 16);
+//   - two constant chunks (a ones column and zeros) make a fifth K=16 step
+//     that adds the bias, whose B tile the producer writes per tap;
+//   - the producer brings W's rows of tap (d, k) for all channels by TMA
+//     (a 3-D view of W: [dc][k][j]) into a 4-stage ring;
+//   - D of each tap lands in one of eight TMEM buffers [128 x 64];
+//   - eight worker warps stage the windows, then per tap round the taps to
+//     bf16 and accumulate tap * grad at the gathered position from a
+//     position-major grad window of the current dilation.
+#include "bwd_tc_common.cuh"
+#include "tc.cuh"
+
+namespace ddpm {
+namespace {
+
+using namespace bwdtc;
+
+constexpr int kDxTH = 16, kDxTW = 8;      // pixel tile
+constexpr int kDxMaxR = 6;                // halo radius supported by the window buffers
+constexpr int kMaxPos = (kDxTH + 2 * kDxMaxR) * (kDxTW + 2 * kDxMaxR);   // 560
+constexpr int kN = 64;
+constexpr int kTaps = 27;
+constexpr int kWorkWarps = 8;
+constexpr int kThreads = 32 * (2 + kWorkWarps);
+constexpr int kStages = 4;
+constexpr int kDBufs = 8;
+
+// shared memory (bytes from a 1024-aligned base)
+constexpr int kWTStage = 8192 + 2048;                 // W tap tile (SW128, 64 rows) + bias tile
+constexpr int kWT = 0;
+constexpr int kYW = kWT + kStages * kWTStage;         // 10 chunks x positions x 16 B
+constexpr int kYWBytes = 10 * kMaxPos * 16;           // 89600
+constexpr int kGW = kYW + kYWBytes;                   // [position][64] bf16, 16-byte chunks swizzled
+constexpr int kGWBytes = kMaxPos * 128;               // 71680
+constexpr int kSmemBytes = kGW + kGWBytes + 1024;
+static_assert(kWTStage % 1024 == 0, "W tap tiles need 1 KiB alignment");
+
+struct DxTcParams {
+    Dims d;
+    int tiles_w, tiles_per_img, n_tiles;
+    int R, WH, WW, npos;
+    const bf16* y;
+    const bf16* g;
+    const bf16* bias;
+    bf16* dx;
+    unsigned int* err;
+};
+
+__device__ __forceinline__ void work_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kWorkWarps) : "memory"); }
+
+// bf16 (nearest even) of an fp32 value, returned as fp32
+__device__ __forceinline__ float round_bf16(float t) { return __bfloat162float(__float2bfloat16_rn(t)); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dx_tc_kernel(const __grid_constant__ CUtensorMap tmW, const DxTcParams P) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t wt_full[kStages], wt_empty[kStages], d_full[kDBufs], d_empty[kDBufs], yw_full, yw_empty,
+        mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = P.d.C, H = P.d.H, W = P.d.W;
+    const long long HW = P.d.HW;
+    const int n_my = blockIdx.x < P.n_tiles ? (P.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int R = P.R, WW = P.WW, npos = P.npos;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&wt_full[i], 1);
+            mbar_init(&wt_empty[i], 1);
+        }
+        for (int i = 0; i < kDBufs; ++i) {
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], kWorkWarps);
+        }
+        mbar_init(&yw_full, kWorkWarps);
+        mbar_init(&yw_empty, 1);
+        mbar_init(&mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_slot, 512);
+    if (warp >= 2) {
+        // constant chunks 8 (ones column) and 9 (zeros) of the y window: the bias K-step
+        const int et = threadIdx.x - 64;
+        for (int p = et; p < 2 * npos; p += 32 * kWorkWarps) {
+            const uint4 v = p < npos ? make_uint4(0x3F80u, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(sm + kYW + (8 * npos + p) * 16) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- producer: W tap tiles + bias tiles
+        if (lane == 0) prefetch_tmap(&tmW);
+        bool ok = true;
+        int issued = 0;
+        for (int tl = 0; tl < n_my && ok; ++tl) {
+            for (int u = 0; u < kTaps; ++u) {
+                const int i = tl * kTaps + u, st = i % kStages, ph = (i / kStages) & 1;
+                int good = 1;
+                if (lane == 0) good = mbar_wait(&wt_empty[st], ph ^ 1, P.err, abort_v) ? 1 : 0;
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    break;
+                }
+                const int dd = u / 9, k = u % 9;
+                uint8_t* bt = sm + kWT + st * kWTStage + 8192;
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int c = 2 * lane + rr;
+                    const long long o = (long long)(dd * C + c) * 9 + k;
+                    uint32_t bv = 0u;
+                    if (P.bias != nullptr && c < C) {
+                        const bf16 b = P.bias[o];
+                        bv = (uint32_t)(*reinterpret_cast<const unsigned short*>(&b));
+                    }
+                    *reinterpret_cast<uint4*>(bt + (c / 8) * 256 + (c % 8) * 16) = make_uint4(bv, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(bt + (c / 8) * 256 + 128 + (c % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&wt_full[st], 8192);
+                    tma_load_3d(sm + kWT + st * kWTStage, &tmW, &wt_full[st], 0, k, dd * C);
+                }
+                issued = i + 1;
+            }
+        }
+        if (lane == 0) {
+            // drain: every copy this CTA started lands before its shared memory is released
+            int never = 0;
+            for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+                mbar_wait(&wt_full[i % kStages], (i / kStages) & 1, P.err, &never);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0 && n_my > 0) {
+            const uint32_t idesc = instr_desc(1, 0, 0, 128, kN);
+            const uint32_t yw = smem_u32(sm + kYW);
+            const uint32_t lbo_y = (uint32_t)npos * 16, sbo_y = (uint32_t)WW * 16;
+            bool ok = true;
+            for (int tl = 0; tl < n_my && ok; ++tl) {
+                if (!mbar_wait(&yw_full, tl & 1, P.err, abort_v)) break;
+                tc_fence_after();
+                for (int u = 0; u < kTaps; ++u) {
+                    const int i = tl * kTaps + u, st = i % kStages, buf = i % kDBufs;
+                    if (!mbar_wait(&wt_full[st], (i / kStages) & 1, P.err, abort_v) ||
+                        !mbar_wait(&d_empty[buf], ((i / kDBufs) & 1) ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int dd = u / 9, k = u % 9, dil = dil_of(P.d, dd);
+                    const int ky = k / 3, kx = k - ky * 3;
+                    const uint32_t shift = (uint32_t)((R - (ky - 1) * dil) * WW + (R - (kx - 1) * dil)) * 16;
+                    const uint32_t wt = smem_u32(sm + kWT + st * kWTStage);
+                    const uint32_t dt = tmem + buf * kN;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16(dt, smem_desc(yw + shift + 2 * kk * lbo_y, lbo_y, sbo_y, kSwizzleNone),
+                                smem_desc(wt + kk * 32, 16, 1024, kSwizzle128B), idesc, kk > 0);
+                    mma_f16(dt, smem_desc(yw + shift + 8 * lbo_y, lbo_y, sbo_y, kSwizzleNone),
+                            smem_desc(wt + 8192, 128, 256, kSwizzleNone), idesc, 1);
+                    mma_commit(&d_full[buf]);
+                    mma_commit(&wt_empty[st]);
+                }
+                if (ok) mma_commit(&yw_empty);
+            }
+            mma_commit(&mma_done);
+            int never = 0;
+            mbar_wait(&mma_done, 0, P.err, &never);
+        }
+    } else {
+        // ------------------------------------------------------- workers
+        const int et = threadIdx.x - 64;
+        const int q = warp & 3, hc = (warp - 2) >> 2;   // lane quadrant, channel half [32 hc, 32 hc + 32)
+        const int s = q * 32 + lane;                    // slot == TMEM lane
+        const int r = s >> 3, c = s & 7;
+        uint8_t* ywp = sm + kYW;
+        uint8_t* gwp = sm + kGW;
+        bool ok = true;
+        for (int tl = 0; tl < n_my && ok; ++tl) {
+            const int t = blockIdx.x + tl * gridDim.x;
+            const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
+            const int h0 = (ti / P.tiles_w) * kDxTH, w0 = (ti % P.tiles_w) * kDxTW;
+            // y window: [chunk][position][8 channels], zero outside the image / beyond C
+            if (!mbar_wait(&yw_empty, (tl & 1) ^ 1, P.err, abort_v)) break;
+            const bf16* yb = P.y + (long long)b * C * HW;
+            for (int uidx = et; uidx < 8 * npos; uidx += 32 * kWorkWarps) {
+                const int jc = uidx / npos, pos = uidx - jc * npos;
+                const int h = h0 - R + pos / WW, w = w0 - R + pos % WW;
+                const bool inside = h >= 0 && h < H && w >= 0 && w < W;
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j0 = jc * 8 + 2 * e;
+                    unsigned short lo = 0, hi = 0;
+                    if (inside && j0 < C) lo = reinterpret_cast<const unsigned short*>(yb)[(long long)j0 * HW + (long long)h * W + w];
+                    if (inside && j0 + 1 < C)
+                        hi = reinterpret_cast<const unsigned short*>(yb)[(long long)(j0 + 1) * HW + (long long)h * W + w];
+                    pk[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+                *reinterpret_cast<uint4*>(ywp + (jc * npos + pos) * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&yw_full);
+
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+            for (int dd = 0; dd < 3 && ok; ++dd) {
+                const int dil = dil_of(P.d, dd);
+                // grad window of dilation dd: [position][64 channels] bf16, 16-byte chunks rotated by position
+                work_bar();
+                const bf16* gb = P.g + ((long long)b * 4 * C + (1 + dd) * C) * HW;
+                for (int uidx = et; uidx < 8 * npos; uidx += 32 * kWorkWarps) {
+                    const int jc = uidx / npos, pos = uidx - jc * npos;
+                    const int h = h0 - R + pos / WW, w = w0 - R + pos % WW;
+                    const bool inside = h >= 0 && h < H && w >= 0 && w < W;
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j0 = jc * 8 + 2 * e;
+                        unsigned short lo = 0, hi = 0;
+                        if (inside && j0 < C)
+                            lo = reinterpret_cast<const unsigned short*>(gb)[(long long)j0 * HW + (long long)h * W + w];
+                        if (inside && j0 + 1 < C)
+                            hi = reinterpret_cast<const unsigned short*>(gb)[(long long)(j0 + 1) * HW + (long long)h * W + w];
+                        pk[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                    }
+                    *reinterpret_cast<uint4*>(gwp + pos * 128 + ((jc ^ (pos & 7)) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                work_bar();
+                for (int k = 0; k < 9; ++k) {
+                    const int i = tl * kTaps + dd * 9 + k, buf = i % kDBufs;
+                    if (!mbar_wait(&d_full[buf], (i / kDBufs) & 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t v[32];
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * kN + hc * 32;
+                    DDPM_TMEM_LD_X16(ta, (v + 0));
+                    DDPM_TMEM_LD_X16(ta + 16, (v + 16));
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&d_empty[buf]);
+                    const int ky = k / 3, kx = k - ky * 3;
+                    const int pos = (r + R - (ky - 1) * dil) * WW + (c + R - (kx - 1) * dil);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint4 gv = *reinterpret_cast<const uint4*>(gwp + pos * 128 + (((4 * hc + e) ^ (pos & 7)) << 4));
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                        for (int f = 0; f < 4; ++f) {
+                            const float g0 = __uint_as_float(gw[f] << 16), g1 = __uint_as_float(gw[f] & 0xFFFF0000u);
+                            const int ci = e * 8 + 2 * f;
+                            acc[ci] = fmaf(round_bf16(__uint_as_float(v[ci])), g0, acc[ci]);
+                            acc[ci + 1] = fmaf(round_bf16(__uint_as_float(v[ci + 1])), g1, acc[ci + 1]);
+                        }
+                    }
+                }
+            }
+            if (!ok) break;
+            // dx = grad (channel block 0) + gathered sum
+            const int h = h0 + r, w = w0 + c;
+            if (h < H && w < W) {
+                const long long pix = (long long)h * W + w;
+                const bf16* g0p = P.g + (long long)b * 4 * C * HW + pix;
+                bf16* dxp = P.dx + (long long)b * C * HW + pix;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int ch = hc * 32 + i;
+                    if (ch < C) dxp[(long long)ch * HW] = __float2bfloat16_rn(__bfloat162float(g0p[(long long)ch * HW]) + acc[i]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool bwd_dx_tc_eligible(const Dims& d, const void* g, const void* y, const void* w) {
+    return bwdtc::eligible(d, g, y, w) && d.R() <= kDxMaxR;
+}
+
+cudaError_t launch_bwd_dx_tc(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
+                             cudaStream_t s) {
+    static int attr_done = 0;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_dx_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = 1;
+    }
+    DxTcParams P;
+    P.d = d;
+    P.tiles_w = (d.W + kDxTW - 1) / kDxTW;
+    P.tiles_per_img = ((d.H + kDxTH - 1) / kDxTH) * P.tiles_w;
+    P.n_tiles = d.B * P.tiles_per_img;
+    P.R = d.R();
+    P.WH = kDxTH + 2 * P.R;
+    P.WW = kDxTW + 2 * P.R;
+    P.npos = P.WH * P.WW;
+    P.y = static_cast<const bf16*>(y);
+    P.g = static_cast<const bf16*>(g);
+    P.bias = static_cast<const bf16*>(bias);
+    P.dx = static_cast<bf16*>(dx);
+    P.err = device_error_word();
+    if (P.err == nullptr) return cudaErrorUnknown;
+    CUtensorMap tmW;
+    {
+        // W viewed as [3C (dc)][9 (k)][C (j)]: box {64 j, 1 k, 64 dc} = rows (d*C + c, k) for 64 channels
+        const cuuint64_t dims[3] = {(cuuint64_t)d.C, 9, (cuuint64_t)(3 * d.C)};
+        const cuuint64_t str[2] = {(cuuint64_t)d.C * 2, (cuuint64_t)d.C * 9 * 2};
+        const cuuint32_t box[3] = {64, 1, 64};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (encode_fn()(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, str, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    int grid = num_sms();
+    if (grid > P.n_tiles) grid = P.n_tiles;
+    trace_begin(s, kKBwdDxTc);
+    bwd_dx_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmW, P);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace ddpm

@@ -75,6 +75,11 @@ int bwd_dw_tc_splits(const Dims& d, size_t workspace_bytes);
 cudaError_t launch_bwd_dw_tc(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S,
                              cudaStream_t s);
 
+// dX on tcgen05 tensor cores: one shifted GEMM per tap (halo radius <= 6).
+bool bwd_dx_tc_eligible(const Dims& d, const void* g, const void* y, const void* w);
+cudaError_t launch_bwd_dx_tc(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
+                             cudaStream_t s);
+
 // dY on tcgen05 tensor cores (same shapes as the dW kernel).
 bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w);
 cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s);
