@@ -115,7 +115,7 @@ ddpm_status ddpm_forward(const ddpm_problem* problem, const void* x, const void*
     DDPM_TRY(check_ptr(bias, es, true));
     DDPM_TRY(check_ptr(out, es, false));
     try {
-        if (ddpm::forward_tc_eligible(d, y, weight))
+        if (ddpm::forward_tc_eligible(d, y, weight) && (uintptr_t)x % 16 == 0)
             return from_cuda(ddpm::launch_forward_tc(d, x, y, weight, bias, out, (cudaStream_t)stream));
         return from_cuda(ddpm::launch_forward_simt(d, x, y, weight, bias, out, (cudaStream_t)stream));
     } catch (...) {

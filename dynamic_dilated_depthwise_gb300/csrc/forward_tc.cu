@@ -13,17 +13,17 @@
 // TMEM lane = pixel, so each epilogue thread owns every tap of its pixel and
 // filters without any cross-thread reduction.
 //
-//   warp 0      TMA producer: W slice of the group (once), y tiles (2 stages)
+//   warp 0      TMA producer: W slice of the group (once), y tiles (2 stages),
+//               the raw x window of each tile ([16 ch][rows][cols] bf16)
 //   warp 1      TMEM owner + MMA issuer (one elected lane)
-//   warps 2..9  epilogue: stage the x window (fp32, position-major), read the
-//               taps from TMEM, round to bf16, multiply by shifted x, store.
-// Three TMEM regions (one per dilation, 144 columns each) form the pipeline:
-// the MMA of tile i+1 / dilation d starts as soon as the epilogue has drained
-// region d of tile i.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include "launch.h"
+//   warps 2..9  epilogue: transpose the raw x window to position-major
+//               [pos][16 ch] (so one 8-byte load brings four channels of one
+//               neighbour), read the taps from TMEM, round them to bf16,
+//               multiply by shifted x and store the 4C output channels.
+// Three TMEM regions (one per dilation, 144 columns each) form the MMA /
+// epilogue pipeline; the raw window is refilled by TMA as soon as the previous
+// tile's window has been transposed, so its latency hides behind the filter.
+#include "bwd_tc_common.cuh"
 #include "tc.cuh"
 
 namespace ddpm {
@@ -38,9 +38,9 @@ constexpr int kTile = 128;               // pixels per tile (MMA M)
 constexpr int kKPad = 64;                // generator K (channels of y), zero padded
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kWinMax = 1536;            // x window positions (fits R = 5 at TW = 128)
+constexpr int kWinMax = 1600;            // x window positions: (TH + 2R) x (TW + 16) <= 1600
 
-// shared-memory carve-up (bytes, from a 1024-aligned base).  The two 128-byte
+// shared-memory carve-up (bytes, from a 1024-aligned base).  The 128-byte
 // swizzled operands come first so that every swizzle atom starts on 1024 B.
 constexpr int kSW = 0;                                 // W slice, 3 x [144 x 128 B], SW128 K-major
 constexpr int kSWBytes = 3 * kN * 128;                 // 55296 = 54 KiB
@@ -50,11 +50,13 @@ constexpr int kSBias = kSY + kSYBytes;                 // bias B operand, 3 x [1
 constexpr int kSBiasBytes = 3 * kN * 32;               // 13824
 constexpr int kSOnes = kSBias + kSBiasBytes;           // ones A operand [128 x 16] no swizzle
 constexpr int kSOnesBytes = kTile * 32;                // 4096
-constexpr int kSX = kSOnes + kSOnesBytes;              // x window, [pos][16] fp32
-constexpr int kSXBytes = kWinMax * kCG * 4;            // 98304
+constexpr int kSRaw = kSOnes + kSOnesBytes;            // raw x window [16 ch][rows][cols] bf16 (TMA)
+constexpr int kSRawBytes = kWinMax * kCG * 2;          // 51200
+constexpr int kSX = kSRaw + kSRawBytes;                // x window [pos][16 ch] bf16, 16-byte halves rotated
+constexpr int kSXBytes = kWinMax * kCG * 2;            // 51200
 constexpr int kSmemBytes = kSX + kSXBytes + 1024;      // + alignment slack
 static_assert(kSW % 1024 == 0 && kSY % 1024 == 0 && (kSY + kSYBytes / 2) % 1024 == 0, "SW128 atoms need 1 KiB");
-static_assert(kSBias % 16 == 0 && kSOnes % 16 == 0 && kSX % 16 == 0, "16-byte aligned operands");
+static_assert(kSBias % 16 == 0 && kSOnes % 16 == 0 && kSRaw % 128 == 0 && kSX % 16 == 0, "operand alignment");
 
 struct FwdTcParams {
     Dims d;
@@ -65,7 +67,7 @@ struct FwdTcParams {
     int n_groups;          // ceil(C / 16)
     int ctas_per_group;
     int R;                 // halo radius = max dilation * (K / 2)
-    int WH, WW;            // x window rows / columns
+    int WH, WC;            // x window rows (TH + 2R) / columns (TW + 16, origin w0 - 8)
     const bf16* x;
     const bf16* bias;      // may be null
     bf16* out;
@@ -74,9 +76,10 @@ struct FwdTcParams {
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
 
-// x window slot of (position, float4 group j): the group index is rotated by
-// (pos >> 1) & 3 so that 8 consecutive positions hit 8 distinct bank quads.
-__device__ __forceinline__ int xw_index(int pos, int j) { return pos * kCG + (((j + (pos >> 1)) & 3) << 2); }
+// byte offset of the 16-byte half `h` (channels 8h..8h+7) of position pos in the
+// transposed window: the halves swap on every other group of four positions so
+// that eight consecutive positions hit distinct bank quads.
+__device__ __forceinline__ int xw_off(int pos, int h) { return pos * 32 + ((h ^ ((pos >> 2) & 1)) << 4); }
 
 struct TileCoord {
     int b, h0, w0, nvalid;
@@ -100,12 +103,12 @@ __device__ __forceinline__ TileCoord tile_coord(const FwdTcParams& P, int t) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     forward_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmW,
-                      const FwdTcParams P) {
+                      const __grid_constant__ CUtensorMap tmX, const FwdTcParams P) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* sX = reinterpret_cast<float*>(sm + kSX);
-    __shared__ uint64_t bar_w, bar_y_full[2], bar_y_empty[2], bar_acc_full[3], bar_acc_empty[3], bar_done;
+    __shared__ uint64_t bar_w, bar_y_full[2], bar_y_empty[2], bar_acc_full[3], bar_acc_empty[3], bar_raw_full,
+        bar_raw_empty, bar_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -116,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = group * kCG;
     const int C = P.d.C;
     const long long HW = P.d.HW;
+    const int npos = P.WH * P.WC;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -128,6 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_acc_full[dd], 1);
             mbar_init(&bar_acc_empty[dd], kEpiWarps);
         }
+        mbar_init(&bar_raw_full, 1);
+        mbar_init(&bar_raw_empty, kEpiWarps);
         mbar_init(&bar_done, 1);
         fence_mbar_init();
     }
@@ -161,25 +167,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tmY);
             prefetch_tmap(&tmW);
+            prefetch_tmap(&tmX);
             mbar_arrive_expect_tx(&bar_w, 3 * kN * 128);
             for (int dd = 0; dd < 3; ++dd)
                 tma_load_2d(sm + kSW + dd * kN * 128, &tmW, &bar_w, 0, (dd * C + c0) * kTaps);
-            int issued = 0;
+            const uint32_t raw_bytes = (uint32_t)npos * kCG * 2;
+            int issued_y = 0, issued_x = 0;
             for (int i = 0; i < n_my; ++i) {
                 const int s = i & 1, ph = (i >> 1) & 1;
-                if (!mbar_wait(&bar_y_empty[s], ph ^ 1, P.err, abort_v)) break;
                 const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
+                if (!mbar_wait(&bar_y_empty[s], ph ^ 1, P.err, abort_v)) break;
                 const int pb = tcd.h0 * P.d.W + tcd.w0;
                 mbar_arrive_expect_tx(&bar_y_full[s], kTile * kKPad * 2);
                 tma_load_3d(sm + kSY + s * 16384, &tmY, &bar_y_full[s], pb, 0, tcd.b);
                 tma_load_3d(sm + kSY + s * 16384 + 8192, &tmY, &bar_y_full[s], pb + 64, 0, tcd.b);
-                issued = i + 1;
+                issued_y = i + 1;
+                if (!mbar_wait(&bar_raw_empty, (i & 1) ^ 1, P.err, abort_v)) break;
+                mbar_arrive_expect_tx(&bar_raw_full, raw_bytes);
+                tma_load_4d(sm + kSRaw, &tmX, &bar_raw_full, tcd.w0 - 8, tcd.h0 - P.R, c0, tcd.b);
+                issued_x = i + 1;
             }
             // drain: every copy this CTA started must land before its shared memory is released
             int never = 0;
             mbar_wait(&bar_w, 0, P.err, &never);
-            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+            for (int i = issued_y > 2 ? issued_y - 2 : 0; i < issued_y; ++i)
                 mbar_wait(&bar_y_full[i & 1], (i >> 1) & 1, P.err, &never);
+            if (issued_x > 0) mbar_wait(&bar_raw_full, (issued_x - 1) & 1, P.err, &never);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -227,75 +240,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool slot_in_tile = s < P.TH * P.TW;
         const int rr = slot_in_tile ? s / P.TW : 0;
         const int cc = slot_in_tile ? s % P.TW : 0;
-        const int R = P.R, WW = P.WW;
-        const int npos = P.WH * P.WW;
+        const int R = P.R, WC = P.WC;
+        const unsigned short* raw = reinterpret_cast<const unsigned short*>(sm + kSRaw);
+        uint8_t* xw = sm + kSX;
         for (int i = 0; i < n_my; ++i) {
             const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
-            epi_bar();  // the previous tile's window is no longer read
-            const bf16* xb = P.x + ((long long)tcd.b * C + c0) * HW;
+            epi_bar();  // every thread is done with the previous tile's transposed window
+            if (!mbar_wait(&bar_raw_full, i & 1, P.err, abort_v)) goto epilogue_done;
+            // transpose [16 ch][pos] -> [pos][16 ch] (bf16)
             for (int pos = et; pos < npos; pos += 32 * kEpiWarps) {
-                const int wr = pos / WW, wc = pos % WW;
-                const int h = tcd.h0 - R + wr, w = tcd.w0 - R + wc;
-                const bool inside = h >= 0 && h < P.d.H && w >= 0 && w < P.d.W;
-                float v[kCG];
+                uint32_t w[8];
 #pragma unroll
-                for (int c = 0; c < kCG; ++c)
-                    v[c] = (inside && c0 + c < C) ? __bfloat162float(xb[(long long)c * HW + (long long)h * P.d.W + w])
-                                                  : 0.0f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<float4*>(sX + xw_index(pos, j)) =
-                        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                for (int e = 0; e < 8; ++e)
+                    w[e] = (uint32_t)raw[(2 * e) * npos + pos] | ((uint32_t)raw[(2 * e + 1) * npos + pos] << 16);
+                *reinterpret_cast<uint4*>(xw + xw_off(pos, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(xw + xw_off(pos, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
-            epi_bar();  // window ready
+            epi_bar();  // window ready; the raw buffer may be refilled
+            if (lane == 0) mbar_arrive(&bar_raw_empty);
             const bool valid = s < tcd.nvalid;
             const long long p = (long long)(tcd.h0 + rr) * P.d.W + tcd.w0 + cc;
             bf16* ob = P.out + (long long)tcd.b * 4 * C * HW;
             if (valid) {
-                const int cpos = (rr + R) * WW + cc + R;
+                // channels c0 .. c0+15 of the output are x itself
+                const int cpos = (rr + R) * WC + cc + 8;
+                const uint4 xv = *reinterpret_cast<const uint4*>(xw + xw_off(cpos, g));
+                const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                for (int cl = 0; cl < 8; ++cl) {
-                    const int c = 8 * g + cl;
-                    if (c0 + c < C)
-                        ob[(long long)(c0 + c) * HW + p] =
-                            __float2bfloat16(sX[xw_index(cpos, c >> 2) + (c & 3)]);
+                for (int e = 0; e < 4; ++e) {
+                    const int c = c0 + 8 * g + 2 * e;
+                    if (c < C) ob[(long long)c * HW + p] = __ushort_as_bfloat16((unsigned short)(xs[e] & 0xFFFFu));
+                    if (c + 1 < C) ob[(long long)(c + 1) * HW + p] = __ushort_as_bfloat16((unsigned short)(xs[e] >> 16));
                 }
             }
             for (int dd = 0; dd < 3; ++dd) {
                 if (!mbar_wait(&bar_acc_full[dd], i & 1, P.err, abort_v)) goto epilogue_done;
                 tc_fence_after();
-                uint32_t t[72];
-                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + dd * kN + g * 72;
-                DDPM_TMEM_LD_X16(ta, (t + 0));
-                DDPM_TMEM_LD_X16(ta + 16, (t + 16));
-                DDPM_TMEM_LD_X16(ta + 32, (t + 32));
-                DDPM_TMEM_LD_X16(ta + 48, (t + 48));
-                DDPM_TMEM_LD_X8(ta + 64, (t + 64));
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_acc_empty[dd]);
-                if (valid) {
-                    const int dil = dil_of(P.d, dd);
-                    float acc[8];
+                const int dil = dil_of(P.d, dd);
+                const int base = (rr + R) * WC + cc + 8;
+                for (int cq = 0; cq < 2; ++cq) {
+                    uint32_t t[36];
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + dd * kN + (8 * g + 4 * cq) * kTaps;
+                    DDPM_TMEM_LD_X16(ta, (t + 0));
+                    DDPM_TMEM_LD_X16(ta + 16, (t + 16));
+                    DDPM_TMEM_LD_X4(ta + 32, (t + 32));
+                    tmem_ld_wait();
+                    if (cq == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar_acc_empty[dd]);
+                    }
+                    if (!valid) continue;
+                    // taps rounded to bf16 (nearest even), two at a time
+                    float tr[36];
 #pragma unroll
-                    for (int cl = 0; cl < 8; ++cl) acc[cl] = 0.0f;
+                    for (int e = 0; e < 18; ++e) {
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(t[2 * e]), __uint_as_float(t[2 * e + 1]));
+                        const uint32_t u = *reinterpret_cast<uint32_t*>(&h2);
+                        tr[2 * e] = __uint_as_float(u << 16);
+                        tr[2 * e + 1] = __uint_as_float(u & 0xFFFF0000u);
+                    }
+                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                     for (int k = 0; k < kTaps; ++k) {
                         const int ky = k / 3, kx = k % 3;
-                        const int pos = (rr + R + (ky - 1) * dil) * WW + cc + R + (kx - 1) * dil;
-                        const float4 xa = *reinterpret_cast<const float4*>(sX + xw_index(pos, 2 * g));
-                        const float4 xc = *reinterpret_cast<const float4*>(sX + xw_index(pos, 2 * g + 1));
-                        const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
-#pragma unroll
-                        for (int cl = 0; cl < 8; ++cl) {
-                            const float tq = __bfloat162float(__float2bfloat16_rn(__uint_as_float(t[cl * kTaps + k])));
-                            acc[cl] = fmaf(tq, xv[cl], acc[cl]);
-                        }
+                        const int pos = base + (ky - 1) * dil * WC + (kx - 1) * dil;
+                        const uint2 xv = *reinterpret_cast<const uint2*>(xw + xw_off(pos, g) + cq * 8);
+                        acc[0] = fmaf(tr[0 * kTaps + k], __uint_as_float(xv.x << 16), acc[0]);
+                        acc[1] = fmaf(tr[1 * kTaps + k], __uint_as_float(xv.x & 0xFFFF0000u), acc[1]);
+                        acc[2] = fmaf(tr[2 * kTaps + k], __uint_as_float(xv.y << 16), acc[2]);
+                        acc[3] = fmaf(tr[3 * kTaps + k], __uint_as_float(xv.y & 0xFFFF0000u), acc[3]);
                     }
 #pragma unroll
-                    for (int cl = 0; cl < 8; ++cl) {
-                        const int c = c0 + 8 * g + cl;
+                    for (int cl = 0; cl < 4; ++cl) {
+                        const int c = c0 + 8 * g + 4 * cq + cl;
                         if (c < C) ob[(long long)((1 + dd) * C + c) * HW + p] = __float2bfloat16_rn(acc[cl]);
                     }
                 }
@@ -311,21 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
-
 struct Tiling {
-    int TH, TW, tiles_per_row, tiles_per_img, R, WH, WW;
+    int TH, TW, tiles_per_row, tiles_per_img, R, WH, WC;
 };
 
 Tiling tiling_of(const Dims& d) {
@@ -341,11 +346,9 @@ Tiling tiling_of(const Dims& d) {
         t.tiles_per_row = 1;
         t.tiles_per_img = (d.H + t.TH - 1) / t.TH;
     }
-    const int maxdil = d.dil[0] > d.dil[1] ? (d.dil[0] > d.dil[2] ? d.dil[0] : d.dil[2])
-                                           : (d.dil[1] > d.dil[2] ? d.dil[1] : d.dil[2]);
-    t.R = maxdil * (d.K / 2);
+    t.R = d.R();
     t.WH = t.TH + 2 * t.R;
-    t.WW = t.TW + 2 * t.R;
+    t.WC = t.TW + 16;
     return t;
 }
 
@@ -356,12 +359,12 @@ bool forward_tc_eligible(const Dims& d, const void* y, const void* w) {
     if (d.C % 8 != 0 || d.C > kKPad) return false;      // TMA row stride of W; one 64-wide K block
     if (d.W % 8 != 0) return false;                     // every tile start is a 16-byte TMA coordinate
     if ((uintptr_t)y % 16 != 0 || (uintptr_t)w % 16 != 0) return false;
-    if (d.R() > 1024) return false;
+    if (d.R() > 8) return false;                        // the x window spans w0 - 8 .. w0 + TW + 8
     const Tiling t = tiling_of(d);
-    if ((long long)t.WH * t.WW > kWinMax) return false;
+    if ((long long)t.WH * t.WC > kWinMax || t.WH > 256) return false;
     const long long tiles = (long long)d.B * t.tiles_per_img;
     if (tiles > (1LL << 30) || d.O > (1LL << 30) || d.HW > (1LL << 31) - 1024) return false;
-    return encode_fn() != nullptr;
+    return bwdtc::encode_fn() != nullptr;
 }
 
 cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const void* w, const void* bias,
@@ -372,9 +375,11 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
         if (e != cudaSuccess) return e;
         attr_done = 1;
     }
-    auto enc = encode_fn();
+    auto enc = bwdtc::encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
-    CUtensorMap tmY, tmW;
+    if ((uintptr_t)x % 16 != 0) return cudaErrorInvalidValue;
+    const Tiling t = tiling_of(d);
+    CUtensorMap tmY, tmW, tmX;
     const cuuint64_t dimY[3] = {(cuuint64_t)d.HW, (cuuint64_t)d.C, (cuuint64_t)d.B};
     const cuuint64_t strY[2] = {(cuuint64_t)d.HW * 2, (cuuint64_t)d.HW * d.C * 2};
     const cuuint32_t boxY[3] = {64, (cuuint32_t)kKPad, 1};
@@ -391,8 +396,9 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    if (!bwdtc::encode_nchw(&tmX, x, d, d.C, (uint32_t)t.WC, (uint32_t)t.WH, kCG, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
 
-    const Tiling t = tiling_of(d);
     FwdTcParams P;
     P.d = d;
     P.TH = t.TH;
@@ -408,14 +414,14 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
     P.ctas_per_group = cpg;
     P.R = t.R;
     P.WH = t.WH;
-    P.WW = t.WW;
+    P.WC = t.WC;
     P.x = static_cast<const bf16*>(x);
     P.bias = static_cast<const bf16*>(bias);
     P.out = static_cast<bf16*>(out);
     P.err = device_error_word();
     if (P.err == nullptr) return cudaErrorUnknown;
     trace_begin(s, kKForwardTc);
-    forward_tc_kernel<<<P.n_groups * cpg, kThreads, kSmemBytes, s>>>(tmY, tmW, P);
+    forward_tc_kernel<<<P.n_groups * cpg, kThreads, kSmemBytes, s>>>(tmY, tmW, tmX, P);
     trace_end(s);
     return cudaGetLastError();
 }
