@@ -18,9 +18,12 @@
 //   - the producer brings W's rows of tap (d, k) for all channels by TMA
 //     (a 3-D view of W: [dc][k][j]) into a 4-stage ring;
 //   - D of each tap lands in one of eight TMEM buffers [128 x 64];
-//   - eight worker warps stage the windows, then per tap round the taps to
-//     bf16 and accumulate tap * grad at the gathered position from a
-//     position-major grad window of the current dilation.
+//   - a second producer warp streams the raw windows -- 8-channel chunks
+//     [8 ch][16+2R rows][24 cols] of y and of each dilation's grad planes --
+//     by TMA through a 2-stage ring; eight worker warps transpose each chunk
+//     into the K-major y window or the position-major grad window, then per
+//     tap round the taps to bf16 and accumulate tap * grad at the gathered
+//     position.
 #include "bwd_tc_common.cuh"
 #include "tc.cuh"
 
@@ -35,19 +38,25 @@ constexpr int kMaxPos = (kDxTH + 2 * kDxMaxR) * (kDxTW + 2 * kDxMaxR);   // 560
 constexpr int kN = 64;
 constexpr int kTaps = 27;
 constexpr int kWorkWarps = 8;
-constexpr int kThreads = 32 * (2 + kWorkWarps);
+constexpr int kThreads = 32 * (3 + kWorkWarps);   // W producer, MMA, 8 workers, raw producer
+constexpr int kRawWarp = 2 + kWorkWarps;
 constexpr int kStages = 4;
 constexpr int kDBufs = 8;
+constexpr int kRawCols = 24;              // raw window columns: origin w0 - 8 keeps TMA 16-byte aligned
+constexpr int kRawStage = 8 * (kDxTH + 2 * kDxMaxR) * kRawCols * 2;   // 10752
+constexpr int kChunks = 8 + 3 * 8;        // raw chunks per tile: y, then grad of each dilation
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr int kWTStage = 8192 + 2048;                 // W tap tile (SW128, 64 rows) + bias tile
 constexpr int kWT = 0;
-constexpr int kYW = kWT + kStages * kWTStage;         // 10 chunks x positions x 16 B
+constexpr int kRaw = kWT + kStages * kWTStage;        // 2 x raw chunk [8 ch][rows][24] bf16
+constexpr int kYW = kRaw + 2 * kRawStage;             // 10 chunks x positions x 16 B
 constexpr int kYWBytes = 10 * kMaxPos * 16;           // 89600
 constexpr int kGW = kYW + kYWBytes;                   // [position][64] bf16, 16-byte chunks swizzled
 constexpr int kGWBytes = kMaxPos * 128;               // 71680
 constexpr int kSmemBytes = kGW + kGWBytes + 1024;
 static_assert(kWTStage % 1024 == 0, "W tap tiles need 1 KiB alignment");
+static_assert(kRaw % 128 == 0 && kRawStage % 128 == 0 && kYW % 16 == 0 && kGW % 16 == 0, "staging alignment");
 
 struct DxTcParams {
     Dims d;
@@ -66,12 +75,13 @@ __device__ __forceinline__ void work_bar() { asm volatile("bar.sync 1, %0;" ::"n
 __device__ __forceinline__ float round_bf16(float t) { return __bfloat162float(__float2bfloat16_rn(t)); }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_dx_tc_kernel(const __grid_constant__ CUtensorMap tmW, const DxTcParams P) {
+    bwd_dx_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
+                     const __grid_constant__ CUtensorMap tmG, const DxTcParams P) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t wt_full[kStages], wt_empty[kStages], d_full[kDBufs], d_empty[kDBufs], yw_full, yw_empty,
-        mma_done;
+        raw_full[2], raw_empty[2], mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -94,11 +104,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&yw_full, kWorkWarps);
         mbar_init(&yw_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], kWorkWarps);
+        }
         mbar_init(&mma_done, 1);
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(&tmem_slot, 512);
-    if (warp >= 2) {
+    if (warp >= 2 && warp < kRawWarp) {
         // constant chunks 8 (ones column) and 9 (zeros) of the y window: the bias K-step
         const int et = threadIdx.x - 64;
         for (int p = et; p < 2 * npos; p += 32 * kWorkWarps) {
@@ -193,6 +207,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             int never = 0;
             mbar_wait(&mma_done, 0, P.err, &never);
         }
+    } else if (warp == kRawWarp) {
+        // ------------------------------------------------------- raw window producer
+        if (lane == 0) {
+            prefetch_tmap(&tmY);
+            prefetch_tmap(&tmG);
+            const uint32_t raw_bytes = 8u * (uint32_t)P.WH * kRawCols * 2;
+            int issued = 0;
+            bool ok = true;
+            for (int tl = 0; tl < n_my && ok; ++tl) {
+                const int t = blockIdx.x + tl * gridDim.x;
+                const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
+                const int h0 = (ti / P.tiles_w) * kDxTH, w0 = (ti % P.tiles_w) * kDxTW;
+                for (int idx = 0; idx < kChunks; ++idx) {
+                    const int i = tl * kChunks + idx, rs = i & 1;
+                    if (!mbar_wait(&raw_empty[rs], ((i >> 1) & 1) ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = sm + kRaw + rs * kRawStage;
+                    mbar_arrive_expect_tx(&raw_full[rs], raw_bytes);
+                    if (idx < 8) {
+                        tma_load_4d(dst, &tmY, &raw_full[rs], w0 - 8, h0 - R, idx * 8, b);
+                    } else {
+                        const int dd = (idx - 8) / 8, jc = (idx - 8) % 8;
+                        tma_load_4d(dst, &tmG, &raw_full[rs], w0 - 8, h0 - R, (1 + dd) * C + jc * 8, b);
+                    }
+                    issued = i + 1;
+                }
+            }
+            int never = 0;
+            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+                mbar_wait(&raw_full[i & 1], (i >> 1) & 1, P.err, &never);
+        }
     } else {
         // ------------------------------------------------------- workers
         const int et = threadIdx.x - 64;
@@ -201,30 +248,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = s >> 3, c = s & 7;
         uint8_t* ywp = sm + kYW;
         uint8_t* gwp = sm + kGW;
+        const int rplane = P.WH * kRawCols;             // elements per channel of a raw chunk
         bool ok = true;
         for (int tl = 0; tl < n_my && ok; ++tl) {
             const int t = blockIdx.x + tl * gridDim.x;
             const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
             const int h0 = (ti / P.tiles_w) * kDxTH, w0 = (ti % P.tiles_w) * kDxTW;
-            // y window: [chunk][position][8 channels], zero outside the image / beyond C
+            // y window: [chunk][position][8 channels] from the raw chunks (zero outside the image / beyond C)
             if (!mbar_wait(&yw_empty, (tl & 1) ^ 1, P.err, abort_v)) break;
-            const bf16* yb = P.y + (long long)b * C * HW;
-            for (int uidx = et; uidx < 8 * npos; uidx += 32 * kWorkWarps) {
-                const int jc = uidx / npos, pos = uidx - jc * npos;
-                const int h = h0 - R + pos / WW, w = w0 - R + pos % WW;
-                const bool inside = h >= 0 && h < H && w >= 0 && w < W;
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j0 = jc * 8 + 2 * e;
-                    unsigned short lo = 0, hi = 0;
-                    if (inside && j0 < C) lo = reinterpret_cast<const unsigned short*>(yb)[(long long)j0 * HW + (long long)h * W + w];
-                    if (inside && j0 + 1 < C)
-                        hi = reinterpret_cast<const unsigned short*>(yb)[(long long)(j0 + 1) * HW + (long long)h * W + w];
-                    pk[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+            for (int jc = 0; jc < 8 && ok; ++jc) {
+                const int i = tl * kChunks + jc, rs = i & 1;
+                if (!mbar_wait(&raw_full[rs], (i >> 1) & 1, P.err, abort_v)) {
+                    ok = false;
+                    break;
                 }
-                *reinterpret_cast<uint4*>(ywp + (jc * npos + pos) * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                const unsigned short* raw = reinterpret_cast<const unsigned short*>(sm + kRaw + rs * kRawStage);
+                for (int pos = et; pos < npos; pos += 32 * kWorkWarps) {
+                    const int row = pos / WW, re = row * kRawCols + (pos - row * WW) + (8 - R);
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        pk[e] = (uint32_t)raw[(2 * e) * rplane + re] | ((uint32_t)raw[(2 * e + 1) * rplane + re] << 16);
+                    *reinterpret_cast<uint4*>(ywp + (jc * npos + pos) * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[rs]);
             }
+            if (!ok) break;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&yw_full);
@@ -236,25 +286,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int dil = dil_of(P.d, dd);
                 // grad window of dilation dd: [position][64 channels] bf16, 16-byte chunks rotated by position
                 work_bar();
-                const bf16* gb = P.g + ((long long)b * 4 * C + (1 + dd) * C) * HW;
-                for (int uidx = et; uidx < 8 * npos; uidx += 32 * kWorkWarps) {
-                    const int jc = uidx / npos, pos = uidx - jc * npos;
-                    const int h = h0 - R + pos / WW, w = w0 - R + pos % WW;
-                    const bool inside = h >= 0 && h < H && w >= 0 && w < W;
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j0 = jc * 8 + 2 * e;
-                        unsigned short lo = 0, hi = 0;
-                        if (inside && j0 < C)
-                            lo = reinterpret_cast<const unsigned short*>(gb)[(long long)j0 * HW + (long long)h * W + w];
-                        if (inside && j0 + 1 < C)
-                            hi = reinterpret_cast<const unsigned short*>(gb)[(long long)(j0 + 1) * HW + (long long)h * W + w];
-                        pk[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                for (int jc = 0; jc < 8 && ok; ++jc) {
+                    const int i = tl * kChunks + 8 + dd * 8 + jc, rs = i & 1;
+                    if (!mbar_wait(&raw_full[rs], (i >> 1) & 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
                     }
-                    *reinterpret_cast<uint4*>(gwp + pos * 128 + ((jc ^ (pos & 7)) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    const unsigned short* raw = reinterpret_cast<const unsigned short*>(sm + kRaw + rs * kRawStage);
+                    for (int pos = et; pos < npos; pos += 32 * kWorkWarps) {
+                        const int row = pos / WW, re = row * kRawCols + (pos - row * WW) + (8 - R);
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            pk[e] = (uint32_t)raw[(2 * e) * rplane + re] | ((uint32_t)raw[(2 * e + 1) * rplane + re] << 16);
+                        *reinterpret_cast<uint4*>(gwp + pos * 128 + ((jc ^ (pos & 7)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&raw_empty[rs]);
                 }
+                if (!ok) break;
                 work_bar();
                 for (int k = 0; k < 9; ++k) {
                     const int i = tl * kTaps + dd * 9 + k, buf = i % kDBufs;
@@ -351,10 +402,14 @@ cudaError_t launch_bwd_dx_tc(const Dims& d, const void* g, const void* y, const 
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    CUtensorMap tmY, tmG;
+    if (!encode_nchw(&tmY, y, d, d.C, kRawCols, (uint32_t)P.WH, 8, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_nchw(&tmG, g, d, 4 * d.C, kRawCols, (uint32_t)P.WH, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
     int grid = num_sms();
     if (grid > P.n_tiles) grid = P.n_tiles;
     trace_begin(s, kKBwdDxTc);
-    bwd_dx_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmW, P);
+    bwd_dx_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmW, tmY, tmG, P);
     trace_end(s);
     return cudaGetLastError();
 }
