@@ -42,7 +42,7 @@ constexpr int kGS = kYS + 2 * kYStage;               // 2 stages x [16 slots x 1
 constexpr int kGStage = kSlots * kPx * 2;            // 4096
 constexpr int kXS = kGS + 2 * kGStage;               // 2 stages x [16 slots x rows x 80] bf16
 constexpr int kXStage = kSlots * kWinRowsMax * kWinCols * 2;  // 46080
-constexpr int kSmemBytes = kXS + 2 * kXStage + 1024;
+constexpr int kSmemBytes = kXS + 2 * kXStage + 1024 + 128;   // + alignment slack + over-read margin
 static_assert(kYS % 1024 == 0 && kYStage % 1024 == 0 && kYHalf % 1024 == 0, "SW128 atoms need 1 KiB");
 static_assert(kGS % 128 == 0 && kXS % 128 == 0 && kGStage % 128 == 0 && kXStage % 128 == 0, "TMA dst 128 B");
 
@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t v = row == 0 ? 0x3F803F80u : 0u;  // bf16 pair (1.0, 1.0)
             reinterpret_cast<uint32_t*>(sm + kYS + st * kYStage + half * kYHalf + (64 + row) * 128)[word] = v;
         }
+        zero_dk_pad_rows(sm + kDK, et, 32 * kFormWarps);
+        zero_dk_pad_rows(sm + kDK + kDKBytes, et, 32 * kFormWarps);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             form_dk_tile(sm + kDK + s * kDKBytes, reinterpret_cast<const uint32_t*>(sm + kXS + s * kXStage),
-                         reinterpret_cast<const bf16*>(sm + kGS + s * kGStage), nrows, slot_elems, P.R, dil, 0, et,
+                         reinterpret_cast<const bf16*>(sm + kGS + s * kGStage), kPx, nrows, slot_elems, P.R, dil, 0, et,
                          32 * kFormWarps);
             fence_proxy_async_smem();
             __syncwarp();

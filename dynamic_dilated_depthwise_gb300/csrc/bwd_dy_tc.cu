@@ -5,14 +5,16 @@
 // weight straight away:
 //   dy[b, j, p] = sum_o W[o, j] * dK[b, o, p].
 //
-// GB300 design.  Persistent CTAs walk 2x64 pixel tiles.  For each tile the
-// CTA visits every block of taps (14 channels of one dilation, 126 taps):
-//   - TMA brings the block's grad planes, x windows and W rows [128 o x 64 j];
-//   - eight warps form the dK^T tile (bwdtc::form_dk_tile);
-//   - one thread issues D[px, j] += dK[px, o] * W[o, j] (M = 128 pixels read
+// GB300 design.  Persistent CTAs walk super tiles of 8 rows x 64 columns (four
+// 2x64 sub-tiles, 512 pixels).  For each super tile the CTA visits every block
+// of taps (14 channels of one dilation, 126 taps); per block one TMA stage
+// brings the block's W rows [128 o x 64 j], grad planes [16 x 512 px] and x
+// windows [16 x (8+2R) x 80], and serves four sub-tiles:
+//   - eight warps form each sub-tile's dK^T tile (bwdtc::form_dk_tile);
+//   - one thread issues D_st[px, j] += dK[px, o] * W[o, j] (M = 128 pixels read
 //     MN-major from the dK^T tile, N = 64, K = 128 taps in eight K=16 steps).
-// The accumulator [128 px x 64 j] fp32 is double-buffered in TMEM so that
-// four epilogue warps store tile i while tile i+1 accumulates.
+// Four accumulators [128 px x 64 j] fp32 per super tile, double-buffered, fill
+// the 512 TMEM columns; four epilogue warps store super tile i while i+1 runs.
 #include "bwd_tc_common.cuh"
 #include "tc.cuh"
 
@@ -22,26 +24,30 @@ namespace {
 using namespace bwdtc;
 
 constexpr int kN = 64;            // MMA N: output channels j (zero padded beyond C)
+constexpr int kSub = 4;           // 2x64 sub-tiles per super tile
+constexpr int kSTH = kSub * kTH;  // 8 rows
+constexpr int kSPx = kSub * kPx;  // 512 pixels
+constexpr int kDyMaxR = 5;        // halo radius the window buffers hold
 constexpr int kFormWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 32 * (2 + kFormWarps + kEpiWarps);
-constexpr int kWinRowsMax = kTH + 2 * kMaxR;   // 18
+constexpr int kWinRowsMax = kSTH + 2 * kDyMaxR;   // 18
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr int kDK = 0;                               // 2 x dK^T tiles
 constexpr int kWS = kDK + 2 * kDKBytes;              // 2 stages x W block [128 o x 128 B] SW128
 constexpr int kWStage = kBlockRows * 128;            // 16384
-constexpr int kGS = kWS + 2 * kWStage;               // 2 stages x [16 slots x 128 px] bf16
-constexpr int kGStage = kSlots * kPx * 2;            // 4096
+constexpr int kGS = kWS + 2 * kWStage;               // 2 stages x [16 slots x 512 px] bf16
+constexpr int kGStage = kSlots * kSPx * 2;           // 16384
 constexpr int kXS = kGS + 2 * kGStage;               // 2 stages x [16 slots x rows x 80] bf16
 constexpr int kXStage = kSlots * kWinRowsMax * kWinCols * 2;  // 46080
-constexpr int kSmemBytes = kXS + 2 * kXStage + 1024;
+constexpr int kSmemBytes = kXS + 2 * kXStage + 1024 + 128;   // + alignment slack + over-read margin
 static_assert(kWS % 1024 == 0 && kWStage % 1024 == 0, "SW128 atoms need 1 KiB");
 static_assert(kGS % 128 == 0 && kXS % 128 == 0 && kXStage % 128 == 0, "TMA dst 128 B");
 
 struct DyTcParams {
     Dims d;
-    int tiles_w, tiles_per_img, n_tiles;
+    int tiles_w, tiles_per_img, n_tiles;   // super tiles
     int n_cblk, n_oblk;
     int R, WHx, xslot_bytes;
     bf16* dy;
@@ -77,7 +83,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&mma_done, 1);
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(&tmem_slot, 128);
+    if (warp == 1) tmem_alloc(&tmem_slot, 512);
+    if (warp >= 2 && warp < 2 + kFormWarps) {
+        zero_dk_pad_rows(sm + kDK, threadIdx.x - 64, 32 * kFormWarps);
+        zero_dk_pad_rows(sm + kDK + kDKBytes, threadIdx.x - 64, 32 * kFormWarps);
+        tc::fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -95,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tl = 0; tl < n_my && ok; ++tl) {
                 const int t = blockIdx.x + tl * gridDim.x;
                 const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
-                const int h0 = (ti / P.tiles_w) * kTH, w0 = (ti % P.tiles_w) * kTW;
+                const int h0 = (ti / P.tiles_w) * kSTH, w0 = (ti % P.tiles_w) * kTW;
                 for (int ob = 0; ob < NB; ++ob) {
                     const int i = tl * NB + ob, s = i & 1, ph = (i >> 1) & 1;
                     if (!mbar_wait(&in_empty[s], ph ^ 1, P.err, abort_v)) {
@@ -123,22 +134,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tb = tl & 1, tph = (tl >> 1) & 1;
                 if (!mbar_wait(&acc_empty[tb], tph ^ 1, P.err, abort_v)) break;
                 tc_fence_after();
-                const uint32_t dt = tmem + tb * kN;
-                for (int ob = 0; ob < NB; ++ob) {
+                for (int ob = 0; ob < NB && ok; ++ob) {
                     const int i = tl * NB + ob, s = i & 1, ph = (i >> 1) & 1;
-                    if (!mbar_wait(&dk_full[s], ph, P.err, abort_v) || !mbar_wait(&in_full[s], ph, P.err, abort_v)) {
+                    if (!mbar_wait(&in_full[s], ph, P.err, abort_v)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t da = smem_u32(sm + kDK + s * kDKBytes);
                     const uint32_t wa = smem_u32(sm + kWS + s * kWStage);
+                    for (int st = 0; st < kSub; ++st) {
+                        const int kd = i * kSub + st, db = kd & 1;
+                        if (!mbar_wait(&dk_full[db], (kd >> 1) & 1, P.err, abort_v)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t da = smem_u32(sm + kDK + db * kDKBytes);
+                        const uint32_t dt = tmem + (tb * kSub + st) * kN;
 #pragma unroll
-                    for (int kk = 0; kk < kBlockRows / 16; ++kk)
-                        mma_f16(dt, smem_desc(da + kk * 2048, 16384, 1024, kSwizzle128B),
-                                smem_desc(wa + kk * 2048, 8192, 1024, kSwizzle128B), idesc,
-                                (ob > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&dk_empty[s]);
+                        for (int kk = 0; kk < kBlockRows / 16; ++kk)
+                            mma_f16(dt, smem_desc(da + kk * 2048, 16384, 1024, kSwizzle128B),
+                                    smem_desc(wa + kk * 2048, 8192, 1024, kSwizzle128B), idesc,
+                                    (ob > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&dk_empty[db]);
+                    }
                     mma_commit(&in_empty[s]);
                 }
                 if (ok) mma_commit(&acc_full[tb]);
@@ -153,67 +171,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot_elems = P.xslot_bytes / 2;
         bool ok = true;
         for (int tl = 0; tl < n_my && ok; ++tl) {
-            for (int ob = 0; ob < NB; ++ob) {
+            for (int ob = 0; ob < NB && ok; ++ob) {
                 const int i = tl * NB + ob, s = i & 1, ph = (i >> 1) & 1;
-                if (!mbar_wait(&in_full[s], ph, P.err, abort_v) || !mbar_wait(&dk_empty[s], ph ^ 1, P.err, abort_v)) {
+                if (!mbar_wait(&in_full[s], ph, P.err, abort_v)) {
                     ok = false;
                     break;
                 }
                 const int dd = ob / P.n_cblk, c_first = (ob % P.n_cblk) * kCB;
                 const int nrows = min(kCB, C - c_first) * 9;
-                form_dk_tile(sm + kDK + s * kDKBytes, reinterpret_cast<const uint32_t*>(sm + kXS + s * kXStage),
-                             reinterpret_cast<const bf16*>(sm + kGS + s * kGStage), nrows, slot_elems, P.R,
-                             dil_of(P.d, dd), 0, et, 32 * kFormWarps);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&dk_full[s]);
-                    mbar_arrive(&in_empty[s]);
+                const int dil = dil_of(P.d, dd);
+                const uint32_t* xs32 = reinterpret_cast<const uint32_t*>(sm + kXS + s * kXStage);
+                const bf16* gs = reinterpret_cast<const bf16*>(sm + kGS + s * kGStage);
+                for (int st = 0; st < kSub; ++st) {
+                    const int kd = i * kSub + st, db = kd & 1;
+                    if (!mbar_wait(&dk_empty[db], ((kd >> 1) & 1) ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    form_dk_tile(sm + kDK + db * kDKBytes, xs32, gs + st * kPx, kSPx, nrows, slot_elems, P.R, dil,
+                                 st * kTH, et, 32 * kFormWarps);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&dk_full[db]);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&in_empty[s]);
             }
         }
     } else {
         // ------------------------------------------------------- epilogue: dy stores
         const int q = warp & 3;
         const int m = q * 32 + lane;              // pixel slot == TMEM lane
-        const int tr = m / kTW, tc_ = m % kTW;
+        const int tr = m / kTW, tcol = m % kTW;
         for (int tl = 0; tl < n_my; ++tl) {
             const int tb = tl & 1, tph = (tl >> 1) & 1;
             if (!mbar_wait(&acc_full[tb], tph, P.err, abort_v)) break;
             tc_fence_after();
-            uint32_t v[64];
-            const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * kN;
-            DDPM_TMEM_LD_X16(ta, (v + 0));
-            DDPM_TMEM_LD_X16(ta + 16, (v + 16));
-            DDPM_TMEM_LD_X16(ta + 32, (v + 32));
-            DDPM_TMEM_LD_X16(ta + 48, (v + 48));
-            tmem_ld_wait();
+            const int t = blockIdx.x + tl * gridDim.x;
+            const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
+            const int h0 = (ti / P.tiles_w) * kSTH, w0 = (ti % P.tiles_w) * kTW;
+            for (int st = 0; st < kSub; ++st) {
+                uint32_t v[64];
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (tb * kSub + st) * kN;
+                DDPM_TMEM_LD_X16(ta, (v + 0));
+                DDPM_TMEM_LD_X16(ta + 16, (v + 16));
+                DDPM_TMEM_LD_X16(ta + 32, (v + 32));
+                DDPM_TMEM_LD_X16(ta + 48, (v + 48));
+                tmem_ld_wait();
+                const int h = h0 + st * kTH + tr, w = w0 + tcol;
+                if (h < P.d.H && w < P.d.W) {
+                    bf16* out = P.dy + (long long)b * C * P.d.HW + (long long)h * P.d.W + w;
+#pragma unroll
+                    for (int j = 0; j < kN; ++j)
+                        if (j < C) out[(long long)j * P.d.HW] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[tb]);
-            const int t = blockIdx.x + tl * gridDim.x;
-            const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
-            const int h = (ti / P.tiles_w) * kTH + tr, w = (ti % P.tiles_w) * kTW + tc_;
-            if (h < P.d.H && w < P.d.W) {
-                bf16* out = P.dy + (long long)b * C * P.d.HW + (long long)h * P.d.W + w;
-#pragma unroll
-                for (int j = 0; j < kN; ++j)
-                    if (j < C) out[(long long)j * P.d.HW] = __float2bfloat16_rn(__uint_as_float(v[j]));
-            }
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, 512);
     }
 }
 
 }  // namespace
 
 bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w) {
-    return bwdtc::eligible(d, g, x, w);
+    return bwdtc::eligible(d, g, x, w) && d.R() <= kDyMaxR;
 }
 
 cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
@@ -226,12 +255,12 @@ cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const 
     DyTcParams P;
     P.d = d;
     P.tiles_w = (d.W + kTW - 1) / kTW;
-    P.tiles_per_img = ((d.H + kTH - 1) / kTH) * P.tiles_w;
+    P.tiles_per_img = ((d.H + kSTH - 1) / kSTH) * P.tiles_w;
     P.n_tiles = d.B * P.tiles_per_img;
     P.n_cblk = (d.C + kCB - 1) / kCB;
     P.n_oblk = 3 * P.n_cblk;
     P.R = d.R();
-    P.WHx = kTH + 2 * P.R;
+    P.WHx = kSTH + 2 * P.R;
     P.xslot_bytes = P.WHx * kWinCols * 2;
     P.dy = static_cast<bf16*>(dy);
     P.err = device_error_word();
@@ -247,7 +276,7 @@ cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const 
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    if (!encode_nchw(&tmG, g, d, 4 * d.C, kTW, kTH, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    if (!encode_nchw(&tmG, g, d, 4 * d.C, kTW, kSTH, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_nchw(&tmX, x, d, d.C, kWinCols, (uint32_t)P.WHx, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     int grid = num_sms();

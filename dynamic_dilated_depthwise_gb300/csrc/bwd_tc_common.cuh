@@ -45,37 +45,86 @@ __device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
 //   dk        destination tile (32 KiB, swizzled as described above)
 //   xs32      x window of the block's channels: slot c_local, rows (tile rows + 2R),
 //             kWinCols columns, bf16, origin (h0 - R + row_off, w0 - 8)
-//   gs        grad planes of the block: slot c_local, 128 pixels of this tile
+//   gs        grad planes of the block: slot c_local, the 128 pixels of this tile
+//             at gs + c_local * gstride
 //   row_off   first window row of this tile (tiles stacked in one window)
 //   tid/nthr  this thread among the forming threads
-// Rows r >= nrows (the padding of a 126-tap block) are written as zeros.
-__device__ __forceinline__ void form_dk_tile(uint8_t* dk, const uint32_t* xs32, const bf16* gs, int nrows,
-                                             int slot_elems, int R, int dil, int row_off, int tid, int nthr) {
-    for (int u = tid; u < kBlockRows * 16; u += nthr) {
-        const int ol = u >> 4, chunk = u & 15;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (ol < nrows) {
-            const int cl = ol / 9, k = ol - cl * 9;
-            const int ky = k / 3, kx = k - ky * 3;
-            const int tr = chunk >> 3, c8 = (chunk & 7) * 8;
-            const int e0 = cl * slot_elems + (row_off + tr + R + (ky - 1) * dil) * kWinCols + (c8 + 8 + (kx - 1) * dil);
-            const uint32_t* wp = xs32 + (e0 >> 1);
-            uint32_t a0 = wp[0], a1 = wp[1], a2 = wp[2], a3 = wp[3];
-            if (e0 & 1) {
-                const uint32_t a4 = wp[4];
-                a0 = __byte_perm(a0, a1, 0x5432);
-                a1 = __byte_perm(a1, a2, 0x5432);
-                a2 = __byte_perm(a2, a3, 0x5432);
-                a3 = __byte_perm(a3, a4, 0x5432);
+// One work unit is (channel c_local, 8-pixel chunk) for all nine taps: the grad
+// chunk is loaded once, and each of the three window rows as three aligned
+// 16-byte vectors (elements c8 .. c8+23 of the row, i.e. columns -8 .. +15 around
+// the chunk) from which the three horizontal taps, shifted by compile-time
+// multiples of the dilation DIL <= 8, are cut with byte permutes.  A warp's 16-byte
+// loads and stores touch each bank once per eight threads, so they run without
+// shared-memory bank conflicts.  Rows of channels c_local >= nc are written as
+// zeros; rows 126 and 127 of the block are never written (the caller zeroes them
+// once).
+template <int DIL>
+__device__ __forceinline__ void form_dk_tile_dil(uint8_t* dk, const uint32_t* xs32, const bf16* gs, int gstride,
+                                                 int nc, int slot_elems, int R, int row_off, int tid, int nthr) {
+    static_assert(DIL >= 1 && DIL <= 8, "the window holds 8 columns of halo");
+    const uint4* xs4 = reinterpret_cast<const uint4*>(xs32);
+    for (int u = tid; u < kCB * 16; u += nthr) {
+        const int cl = u >> 4, chunk = u & 15;
+        const int tr = chunk >> 3, c8 = (chunk & 7) * 8;
+        uint8_t* rowbase = dk + tr * 16384;
+        const int sw = chunk & 7;
+        if (cl >= nc) {
+#pragma unroll
+            for (int k = 0; k < 9; ++k) {
+                const int ol = cl * 9 + k;
+                *reinterpret_cast<uint4*>(rowbase + (ol >> 3) * 1024 + (ol & 7) * 128 + ((sw ^ (ol & 7)) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
             }
-            const uint4 gv = *reinterpret_cast<const uint4*>(gs + cl * kPx + chunk * 8);
-            v.x = bf2_mul(gv.x, a0);
-            v.y = bf2_mul(gv.y, a1);
-            v.z = bf2_mul(gv.z, a2);
-            v.w = bf2_mul(gv.w, a3);
+            continue;
         }
-        *reinterpret_cast<uint4*>(dk + (chunk >> 3) * 16384 + (ol >> 3) * 1024 + (ol & 7) * 128 +
-                                  (((chunk & 7) ^ (ol & 7)) << 4)) = v;
+        const uint4 gv = *reinterpret_cast<const uint4*>(gs + cl * gstride + chunk * 8);
+#pragma unroll
+        for (int ky = 0; ky < 3; ++ky) {
+            const int e = cl * slot_elems + (row_off + tr + R + (ky - 1) * DIL) * kWinCols + c8;   // multiple of 8
+            const uint4 q0 = xs4[(e >> 3)], q1 = xs4[(e >> 3) + 1], q2 = xs4[(e >> 3) + 2];
+            const uint32_t w[12] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w, q2.x, q2.y, q2.z, q2.w};
+#pragma unroll
+            for (int kx = 0; kx < 3; ++kx) {
+                const int off = 8 + (kx - 1) * DIL;              // element of tap kx's first pixel
+                uint32_t a[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int wi = (off >> 1) + i;
+                    a[i] = (off & 1) ? __byte_perm(w[wi], w[(wi + 1) < 12 ? wi + 1 : 11], 0x5432) : w[wi];
+                }
+                const int ol = cl * 9 + ky * 3 + kx;
+                uint4 v;
+                v.x = bf2_mul(gv.x, a[0]);
+                v.y = bf2_mul(gv.y, a[1]);
+                v.z = bf2_mul(gv.z, a[2]);
+                v.w = bf2_mul(gv.w, a[3]);
+                *reinterpret_cast<uint4*>(rowbase + (ol >> 3) * 1024 + (ol & 7) * 128 + ((sw ^ (ol & 7)) << 4)) = v;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void form_dk_tile(uint8_t* dk, const uint32_t* xs32, const bf16* gs, int gstride, int nrows,
+                                             int slot_elems, int R, int dil, int row_off, int tid, int nthr) {
+    const int nc = nrows / 9;
+    switch (dil) {
+        case 1: form_dk_tile_dil<1>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 2: form_dk_tile_dil<2>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 3: form_dk_tile_dil<3>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 4: form_dk_tile_dil<4>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 5: form_dk_tile_dil<5>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 6: form_dk_tile_dil<6>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 7: form_dk_tile_dil<7>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        default: form_dk_tile_dil<8>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+    }
+}
+
+// Zero the two padding rows (126, 127) of a dK^T tile.
+__device__ __forceinline__ void zero_dk_pad_rows(uint8_t* dk, int tid, int nthr) {
+    for (int u = tid; u < 2 * 2 * 8; u += nthr) {      // 2 rows x 2 halves x 8 chunks
+        const int ol = 126 + (u >> 4), half = (u >> 3) & 1, c = u & 7;
+        *reinterpret_cast<uint4*>(dk + half * 16384 + (ol >> 3) * 1024 + (ol & 7) * 128 + ((c ^ (ol & 7)) << 4)) =
+            make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
