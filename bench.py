@@ -78,7 +78,9 @@ def kernel_work(name: str, p, es: int, splits: int):
         return "alu", 2.0 * O * (C + 1) * P, "flops"
     if name == "bwd_dw_reduce":
         return "hbm", splits * O * (C + 1) * 4 + O * (C + 1) * es, "bytes"
-    if name in ("forward_tc", "bwd_dx_tc", "bwd_dy_tc", "bwd_dw_tc"):
+    if name == "pack_chunks":
+        return "hbm", 2 * P * 4 * C * es, "bytes"
+    if name in ("forward_tc", "bwd_dx_tc", "bwd_dx_tc_packed", "bwd_dy_tc", "bwd_dw_tc"):
         return "tensor", gemm, "flops"
     return "unknown", 0.0, "flops"
 

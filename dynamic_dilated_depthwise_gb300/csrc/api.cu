@@ -54,6 +54,11 @@ constexpr size_t kMaxSmem = 227 * 1024;
 
 size_t elem_size(int dtype) { return dtype == DDPM_BFLOAT16 ? 2 : 4; }
 
+// Workspace layout of ddpm_backward: the FP32 dW/dbias partial sums (the minimum
+// a caller must supply), then -- when the workspace is large enough -- the
+// channel-chunked copies of y and grad that the packed dX kernel reads.
+size_t packed_offset(const Dims& d) { return (ddpm::backward_simt_workspace(d) + 255) & ~size_t(255); }
+
 ddpm_status validate(const ddpm_problem* p, Dims* d) {
     if (p == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
     if (p->B < 1 || p->C < 1 || p->H < 1 || p->W < 1) return DDPM_ERR_INVALID_ARGUMENT;
@@ -142,7 +147,9 @@ ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* by
     Dims d;
     DDPM_TRY(validate(problem, &d));
     if (bytes == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
-    *bytes = ddpm::backward_simt_workspace(d);
+    *bytes = ddpm::bwd_dx_packed_shape_ok(d)
+                 ? packed_offset(d) + ddpm::bwd_dx_packed_bytes(d)
+                 : ddpm::backward_simt_workspace(d);
     return DDPM_OK;
 }
 
@@ -165,10 +172,19 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
     if (workspace_bytes < ddpm::backward_simt_workspace(d)) return DDPM_ERR_WORKSPACE_TOO_SMALL;
     try {
         const cudaStream_t s = (cudaStream_t)stream;
-        // each piece runs on the tensor-core kernel where one exists for the problem
-        cudaError_t e = ddpm::bwd_dx_tc_eligible(d, grad_out, y, weight)
-                            ? ddpm::launch_bwd_dx_tc(d, grad_out, y, weight, bias, dx, s)
-                            : ddpm::launch_bwd_dx_simt(d, grad_out, y, weight, bias, dx, s);
+        // each piece runs on the tensor-core kernel where one exists for the problem;
+        // dX takes the packed-operand kernel when the workspace also holds the copies
+        const size_t poff = packed_offset(d);
+        const bool packed = ddpm::bwd_dx_packed_eligible(d, grad_out, y, weight) &&
+                            workspace_bytes >= poff + ddpm::bwd_dx_packed_bytes(d);
+        const size_t part_bytes = packed ? poff : workspace_bytes;
+        cudaError_t e;
+        if (packed)
+            e = ddpm::launch_bwd_dx_packed(d, grad_out, y, weight, bias, dx, static_cast<char*>(workspace) + poff, s);
+        else if (ddpm::bwd_dx_tc_eligible(d, grad_out, y, weight))
+            e = ddpm::launch_bwd_dx_tc(d, grad_out, y, weight, bias, dx, s);
+        else
+            e = ddpm::launch_bwd_dx_simt(d, grad_out, y, weight, bias, dx, s);
         if (e == cudaSuccess) {
             if (ddpm::bwd_dy_tc_eligible(d, grad_out, x, weight))
                 e = ddpm::launch_bwd_dy_tc(d, grad_out, x, weight, dy, s);
@@ -177,7 +193,7 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
         }
         if (e == cudaSuccess) {
             if (ddpm::bwd_dw_tc_eligible(d, grad_out, x, y)) {
-                const int S = ddpm::bwd_dw_tc_splits(d, workspace_bytes);
+                const int S = ddpm::bwd_dw_tc_splits(d, part_bytes);
                 e = ddpm::launch_bwd_dw_tc(d, grad_out, x, y, (float*)workspace, S, s);
                 if (e == cudaSuccess) e = ddpm::launch_bwd_reduce(d, (const float*)workspace, S, dweight, dbias, s);
             } else {
@@ -223,3 +239,16 @@ const char* ddpm_status_string(ddpm_status status) {
 int ddpm_version(void) { return 100; }
 
 }  // extern "C"
+
+namespace ddpm {
+
+// Smallest workspace ddpm_backward accepts (the FP32 dW/dbias partial sums).
+ddpm_status backward_workspace_min(const ddpm_problem* problem, size_t* bytes) {
+    Dims d;
+    DDPM_TRY(validate(problem, &d));
+    if (bytes == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
+    *bytes = backward_simt_workspace(d);
+    return DDPM_OK;
+}
+
+}  // namespace ddpm

@@ -5,7 +5,9 @@
 // device memory, a real-time loop that forbids allocation after start-up, or
 // a plain C caller with no allocator for temporaries).  For them this entry
 // point keeps the backward's scratch -- the <= 16 FP32 dW/dbias partial sums
-// -- in a fixed device array that is part of the library itself.
+// -- in a fixed device array that is part of the library itself.  The array
+// holds no channel-chunked copies of y and grad, so dX runs on the kernel that
+// stages its operands itself.
 //
 // The array is a file-scope __device__ object of DDPM_NOALLOC_SCRATCH_BYTES.
 // Every GPU that loads this library holds it until the process exits.  Host
@@ -48,11 +50,15 @@ ddpm_status scratch_address(void** out) {
 
 }  // namespace
 
+namespace ddpm {
+ddpm_status backward_workspace_min(const ddpm_problem* problem, size_t* bytes);  // api.cu
+}
+
 extern "C" ddpm_status ddpm_backward_noalloc(const ddpm_problem* problem, const void* grad_out, const void* x,
                                              const void* y, const void* weight, const void* bias, void* dx,
                                              void* dy, void* dweight, void* dbias, ddpm_stream_t stream) {
     size_t need = 0;
-    const ddpm_status s = ddpm_backward_workspace_size(problem, &need);  // validates the problem
+    const ddpm_status s = ddpm::backward_workspace_min(problem, &need);  // validates the problem
     if (s != DDPM_OK) return s;
     if (need > DDPM_NOALLOC_SCRATCH_BYTES) return DDPM_ERR_UNSUPPORTED;  // partials exceed the fixed scratch
     void* scratch = nullptr;

@@ -146,6 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- MMA issuer
         if (lane == 0 && n_my > 0) {
             const uint32_t idesc = instr_desc(1, 0, 0, kBlockRows, kNY);   // both operands K-major
+            // descriptors are built once; each MMA only moves a start address (desc_advance)
+            const uint64_t dk_base = smem_desc(smem_u32(sm + kDK), 16, 1024, kSwizzle128B);
+            const uint64_t y_base = smem_desc(smem_u32(sm + kYS), 16, 1024, kSwizzle128B);
             bool ok = true;
             for (int i = 0; i < n_my && ok; ++i) {
                 const int s = i & 1, ph = (i >> 1) & 1;
@@ -154,15 +157,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t da = smem_u32(sm + kDK + s * kDKBytes);
-                const uint32_t ya = smem_u32(sm + kYS + s * kYStage);
+                const uint64_t da = desc_advance(dk_base, (uint32_t)s * kDKBytes);
+                const uint64_t ya = desc_advance(y_base, (uint32_t)s * kYStage);
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_f16(tmem, smem_desc(da + half * 16384 + kk * 32, 16, 1024, kSwizzle128B),
-                                smem_desc(ya + half * kYHalf + kk * 32, 16, 1024, kSwizzle128B), idesc,
-                                (i > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                        mma_f16(tmem, desc_advance(da, half * 16384 + kk * 32), desc_advance(ya, half * kYHalf + kk * 32),
+                                idesc, (i > 0 || half > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&dk_empty[s]);
                 mma_commit(&in_empty[s]);
             }

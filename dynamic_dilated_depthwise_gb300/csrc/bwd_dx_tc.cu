@@ -173,8 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- MMA issuer
         if (lane == 0 && n_my > 0) {
             const uint32_t idesc = instr_desc(1, 0, 0, 128, kN);
-            const uint32_t yw = smem_u32(sm + kYW);
             const uint32_t lbo_y = (uint32_t)npos * 16, sbo_y = (uint32_t)WW * 16;
+            // descriptors are built once; each MMA only moves a start address (desc_advance)
+            const uint64_t y_base = smem_desc(smem_u32(sm + kYW), lbo_y, sbo_y, kSwizzleNone);
+            const uint64_t w_base = smem_desc(smem_u32(sm + kWT), 16, 1024, kSwizzle128B);
+            const uint64_t bias_base = smem_desc(smem_u32(sm + kWT + 8192), 128, 256, kSwizzleNone);
             bool ok = true;
             for (int tl = 0; tl < n_my && ok; ++tl) {
                 if (!mbar_wait(&yw_full, tl & 1, P.err, abort_v)) break;
@@ -190,14 +193,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int dd = u / 9, k = u % 9, dil = dil_of(P.d, dd);
                     const int ky = k / 3, kx = k - ky * 3;
                     const uint32_t shift = (uint32_t)((R - (ky - 1) * dil) * WW + (R - (kx - 1) * dil)) * 16;
-                    const uint32_t wt = smem_u32(sm + kWT + st * kWTStage);
+                    const uint64_t ya = desc_advance(y_base, shift);
+                    const uint64_t wt = desc_advance(w_base, (uint32_t)st * kWTStage);
                     const uint32_t dt = tmem + buf * kN;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_f16(dt, smem_desc(yw + shift + 2 * kk * lbo_y, lbo_y, sbo_y, kSwizzleNone),
-                                smem_desc(wt + kk * 32, 16, 1024, kSwizzle128B), idesc, kk > 0);
-                    mma_f16(dt, smem_desc(yw + shift + 8 * lbo_y, lbo_y, sbo_y, kSwizzleNone),
-                            smem_desc(wt + 8192, 128, 256, kSwizzleNone), idesc, 1);
+                        mma_f16(dt, desc_advance(ya, 2 * kk * lbo_y), desc_advance(wt, kk * 32), idesc, kk > 0);
+                    mma_f16(dt, desc_advance(ya, 8 * lbo_y), desc_advance(bias_base, (uint32_t)st * kWTStage), idesc, 1);
                     mma_commit(&d_full[buf]);
                     mma_commit(&wt_empty[st]);
                 }
@@ -279,9 +281,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&yw_full);
 
+            // dx = grad (channel block 0) + the gathered sum: the accumulators start from the
+            // identity term, loaded now so that its latency hides behind the gather
+            const int h = h0 + r, w = w0 + c;
+            const bool inside = h < H && w < W;
+            const long long pix = inside ? (long long)h * W + w : 0;
             float acc[32];
+            {
+                const bf16* g0p = P.g + (long long)b * 4 * C * HW + pix;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+                for (int i = 0; i < 32; ++i) {
+                    const int ch = hc * 32 + i;
+                    acc[i] = (inside && ch < C) ? __bfloat162float(__ldg(g0p + (long long)ch * HW)) : 0.0f;
+                }
+            }
             for (int dd = 0; dd < 3 && ok; ++dd) {
                 const int dil = dil_of(P.d, dd);
                 // grad window of dilation dd: [position][64 channels] bf16, 16-byte chunks rotated by position
@@ -339,16 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
-            // dx = grad (channel block 0) + gathered sum
-            const int h = h0 + r, w = w0 + c;
-            if (h < H && w < W) {
-                const long long pix = (long long)h * W + w;
-                const bf16* g0p = P.g + (long long)b * 4 * C * HW + pix;
+            if (inside) {
                 bf16* dxp = P.dx + (long long)b * C * HW + pix;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int ch = hc * 32 + i;
-                    if (ch < C) dxp[(long long)ch * HW] = __float2bfloat16_rn(__bfloat162float(g0p[(long long)ch * HW]) + acc[i]);
+                    if (ch < C) dxp[(long long)ch * HW] = __float2bfloat16_rn(acc[i]);
                 }
             }
         }

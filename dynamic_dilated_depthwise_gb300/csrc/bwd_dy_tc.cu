@@ -129,6 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- MMA issuer
         if (lane == 0 && n_my > 0) {
             const uint32_t idesc = instr_desc(1, 1, 1, kPx, kN);   // A (dK) and B (W) MN-major
+            // descriptors are built once; each MMA only moves a start address (desc_advance)
+            const uint64_t dk_base = smem_desc(smem_u32(sm + kDK), 16384, 1024, kSwizzle128B);
+            const uint64_t w_base = smem_desc(smem_u32(sm + kWS), 8192, 1024, kSwizzle128B);
             bool ok = true;
             for (int tl = 0; tl < n_my && ok; ++tl) {
                 const int tb = tl & 1, tph = (tl >> 1) & 1;
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t wa = smem_u32(sm + kWS + s * kWStage);
+                    const uint64_t wa = desc_advance(w_base, (uint32_t)s * kWStage);
                     for (int st = 0; st < kSub; ++st) {
                         const int kd = i * kSub + st, db = kd & 1;
                         if (!mbar_wait(&dk_full[db], (kd >> 1) & 1, P.err, abort_v)) {
@@ -148,12 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t da = smem_u32(sm + kDK + db * kDKBytes);
+                        const uint64_t da = desc_advance(dk_base, (uint32_t)db * kDKBytes);
                         const uint32_t dt = tmem + (tb * kSub + st) * kN;
 #pragma unroll
                         for (int kk = 0; kk < kBlockRows / 16; ++kk)
-                            mma_f16(dt, smem_desc(da + kk * 2048, 16384, 1024, kSwizzle128B),
-                                    smem_desc(wa + kk * 2048, 8192, 1024, kSwizzle128B), idesc,
+                            mma_f16(dt, desc_advance(da, kk * 2048), desc_advance(wa, kk * 2048), idesc,
                                     (ob > 0 || kk > 0) ? 1u : 0u);
                         mma_commit(&dk_empty[db]);
                     }

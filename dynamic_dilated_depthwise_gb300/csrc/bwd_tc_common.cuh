@@ -156,12 +156,17 @@ inline bool encode_nchw(CUtensorMap* m, const void* base, const Dims& d, int ch,
 
 // Shapes the tensor-core backward handles: bf16, K = 3, C a multiple of 8 up to 64,
 // W a multiple of 8 (16-byte TMA strides), halo radius <= 8, 16-byte aligned tensors.
-inline bool eligible(const Dims& d, const void* a, const void* b, const void* c) {
+// shape_ok() is the part that depends on the problem alone.
+inline bool shape_ok(const Dims& d) {
     if (d.dtype != 1 || d.K != 3 || (d.flags & kFlagCudaCores)) return false;
     if (d.C > 64 || d.C % 8 != 0 || d.W % 8 != 0) return false;
     if (d.R() > kMaxR) return false;
+    return d.O <= (1LL << 30) && d.HW <= (1LL << 31) - 1024;
+}
+
+inline bool eligible(const Dims& d, const void* a, const void* b, const void* c) {
+    if (!shape_ok(d)) return false;
     if ((uintptr_t)a % 16 || (uintptr_t)b % 16 || (uintptr_t)c % 16) return false;
-    if (d.O > (1LL << 30) || d.HW > (1LL << 31) - 1024) return false;
     return encode_fn() != nullptr;
 }
 

@@ -47,7 +47,7 @@ template <> __device__ __forceinline__ float quantise_tap<__nv_bfloat16>(float t
 }
 
 // d.dil[di] without a dynamic index into the kernel parameter block
-__device__ __forceinline__ int dil_of(const Dims& d, int di) {
+__host__ __device__ __forceinline__ int dil_of(const Dims& d, int di) {
     return di == 0 ? d.dil[0] : (di == 1 ? d.dil[1] : d.dil[2]);
 }
 

@@ -200,12 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait(&bar_w, 0, P.err, abort_v);
             const uint32_t idesc = instr_desc(1, 1, 0, kTile, kN);     // A (y) MN-major, B (W) K-major
             const uint32_t idesc_b = instr_desc(1, 0, 0, kTile, kN);   // ones x bias, both K-major
+            // descriptors are built once; each MMA only moves a start address (desc_advance)
             const uint64_t d_ones = smem_desc(smem_u32(sm + kSOnes), 128, 256, kSwizzleNone);
+            const uint64_t y_base = smem_desc(smem_u32(sm + kSY), 8192, 1024, kSwizzle128B);
+            const uint64_t w_base = smem_desc(smem_u32(sm + kSW), 16, 1024, kSwizzle128B);
+            const uint64_t b_base = smem_desc(smem_u32(sm + kSBias), 128, 256, kSwizzleNone);
             for (int i = 0; ok && i < n_my; ++i) {
                 const int s = i & 1, ph = (i >> 1) & 1;
                 if (!mbar_wait(&bar_y_full[s], ph, P.err, abort_v)) break;
                 tc_fence_after();
-                const uint32_t ya = smem_u32(sm + kSY + s * 16384);
+                const uint64_t ya = desc_advance(y_base, (uint32_t)s * 16384);
                 for (int dd = 0; dd < 3 && ok; ++dd) {
                     if (!mbar_wait(&bar_acc_empty[dd], (i & 1) ^ 1, P.err, abort_v)) {
                         ok = false;
@@ -213,13 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t dt = tmem + dd * kN;
-                    const uint32_t wa = smem_u32(sm + kSW + dd * kN * 128);
+                    const uint64_t wa = desc_advance(w_base, (uint32_t)dd * kN * 128);
 #pragma unroll
                     for (int kk = 0; kk < kKPad / 16; ++kk)
-                        mma_f16(dt, smem_desc(ya + kk * 2048, 8192, 1024, kSwizzle128B),
-                                smem_desc(wa + kk * 32, 16, 1024, kSwizzle128B), idesc, kk > 0);
-                    mma_f16(dt, d_ones, smem_desc(smem_u32(sm + kSBias + dd * kN * 32), 128, 256, kSwizzleNone),
-                            idesc_b, 1);
+                        mma_f16(dt, desc_advance(ya, kk * 2048), desc_advance(wa, kk * 32), idesc, kk > 0);
+                    mma_f16(dt, d_ones, desc_advance(b_base, (uint32_t)dd * kN * 32), idesc_b, 1);
                     mma_commit(&bar_acc_full[dd]);
                 }
                 if (!ok) break;

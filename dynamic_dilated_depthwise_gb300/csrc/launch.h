@@ -21,7 +21,9 @@ enum KernelId : int {
     kKBwdDxTc = 7,
     kKBwdDyTc = 8,
     kKBwdDwTc = 9,
-    kKNumKernels = 10
+    kKPackChunks = 10,
+    kKBwdDxTcPacked = 11,
+    kKNumKernels = 12
 };
 
 // Tracing hooks around each launch (cheap no-ops while tracing is off).
@@ -79,6 +81,15 @@ cudaError_t launch_bwd_dw_tc(const Dims& d, const void* g, const void* x, const 
 bool bwd_dx_tc_eligible(const Dims& d, const void* g, const void* y, const void* w);
 cudaError_t launch_bwd_dx_tc(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
                              cudaStream_t s);
+
+// dX on tcgen05 tensor cores from channel-chunked copies of y and grad that the
+// launcher first writes into `packed` (bwd_dx_packed_bytes(d) bytes, 16-byte
+// aligned); the copies make the staging a plain TMA load (halo radius <= 6).
+bool bwd_dx_packed_shape_ok(const Dims& d);   // the problem alone (sizes the workspace)
+bool bwd_dx_packed_eligible(const Dims& d, const void* g, const void* y, const void* w);
+size_t bwd_dx_packed_bytes(const Dims& d);
+cudaError_t launch_bwd_dx_packed(const Dims& d, const void* g, const void* y, const void* w, const void* bias,
+                                 void* dx, void* packed, cudaStream_t s);
 
 // dY on tcgen05 tensor cores (same shapes as the dW kernel).
 bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w);

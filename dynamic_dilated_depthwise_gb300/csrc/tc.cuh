@@ -108,6 +108,15 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], "
+        "[%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -203,6 +212,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     d |= (uint64_t)1u << 46;
     d |= (uint64_t)(swizzle & 7u) << 61;
     return d;
+}
+
+// The descriptor `desc` with its start address moved by `bytes` (a multiple of 16).
+// Shared-memory addresses stay below 2^18, so the 14-bit address field cannot
+// carry into the next field: one 64-bit add replaces rebuilding the descriptor,
+// which keeps a single issuing thread's dependent-instruction chain short.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+    return desc + (uint64_t)(bytes >> 4);
 }
 
 // Instruction descriptor for kind::f16 / kind::tf32 with fp32 accumulation.

@@ -108,3 +108,25 @@ def test_workspace_is_at_most_16_partials(lib, B, C, H, W, K):
     if B * H * W >= 16 * 2048:
         assert n == 16 * O * (C + 1) * 4
     assert n < 64 << 20  # "a few MiB", independent of the image size
+
+
+def _partials_bytes(B, C, H, W, K):
+    S = min(16, max(1, -(-B * H * W // 2048)))
+    return S * 3 * C * K * K * (C + 1) * 4
+
+
+@pytest.mark.parametrize("B,C,H,W,K,dil,packed", [
+    (1, 64, 256, 256, 3, (1, 3, 5), True),    # partials + channel-chunked copies of y and grad for dX
+    (2, 24, 16, 32, 3, (1, 3, 5), True),
+    (2, 24, 15, 17, 3, (1, 3, 5), False),     # W not a multiple of 8: no tensor-core backward
+    (1, 64, 64, 64, 3, (2, 4, 6), False),     # halo radius 6 with wide windows: dX tiles do not fit
+    (1, 64, 128, 128, 5, (1, 3, 5), False),   # K = 5: CUDA-core backward
+])
+def test_bf16_workspace_adds_packed_copies(lib, B, C, H, W, K, dil, packed):
+    p = _prob(B=B, C=C, H=H, W=W, K=K, dilations=dil, dtype=binding.DDPM_BFLOAT16)
+    n = binding.ddpm_backward_workspace_size(p)
+    parts = _partials_bytes(B, C, H, W, K)
+    if packed:
+        assert n == ((parts + 255) // 256) * 256 + 4 * B * C * H * W * 2
+    else:
+        assert n == parts

@@ -68,8 +68,18 @@ def run_forward(d, p):
     return binding.forward(d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations)
 
 
-def run_backward(d, p, flags=0):
-    return binding.backward(d["grad_out"], d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations, flags=flags)
+def run_backward(d, p, flags=0, workspace=None):
+    return binding.backward(d["grad_out"], d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations, flags=flags,
+                            workspace=workspace)
+
+
+def min_workspace(d, p):
+    """A workspace that holds the dW/dbias partials but not the packed copies of y
+    and grad (4*B*C*H*W bf16 elements), so dX stages its operands itself."""
+    full = binding.backward_workspace_size(d["x"], p.K, p.dilations)
+    packed = 4 * p.B * p.C * p.H * p.W * 2
+    assert full > packed
+    return torch.empty(full - packed, dtype=torch.uint8, device=d["x"].device)
 
 
 # ------------------------------------------------------------ small, full --
@@ -179,14 +189,21 @@ def test_tc_backward_matches_oracle_and_cuda_cores(p):
     h = make_inputs(p, 800, "bfloat16")
     d = _dev(h)
     names = _traced_kernels(lambda: run_backward(d, p))
-    assert {"bwd_dx_tc", "bwd_dy_tc", "bwd_dw_tc"} <= set(names), f"expected the tensor-core backward, got {names}"
+    assert {"pack_chunks", "bwd_dx_tc_packed", "bwd_dy_tc", "bwd_dw_tc"} <= set(names), \
+        f"expected the tensor-core backward, got {names}"
+    ws = min_workspace(d, p)
+    names_small = _traced_kernels(lambda: run_backward(d, p, workspace=ws))
+    assert {"bwd_dx_tc", "bwd_dy_tc", "bwd_dw_tc"} <= set(names_small), names_small
+    assert "bwd_dx_tc_packed" not in names_small
     got = run_backward(d, p)
+    staged = run_backward(d, p, workspace=ws)
     simt = run_backward(d, p, flags=binding.DDPM_FLAG_CUDA_CORES)
     torch.cuda.synchronize()
     ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=True)
     for name, a, b, want in zip(("dx", "dy", "dW", "dbias"), got, simt, ref):
         assert_grad_close(a, want, "bfloat16", name)
         assert_grad_close(b, want, "bfloat16", name + " (cuda cores)")
+    assert_grad_close(staged[0], ref[0], "bfloat16", "dx (operands staged in the kernel)")
 
 
 @pytest.mark.parametrize("p", [Problem(1, 16, 8, 16, 3), Problem(1, 24, 4, 24, 3, (2, 2, 4)), Problem(2, 64, 4, 16, 3)],
@@ -195,12 +212,14 @@ def test_tc_backward_integer_bit_exact(p):
     """Integer inputs with at most 256 pixels: every dW / dbias sum is exact in bf16."""
     h = make_integer_inputs(p, 11, "bfloat16")
     d = _dev(h)
-    assert "bwd_dw_tc" in _traced_kernels(lambda: run_backward(d, p))
+    assert {"bwd_dx_tc_packed", "bwd_dw_tc"} <= set(_traced_kernels(lambda: run_backward(d, p)))
     dx, dy, dw, db = run_backward(d, p)
+    dx_staged = run_backward(d, p, workspace=min_workspace(d, p))[0]
     torch.cuda.synchronize()
     rdx, rdy, rdw, rdb = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations,
                                          bf16=True)
     np.testing.assert_array_equal(to64(dx), rdx)
+    np.testing.assert_array_equal(to64(dx_staged), rdx)
     np.testing.assert_array_equal(to64(dy), rdy)
     np.testing.assert_array_equal(to64(dw), rdw)
     np.testing.assert_array_equal(to64(db), rdb)
