@@ -59,7 +59,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tmX, const DyTcParams P) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1 KiB-aligned base, derived by pointer arithmetic on the shared array so that every
+    // access through it stays a shared-memory access (an integer round trip would make
+    // them generic loads and stores with 64-bit addresses)
+    uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ uint64_t in_full[2], in_empty[2], dk_full[2], dk_empty[2], acc_full[2], acc_empty[2], mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;

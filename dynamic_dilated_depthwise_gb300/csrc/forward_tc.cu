@@ -5,24 +5,26 @@
 // with the taps living only on chip; BF16 taps are rounded to bf16 before use.
 //
 // GB300 design.  A persistent CTA owns one group of 16 output channels and
-// walks pixel tiles of 128 pixels (one row segment, or several whole rows when
-// W < 128).  Per tile and dilation d the generator GEMM is
+// walks pixel tiles of 128 pixels (2 rows x 64 columns, or several whole rows
+// when W < 64).  Per tile and dilation d the generator GEMM is
 //   D[p, n] = sum_j y[j, p] * W[o_n, j] + bias[o_n],  n = c_local*9 + k  (144 columns)
 // issued as tcgen05.mma (M = 128 pixels, N = 144, K = 64 in four K=16 steps,
 // plus one K=16 step that adds the bias through a ones column) into TMEM:
 // TMEM lane = pixel, so each epilogue thread owns every tap of its pixel and
 // filters without any cross-thread reduction.
 //
-//   warp 0      TMA producer: W slice of the group (once), y tiles (2 stages),
-//               the raw x window of each tile ([16 ch][rows][cols] bf16)
+//   warp 0      TMA producer: W slice of the group (once), y tiles (2 stages)
 //   warp 1      TMEM owner + MMA issuer (one elected lane)
-//   warps 2..9  epilogue: transpose the raw x window to position-major
-//               [pos][16 ch] (so one 8-byte load brings four channels of one
-//               neighbour), read the taps from TMEM, round them to bf16,
-//               multiply by shifted x and store the 4C output channels.
+//   warp 2      TMA producer: the x window of each tile, one box per channel
+//               into a slot of fixed stride (3 buffers)
+//   warps 3..   epilogue: each thread owns one pixel and kCPT channels.  Per
+//               dilation it reads its 9*kCPT taps from TMEM, rounds each pair
+//               of channels' taps to bf16 with one conversion, and accumulates
+//               tap * x with the mixed-precision FMA (bf16 operands, FP32
+//               accumulator, exact product), x read as bf16 straight from the
+//               window at immediate offsets.
 // Three TMEM regions (one per dilation, 144 columns each) form the MMA /
-// epilogue pipeline; the raw window is refilled by TMA as soon as the previous
-// tile's window has been transposed, so its latency hides behind the filter.
+// epilogue pipeline: a region is released as soon as its taps are in registers.
 #include "bwd_tc_common.cuh"
 #include "tc.cuh"
 
@@ -36,9 +38,14 @@ constexpr int kTaps = 9;                 // K = 3
 constexpr int kN = kCG * kTaps;          // 144 MMA columns per dilation
 constexpr int kTile = 128;               // pixels per tile (MMA M)
 constexpr int kKPad = 64;                // generator K (channels of y), zero padded
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kWinMax = 1600;            // x window positions: (TH + 2R) x (TW + 16) <= 1600
+constexpr int kEpiWarps = 16;            // 4 TMEM lane quadrants x (16 / kCPT) channel sets
+constexpr int kEpi0 = 3;                 // first epilogue warp
+constexpr int kCPT = kCG / (kEpiWarps / 4);   // channels per epilogue thread
+constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
+constexpr int kWinMax = 1024;            // x window positions: (TH + 2R) x (TW + 16) <= 1024
+constexpr int kSlot = kWinMax * 2;       // bytes per channel slot of an x window buffer
+constexpr int kRawBufs = 3;              // x window buffers
+static_assert(kCPT % 2 == 0 && kEpiWarps % 4 == 0, "channel pairs per thread");
 
 // shared-memory carve-up (bytes, from a 1024-aligned base).  The 128-byte
 // swizzled operands come first so that every swizzle atom starts on 1024 B.
@@ -50,55 +57,67 @@ constexpr int kSBias = kSY + kSYBytes;                 // bias B operand, 3 x [1
 constexpr int kSBiasBytes = 3 * kN * 32;               // 13824
 constexpr int kSOnes = kSBias + kSBiasBytes;           // ones A operand [128 x 16] no swizzle
 constexpr int kSOnesBytes = kTile * 32;                // 4096
-constexpr int kSRaw = kSOnes + kSOnesBytes;            // raw x window [16 ch][rows][cols] bf16 (TMA)
-constexpr int kSRawBytes = kWinMax * kCG * 2;          // 51200
-constexpr int kSX = kSRaw + kSRawBytes;                // x window [pos][16 ch] bf16, 16-byte halves rotated
-constexpr int kSXBytes = kWinMax * kCG * 2;            // 51200
-constexpr int kSmemBytes = kSX + kSXBytes + 1024;      // + alignment slack
+constexpr int kSRaw = kSOnes + kSOnesBytes;            // 3 x x window [16 slots of kSlot B][rows][cols] bf16
+constexpr int kRawBuf = kCG * kSlot;                   // 32768
+constexpr int kSmemBytes = kSRaw + kRawBufs * kRawBuf + 1024;   // + alignment slack
 static_assert(kSW % 1024 == 0 && kSY % 1024 == 0 && (kSY + kSYBytes / 2) % 1024 == 0, "SW128 atoms need 1 KiB");
-static_assert(kSBias % 16 == 0 && kSOnes % 16 == 0 && kSRaw % 128 == 0 && kSX % 16 == 0, "operand alignment");
+static_assert(kSBias % 16 == 0 && kSOnes % 16 == 0 && kSRaw % 128 == 0 && kSlot % 128 == 0, "operand alignment");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
 
 struct FwdTcParams {
     Dims d;
-    int TH, TW;            // tile rows / columns (TH * TW <= 128)
-    int tiles_per_row;     // W >= 128: ceil(W / 128); else 1
+    int TH, TW;            // tile rows / columns (TH * TW = 128, or whole rows when W < 64)
+    int tiles_per_row;     // W >= 64: ceil(W / 64); else 1
     int tiles_per_img;
     int n_tiles;           // B * tiles_per_img
     int n_groups;          // ceil(C / 16)
     int ctas_per_group;
     int R;                 // halo radius = max dilation * (K / 2)
     int WH, WC;            // x window rows (TH + 2R) / columns (TW + 16, origin w0 - 8)
-    const bf16* x;
     const bf16* bias;      // may be null
     bf16* out;
     unsigned int* err;
 };
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
-
-// byte offset of the 16-byte half `h` (channels 8h..8h+7) of position pos in the
-// transposed window: the halves swap on every other group of four positions so
-// that eight consecutive positions hit distinct bank quads.
-__device__ __forceinline__ int xw_off(int pos, int h) { return pos * 32 + ((h ^ ((pos >> 2) & 1)) << 4); }
-
 struct TileCoord {
-    int b, h0, w0, nvalid;
+    int b, h0, w0;
 };
 
 __device__ __forceinline__ TileCoord tile_coord(const FwdTcParams& P, int t) {
     TileCoord c;
     c.b = t / P.tiles_per_img;
     const int ti = t % P.tiles_per_img;
-    if (P.TH == 1) {
-        c.h0 = ti / P.tiles_per_row;
-        c.w0 = (ti % P.tiles_per_row) * P.TW;
-        c.nvalid = min(P.TW, P.d.W - c.w0);
-    } else {
-        c.h0 = ti * P.TH;
-        c.w0 = 0;
-        c.nvalid = P.TW * min(P.TH, P.d.H - c.h0);
-    }
+    c.h0 = (ti / P.tiles_per_row) * P.TH;
+    c.w0 = (ti % P.tiles_per_row) * P.TW;
     return c;
+}
+
+// bf16x2 of two fp32 values (round to nearest even): lo in bits 0..15, hi in 16..31
+__device__ __forceinline__ uint32_t round_pair(uint32_t lo, uint32_t hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+    return r;
+}
+
+// a0 += lo(t) * x0, a1 += hi(t) * x1: bf16 operands, exact product, FP32 accumulate
+__device__ __forceinline__ void fma_pair(float& a0, float& a1, uint32_t t, unsigned short x0, unsigned short x1) {
+    asm("{\n\t.reg .b16 tl, th;\n\t"
+        "mov.b32 {tl, th}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, tl, %3, %0;\n\t"
+        "fma.rn.f32.bf16 %1, th, %4, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(t), "h"(x0), "h"(x1));
+}
+
+// n consecutive TMEM columns of this warp's lane quadrant into r[0..n)
+template <int NCOL>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
+#pragma unroll
+    for (int c = 0; c + 16 <= NCOL; c += 16) DDPM_TMEM_LD_X16(taddr + c, (r + c));
+    constexpr int rem = NCOL % 16;
+    if constexpr (rem == 8) DDPM_TMEM_LD_X8(taddr + (NCOL - 8), (r + NCOL - 8));
+    if constexpr (rem == 4) DDPM_TMEM_LD_X4(taddr + (NCOL - 4), (r + NCOL - 4));
+    static_assert(rem == 0 || rem == 4 || rem == 8, "column count");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -106,9 +125,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tmX, const FwdTcParams P) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_w, bar_y_full[2], bar_y_empty[2], bar_acc_full[3], bar_acc_empty[3], bar_raw_full,
-        bar_raw_empty, bar_done;
+    // 1 KiB-aligned base, derived by pointer arithmetic on the shared array so that every
+    // access through it stays a shared-memory access (an integer round trip would make
+    // them generic loads and stores with 64-bit addresses)
+    uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ uint64_t bar_w, bar_y_full[2], bar_y_empty[2], bar_acc_full[3], bar_acc_empty[3],
+        bar_raw_full[kRawBufs], bar_raw_empty[kRawBufs], bar_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -119,7 +141,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c0 = group * kCG;
     const int C = P.d.C;
     const long long HW = P.d.HW;
-    const int npos = P.WH * P.WC;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -128,19 +149,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bar_y_full[s], 1);
             mbar_init(&bar_y_empty[s], 1);
         }
+        for (int s = 0; s < kRawBufs; ++s) {
+            mbar_init(&bar_raw_full[s], 1);
+            mbar_init(&bar_raw_empty[s], kEpiWarps);
+        }
         for (int dd = 0; dd < 3; ++dd) {
             mbar_init(&bar_acc_full[dd], 1);
             mbar_init(&bar_acc_empty[dd], kEpiWarps);
         }
-        mbar_init(&bar_raw_full, 1);
-        mbar_init(&bar_raw_empty, kEpiWarps);
         mbar_init(&bar_done, 1);
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(&tmem_slot, 512);
-    if (warp >= 2) {
+    if (warp >= kEpi0) {
         // constant MMA operands: a ones column (A) and the bias column (B), K = 16, no swizzle
-        const int et = threadIdx.x - 64;
+        const int et = threadIdx.x - 32 * kEpi0;
         for (int i = et; i < kTile * 16; i += 32 * kEpiWarps) {
             const int m = i / 16, k = i % 16;
             *reinterpret_cast<bf16*>(sm + kSOnes + (m / 8) * 256 + (k / 8) * 128 + (m % 8) * 16 + (k % 8) * 2) =
@@ -167,12 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tmY);
             prefetch_tmap(&tmW);
-            prefetch_tmap(&tmX);
             mbar_arrive_expect_tx(&bar_w, 3 * kN * 128);
             for (int dd = 0; dd < 3; ++dd)
                 tma_load_2d(sm + kSW + dd * kN * 128, &tmW, &bar_w, 0, (dd * C + c0) * kTaps);
-            const uint32_t raw_bytes = (uint32_t)npos * kCG * 2;
-            int issued_y = 0, issued_x = 0;
+            // second 64-pixel half: the next row of a 2 x 64 tile, or the next 64 pixels of whole rows
+            const int half_step = P.TW == 64 ? P.d.W : 64;
+            int issued_y = 0;
             for (int i = 0; i < n_my; ++i) {
                 const int s = i & 1, ph = (i >> 1) & 1;
                 const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
@@ -180,19 +203,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int pb = tcd.h0 * P.d.W + tcd.w0;
                 mbar_arrive_expect_tx(&bar_y_full[s], kTile * kKPad * 2);
                 tma_load_3d(sm + kSY + s * 16384, &tmY, &bar_y_full[s], pb, 0, tcd.b);
-                tma_load_3d(sm + kSY + s * 16384 + 8192, &tmY, &bar_y_full[s], pb + 64, 0, tcd.b);
+                tma_load_3d(sm + kSY + s * 16384 + 8192, &tmY, &bar_y_full[s], pb + half_step, 0, tcd.b);
                 issued_y = i + 1;
-                if (!mbar_wait(&bar_raw_empty, (i & 1) ^ 1, P.err, abort_v)) break;
-                mbar_arrive_expect_tx(&bar_raw_full, raw_bytes);
-                tma_load_4d(sm + kSRaw, &tmX, &bar_raw_full, tcd.w0 - 8, tcd.h0 - P.R, c0, tcd.b);
-                issued_x = i + 1;
             }
-            // drain: every copy this CTA started must land before its shared memory is released
+            // drain: every copy this thread started must land before shared memory is released
             int never = 0;
             mbar_wait(&bar_w, 0, P.err, &never);
             for (int i = issued_y > 2 ? issued_y - 2 : 0; i < issued_y; ++i)
                 mbar_wait(&bar_y_full[i & 1], (i >> 1) & 1, P.err, &never);
-            if (issued_x > 0) mbar_wait(&bar_raw_full, (issued_x - 1) & 1, P.err, &never);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------- TMA producer: x windows
+        if (lane == 0) {
+            prefetch_tmap(&tmX);
+            const int nch = min(kCG, C - c0);                  // channel boxes inside the tensor
+            const uint32_t raw_bytes = (uint32_t)(nch * P.WH * P.WC * 2);
+            int issued_x = 0, s = 0, ph = 0;
+            for (int i = 0; i < n_my; ++i) {
+                const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
+                if (!mbar_wait(&bar_raw_empty[s], ph ^ 1, P.err, abort_v)) break;
+                mbar_arrive_expect_tx(&bar_raw_full[s], raw_bytes);
+                uint8_t* rb = sm + kSRaw + s * kRawBuf;
+                for (int c = 0; c < nch; ++c)
+                    tma_load_4d(rb + c * kSlot, &tmX, &bar_raw_full[s], tcd.w0 - 8, tcd.h0 - P.R, c0 + c, tcd.b);
+                issued_x = i + 1;
+                if (++s == kRawBufs) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            int never = 0;
+            for (int i = issued_x > kRawBufs ? issued_x - kRawBufs : 0; i < issued_x; ++i)
+                mbar_wait(&bar_raw_full[i % kRawBufs], (i / kRawBufs) & 1, P.err, &never);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -234,91 +276,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------- epilogue
-        const int ew = warp - 2;
+        const int ew = warp - kEpi0;
         const int q = warp & 3;          // TMEM lane quadrant this warp may access
-        const int g = ew >> 2;           // channel half: c_local in [8g, 8g+8)
+        const int cl0 = (ew >> 2) * kCPT;   // first local channel of this thread
         const int s = q * 32 + lane;     // pixel slot == TMEM lane
-        const int et = threadIdx.x - 64;
-        const bool slot_in_tile = s < P.TH * P.TW;
-        const int rr = slot_in_tile ? s / P.TW : 0;
-        const int cc = slot_in_tile ? s % P.TW : 0;
-        const int R = P.R, WC = P.WC;
-        const unsigned short* raw = reinterpret_cast<const unsigned short*>(sm + kSRaw);
-        uint8_t* xw = sm + kSX;
+        // slots beyond the tile (whole-row tiles of fewer than 128 pixels) read the window at
+        // pixel (0, 0) and store nothing, so every shared-memory read stays inside the window
+        const bool in_tile = s < P.TH * P.TW;
+        const int rr = in_tile ? s / P.TW : 0, cc = in_tile ? s % P.TW : 0;
+        const int WC = P.WC;
+        const int center = (rr + P.R) * WC + cc + 8;   // window position of this pixel
+        int buf = 0, bph = 0;
         for (int i = 0; i < n_my; ++i) {
             const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
-            epi_bar();  // every thread is done with the previous tile's transposed window
-            if (!mbar_wait(&bar_raw_full, i & 1, P.err, abort_v)) goto epilogue_done;
-            // transpose [16 ch][pos] -> [pos][16 ch] (bf16)
-            for (int pos = et; pos < npos; pos += 32 * kEpiWarps) {
-                uint32_t w[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    w[e] = (uint32_t)raw[(2 * e) * npos + pos] | ((uint32_t)raw[(2 * e + 1) * npos + pos] << 16);
-                *reinterpret_cast<uint4*>(xw + xw_off(pos, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4*>(xw + xw_off(pos, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-            epi_bar();  // window ready; the raw buffer may be refilled
-            if (lane == 0) mbar_arrive(&bar_raw_empty);
-            const bool valid = s < tcd.nvalid;
-            const long long p = (long long)(tcd.h0 + rr) * P.d.W + tcd.w0 + cc;
-            bf16* ob = P.out + (long long)tcd.b * 4 * C * HW;
+            const bool valid = in_tile && tcd.h0 + rr < P.d.H && tcd.w0 + cc < P.d.W;
+            const long long p = valid ? (long long)(tcd.h0 + rr) * P.d.W + tcd.w0 + cc : 0;
+            bf16* ob = P.out + (long long)tcd.b * 4 * C * HW + p;
+            // this thread's channel slots of the window: slot c at xr + c * kSlot / 2
+            const unsigned short* xr =
+                reinterpret_cast<const unsigned short*>(sm + kSRaw + buf * kRawBuf + cl0 * kSlot);
+            if (!mbar_wait(&bar_raw_full[buf], bph, P.err, abort_v)) goto epilogue_done;
             if (valid) {
                 // channels c0 .. c0+15 of the output are x itself
-                const int cpos = (rr + R) * WC + cc + 8;
-                const uint4 xv = *reinterpret_cast<const uint4*>(xw + xw_off(cpos, g));
-                const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = c0 + 8 * g + 2 * e;
-                    if (c < C) ob[(long long)c * HW + p] = __ushort_as_bfloat16((unsigned short)(xs[e] & 0xFFFFu));
-                    if (c + 1 < C) ob[(long long)(c + 1) * HW + p] = __ushort_as_bfloat16((unsigned short)(xs[e] >> 16));
+                for (int c = 0; c < kCPT; ++c) {
+                    const int ch = c0 + cl0 + c;
+                    if (ch < C) ob[(long long)ch * HW] = __ushort_as_bfloat16(xr[c * (kSlot / 2) + center]);
                 }
             }
             for (int dd = 0; dd < 3; ++dd) {
                 if (!mbar_wait(&bar_acc_full[dd], i & 1, P.err, abort_v)) goto epilogue_done;
                 tc_fence_after();
+                uint32_t t[kCPT * kTaps];
+                tmem_load_cols<kCPT * kTaps>(tmem + ((uint32_t)(q * 32) << 16) + dd * kN + cl0 * kTaps, t);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_acc_empty[dd]);
                 const int dil = dil_of(P.d, dd);
-                const int base = (rr + R) * WC + cc + 8;
-                for (int cq = 0; cq < 2; ++cq) {
-                    uint32_t t[36];
-                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + dd * kN + (8 * g + 4 * cq) * kTaps;
-                    DDPM_TMEM_LD_X16(ta, (t + 0));
-                    DDPM_TMEM_LD_X16(ta + 16, (t + 16));
-                    DDPM_TMEM_LD_X4(ta + 32, (t + 32));
-                    tmem_ld_wait();
-                    if (cq == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&bar_acc_empty[dd]);
-                    }
-                    if (!valid) continue;
-                    // taps rounded to bf16 (nearest even), two at a time
-                    float tr[36];
+                const unsigned short* xk[kTaps];
 #pragma unroll
-                    for (int e = 0; e < 18; ++e) {
-                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(t[2 * e]), __uint_as_float(t[2 * e + 1]));
-                        const uint32_t u = *reinterpret_cast<uint32_t*>(&h2);
-                        tr[2 * e] = __uint_as_float(u << 16);
-                        tr[2 * e + 1] = __uint_as_float(u & 0xFFFF0000u);
-                    }
-                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int k = 0; k < kTaps; ++k)
+                    xk[k] = xr + center + (k / 3 - 1) * dil * WC + (k % 3 - 1) * dil;
+                float acc[kCPT];
 #pragma unroll
-                    for (int k = 0; k < kTaps; ++k) {
-                        const int ky = k / 3, kx = k % 3;
-                        const int pos = base + (ky - 1) * dil * WC + (kx - 1) * dil;
-                        const uint2 xv = *reinterpret_cast<const uint2*>(xw + xw_off(pos, g) + cq * 8);
-                        acc[0] = fmaf(tr[0 * kTaps + k], __uint_as_float(xv.x << 16), acc[0]);
-                        acc[1] = fmaf(tr[1 * kTaps + k], __uint_as_float(xv.x & 0xFFFF0000u), acc[1]);
-                        acc[2] = fmaf(tr[2 * kTaps + k], __uint_as_float(xv.y << 16), acc[2]);
-                        acc[3] = fmaf(tr[3 * kTaps + k], __uint_as_float(xv.y & 0xFFFF0000u), acc[3]);
-                    }
+                for (int c = 0; c < kCPT; ++c) acc[c] = 0.0f;
 #pragma unroll
-                    for (int cl = 0; cl < 4; ++cl) {
-                        const int c = c0 + 8 * g + 4 * cq + cl;
-                        if (c < C) ob[(long long)((1 + dd) * C + c) * HW + p] = __float2bfloat16_rn(acc[cl]);
+                for (int k = 0; k < kTaps; ++k) {
+#pragma unroll
+                    for (int c = 0; c < kCPT; c += 2) {
+                        const uint32_t tp = round_pair(t[c * kTaps + k], t[(c + 1) * kTaps + k]);
+                        fma_pair(acc[c], acc[c + 1], tp, xk[k][c * (kSlot / 2)], xk[k][(c + 1) * (kSlot / 2)]);
                     }
                 }
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < kCPT; ++c) {
+                        const int ch = c0 + cl0 + c;
+                        if (ch < C) ob[(long long)((1 + dd) * C + ch) * HW] = __float2bfloat16_rn(acc[c]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_raw_empty[buf]);
+            if (++buf == kRawBufs) {
+                buf = 0;
+                bph ^= 1;
             }
         }
     epilogue_done:;
@@ -337,17 +360,16 @@ struct Tiling {
 
 Tiling tiling_of(const Dims& d) {
     Tiling t;
-    if (d.W >= kTile) {
-        t.TW = kTile;
-        t.TH = 1;
-        t.tiles_per_row = (d.W + kTile - 1) / kTile;
-        t.tiles_per_img = d.H * t.tiles_per_row;
+    if (d.W >= 64) {
+        t.TW = 64;
+        t.TH = 2;
+        t.tiles_per_row = (d.W + 63) / 64;
     } else {
         t.TW = d.W;
         t.TH = kTile / d.W < d.H ? kTile / d.W : d.H;
         t.tiles_per_row = 1;
-        t.tiles_per_img = (d.H + t.TH - 1) / t.TH;
     }
+    t.tiles_per_img = ((d.H + t.TH - 1) / t.TH) * t.tiles_per_row;
     t.R = d.R();
     t.WH = t.TH + 2 * t.R;
     t.WC = t.TW + 16;
@@ -398,7 +420,7 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    if (!bwdtc::encode_nchw(&tmX, x, d, d.C, (uint32_t)t.WC, (uint32_t)t.WH, kCG, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!bwdtc::encode_nchw(&tmX, x, d, d.C, (uint32_t)t.WC, (uint32_t)t.WH, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
     FwdTcParams P;
@@ -417,7 +439,6 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
     P.R = t.R;
     P.WH = t.WH;
     P.WC = t.WC;
-    P.x = static_cast<const bf16*>(x);
     P.bias = static_cast<const bf16*>(bias);
     P.out = static_cast<bf16*>(out);
     P.err = device_error_word();

@@ -59,6 +59,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete is suspended until
+// it completes or about `hint_ns` have passed, instead of returning at once: a
+// waiting warp then takes no issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 20000u;   // re-check abort / time limit at least this often
+
 // Wait for the phase with the given parity to complete.  Returns false (and
 // records kErrTimeout) if it has not after kWaitLimitNs, or if *abort is set
 // by another thread that gave up first.
@@ -67,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
         if (*abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             *abort = 1;
