@@ -33,36 +33,44 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kCG = 16;                  // output channels per CTA group
+constexpr int kCG = 8;                   // output channels per CTA group
 constexpr int kTaps = 9;                 // K = 3
-constexpr int kN = kCG * kTaps;          // 144 MMA columns per dilation
+constexpr int kN = 80;                   // MMA N per dilation: the group's 72 taps, padded to a multiple of 16
 constexpr int kTile = 128;               // pixels per tile (MMA M)
 constexpr int kKPad = 64;                // generator K (channels of y), zero padded
-constexpr int kEpiWarps = 16;            // 4 TMEM lane quadrants x (16 / kCPT) channel sets
+constexpr int kEpiWarps = 8;             // 4 TMEM lane quadrants x (kCG / kCPT) channel sets
 constexpr int kEpi0 = 3;                 // first epilogue warp
 constexpr int kCPT = kCG / (kEpiWarps / 4);   // channels per epilogue thread
 constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
-constexpr int kWinMax = 1024;            // x window positions: (TH + 2R) x (TW + 16) <= 1024
+constexpr int kCtasPerSm = 2;            // two co-resident CTAs: one's MMAs overlap the other's epilogue
+constexpr int kTmemCols = 256;           // 3 x kN columns, rounded up to a power of two
+constexpr int kWinMax = 960;             // x window positions: (TH + 2R) x (TW + 16) <= 960
 constexpr int kSlot = kWinMax * 2;       // bytes per channel slot of an x window buffer
-constexpr int kRawBufs = 3;              // x window buffers
+constexpr int kRawBufs = 2;              // x window buffers
+static_assert(kCG * kTaps <= kN && kN % 16 == 0 && 3 * kN <= kTmemCols, "MMA N and TMEM columns");
 static_assert(kCPT % 2 == 0 && kEpiWarps % 4 == 0, "channel pairs per thread");
 
 // shared-memory carve-up (bytes, from a 1024-aligned base).  The 128-byte
 // swizzled operands come first so that every swizzle atom starts on 1024 B.
 constexpr int kSW = 0;                                 // W slice, 3 x [144 x 128 B], SW128 K-major
-constexpr int kSWBytes = 3 * kN * 128;                 // 55296 = 54 KiB
+constexpr int kSWBytes = 3 * kN * 128;                 // 30720
 constexpr int kSY = kSW + kSWBytes;                    // y tiles, 2 x [64 j x 128 px] SW128 MN-major
 constexpr int kSYBytes = 2 * kTile * kKPad * 2;        // 32768
 constexpr int kSBias = kSY + kSYBytes;                 // bias B operand, 3 x [144 x 16] no swizzle
-constexpr int kSBiasBytes = 3 * kN * 32;               // 13824
+constexpr int kSBiasBytes = 3 * kN * 32;               // 7680
 constexpr int kSOnes = kSBias + kSBiasBytes;           // ones A operand [128 x 16] no swizzle
 constexpr int kSOnesBytes = kTile * 32;                // 4096
-constexpr int kSRaw = kSOnes + kSOnesBytes;            // 3 x x window [16 slots of kSlot B][rows][cols] bf16
-constexpr int kRawBuf = kCG * kSlot;                   // 32768
-constexpr int kSmemBytes = kSRaw + kRawBufs * kRawBuf + 1024;   // + alignment slack
+constexpr int kSRaw = kSOnes + kSOnesBytes;            // 2 x x window [8 slots of kSlot B][rows][cols] bf16
+constexpr int kRawBuf = kCG * kSlot;                   // 15360
+constexpr int kSStage = kSRaw + kRawBufs * kRawBuf;    // output staging, 4 blocks x [8 ch][TH][TW] bf16
+constexpr int kStageBlk = kCG * kTile * 2;             // 2048
+constexpr int kSmemBytes = kSStage + 4 * kStageBlk + 1024;   // + alignment slack
 static_assert(kSW % 1024 == 0 && kSY % 1024 == 0 && (kSY + kSYBytes / 2) % 1024 == 0, "SW128 atoms need 1 KiB");
-static_assert(kSBias % 16 == 0 && kSOnes % 16 == 0 && kSRaw % 128 == 0 && kSlot % 128 == 0, "operand alignment");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
+static_assert(kSBias % 16 == 0 && kSOnes % 16 == 0 && kSRaw % 128 == 0 && kSlot % 128 == 0 && kSStage % 128 == 0,
+              "operand alignment");
+static_assert(kCPT == 4, "the epilogue's load / store sequences are written out for four channels");
+// two blocks per SM: 2 x (dynamic + ~0.2 KiB static + 1 KiB reserved) within the SM's 228 KiB
+static_assert(kCtasPerSm * (kSmemBytes + 256 + 1024) <= 228 * 1024, "shared memory of two co-resident blocks");
 
 struct FwdTcParams {
     Dims d;
@@ -70,12 +78,11 @@ struct FwdTcParams {
     int tiles_per_row;     // W >= 64: ceil(W / 64); else 1
     int tiles_per_img;
     int n_tiles;           // B * tiles_per_img
-    int n_groups;          // ceil(C / 16)
+    int n_groups;          // C / 8
     int ctas_per_group;
     int R;                 // halo radius = max dilation * (K / 2)
     int WH, WC;            // x window rows (TH + 2R) / columns (TW + 16, origin w0 - 8)
     const bf16* bias;      // may be null
-    bf16* out;
     unsigned int* err;
 };
 
@@ -109,6 +116,8 @@ __device__ __forceinline__ void fma_pair(float& a0, float& a1, uint32_t t, unsig
         : "r"(t), "h"(x0), "h"(x1));
 }
 
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
+
 // n consecutive TMEM columns of this warp's lane quadrant into r[0..n)
 template <int NCOL>
 __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
@@ -120,9 +129,10 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
     static_assert(rem == 0 || rem == 4 || rem == 8, "column count");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     forward_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmW,
-                      const __grid_constant__ CUtensorMap tmX, const FwdTcParams P) {
+                      const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
+                      const FwdTcParams P) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB-aligned base, derived by pointer arithmetic on the shared array so that every
@@ -140,7 +150,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cta_in_group = blockIdx.x / P.n_groups;
     const int c0 = group * kCG;
     const int C = P.d.C;
-    const long long HW = P.d.HW;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bar_done, 1);
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(&tmem_slot, 512);
+    if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
     if (warp >= kEpi0) {
         // constant MMA operands: a ones column (A) and the bias column (B), K = 16, no swizzle
         const int et = threadIdx.x - 32 * kEpi0;
@@ -276,36 +285,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------- epilogue
+        // Results go to a staging block [8 ch][TH][TW] per output block (x, d1, d3, d5),
+        // which one thread writes out with TMA stores once every epilogue warp has filled it;
+        // the stores clip pixels outside the image.
         const int ew = warp - kEpi0;
         const int q = warp & 3;          // TMEM lane quadrant this warp may access
         const int cl0 = (ew >> 2) * kCPT;   // first local channel of this thread
         const int s = q * 32 + lane;     // pixel slot == TMEM lane
+        const bool leader = ew == 0 && lane == 0;   // issues the TMA stores
         // slots beyond the tile (whole-row tiles of fewer than 128 pixels) read the window at
-        // pixel (0, 0) and store nothing, so every shared-memory read stays inside the window
-        const bool in_tile = s < P.TH * P.TW;
+        // pixel (0, 0) and store nothing, so every shared-memory access stays inside its buffer
+        const int tpix = P.TH * P.TW;
+        const bool in_tile = s < tpix;
         const int rr = in_tile ? s / P.TW : 0, cc = in_tile ? s % P.TW : 0;
         const int WC = P.WC;
         const int center = (rr + P.R) * WC + cc + 8;   // window position of this pixel
+        const uint32_t ch_stride = (uint32_t)tpix * 2;   // staging bytes per channel
+        // this thread's first staging element of block 0
+        const uint32_t st0 = smem_u32(sm + kSStage) + (uint32_t)cl0 * ch_stride + (uint32_t)(in_tile ? s : 0) * 2;
         int buf = 0, bph = 0;
+        // hand staging block blk of tile tcd to the TMA: called by every epilogue thread after
+        // writing its values, the same number of times by all of them even after a failed
+        // wait (the named barrier has no time limit); the leader first makes sure the block
+        // written next is no longer being read by the store issued three blocks ago
+        bool ok = true;
+        auto flush_block = [&](int blk, const TileCoord& tcd) {
+            fence_proxy_async_smem();
+            if (leader) bulk_wait_read<2>();
+            epi_bar();
+            if (leader && ok) {
+                const int cbase = (blk == 0 ? 0 : blk * C) + c0;
+                const uint8_t* src = sm + kSStage + blk * kStageBlk;
+                tma_store_4d(&tmO, src, tcd.w0, tcd.h0, cbase, tcd.b);
+                bulk_commit();
+            }
+        };
         for (int i = 0; i < n_my; ++i) {
             const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
-            const bool valid = in_tile && tcd.h0 + rr < P.d.H && tcd.w0 + cc < P.d.W;
-            const long long p = valid ? (long long)(tcd.h0 + rr) * P.d.W + tcd.w0 + cc : 0;
-            bf16* ob = P.out + (long long)tcd.b * 4 * C * HW + p;
-            // this thread's channel slots of the window: slot c at xr + c * kSlot / 2
-            const unsigned short* xr =
-                reinterpret_cast<const unsigned short*>(sm + kSRaw + buf * kRawBuf + cl0 * kSlot);
-            if (!mbar_wait(&bar_raw_full[buf], bph, P.err, abort_v)) goto epilogue_done;
-            if (valid) {
-                // channels c0 .. c0+15 of the output are x itself
-#pragma unroll
-                for (int c = 0; c < kCPT; ++c) {
-                    const int ch = c0 + cl0 + c;
-                    if (ch < C) ob[(long long)ch * HW] = __ushort_as_bfloat16(xr[c * (kSlot / 2) + center]);
-                }
+            // this thread's channel slots of the window: slot c at xa + c * kSlot
+            const uint32_t xa = smem_u32(sm + kSRaw + buf * kRawBuf + cl0 * kSlot) + (uint32_t)center * 2;
+            // waits are made warp-uniform (tcgen05.ld is a whole-warp instruction) and sticky:
+            // after a failure the thread only keeps the barrier sequence
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw_full[buf], bph, P.err, abort_v));
+            // channels c0 .. c0+7 of the output are x itself
+            if (ok && in_tile) {
+                const unsigned short v0 = lds_u16<0 * kSlot>(xa), v1 = lds_u16<1 * kSlot>(xa);
+                const unsigned short v2 = lds_u16<2 * kSlot>(xa), v3 = lds_u16<3 * kSlot>(xa);
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0), "h"(v0) : "memory");
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0 + ch_stride), "h"(v1) : "memory");
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0 + 2 * ch_stride), "h"(v2) : "memory");
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0 + 3 * ch_stride), "h"(v3) : "memory");
             }
+            flush_block(0, tcd);
             for (int dd = 0; dd < 3; ++dd) {
-                if (!mbar_wait(&bar_acc_full[dd], i & 1, P.err, abort_v)) goto epilogue_done;
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[dd], i & 1, P.err, abort_v));
+                if (!ok) {
+                    flush_block(1 + dd, tcd);
+                    continue;
+                }
                 tc_fence_after();
                 uint32_t t[kCPT * kTaps];
                 tmem_load_cols<kCPT * kTaps>(tmem + ((uint32_t)(q * 32) << 16) + dd * kN + cl0 * kTaps, t);
@@ -314,10 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar_acc_empty[dd]);
                 const int dil = dil_of(P.d, dd);
-                const unsigned short* xk[kTaps];
+                unsigned short xv[kTaps][kCPT];
 #pragma unroll
-                for (int k = 0; k < kTaps; ++k)
-                    xk[k] = xr + center + (k / 3 - 1) * dil * WC + (k % 3 - 1) * dil;
+                for (int k = 0; k < kTaps; ++k) {
+                    const uint32_t a = xa + (uint32_t)(((k / 3 - 1) * WC + (k % 3 - 1)) * dil * 2);
+                    xv[k][0] = lds_u16<0 * kSlot>(a);
+                    xv[k][1] = lds_u16<1 * kSlot>(a);
+                    xv[k][2] = lds_u16<2 * kSlot>(a);
+                    xv[k][3] = lds_u16<3 * kSlot>(a);
+                }
                 float acc[kCPT];
 #pragma unroll
                 for (int c = 0; c < kCPT; ++c) acc[c] = 0.0f;
@@ -326,31 +368,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < kCPT; c += 2) {
                         const uint32_t tp = round_pair(t[c * kTaps + k], t[(c + 1) * kTaps + k]);
-                        fma_pair(acc[c], acc[c + 1], tp, xk[k][c * (kSlot / 2)], xk[k][(c + 1) * (kSlot / 2)]);
+                        fma_pair(acc[c], acc[c + 1], tp, xv[k][c], xv[k][c + 1]);
                     }
                 }
-                if (valid) {
-#pragma unroll
-                    for (int c = 0; c < kCPT; ++c) {
-                        const int ch = c0 + cl0 + c;
-                        if (ch < C) ob[(long long)((1 + dd) * C + ch) * HW] = __float2bfloat16_rn(acc[c]);
-                    }
+                if (in_tile) {
+                    const uint32_t o01 = round_pair(__float_as_uint(acc[0]), __float_as_uint(acc[1]));
+                    const uint32_t o23 = round_pair(__float_as_uint(acc[2]), __float_as_uint(acc[3]));
+                    const uint32_t sa = st0 + (uint32_t)(1 + dd) * kStageBlk;
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa), "h"((unsigned short)(o01 & 0xFFFFu)) : "memory");
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa + ch_stride), "h"((unsigned short)(o01 >> 16)) : "memory");
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa + 2 * ch_stride), "h"((unsigned short)(o23 & 0xFFFFu)) : "memory");
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa + 3 * ch_stride), "h"((unsigned short)(o23 >> 16)) : "memory");
                 }
+                if (dd == 2) {
+                    // the window has been read for the last time
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_raw_empty[buf]);
+                }
+                flush_block(1 + dd, tcd);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar_raw_empty[buf]);
             if (++buf == kRawBufs) {
                 buf = 0;
                 bph ^= 1;
             }
         }
-    epilogue_done:;
+        // every store has finished writing global memory (and reading shared memory)
+        if (leader) bulk_wait<0>();
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -396,6 +445,8 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
     static int attr_done = 0;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(forward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(forward_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         attr_done = 1;
     }
@@ -403,7 +454,7 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
     if (enc == nullptr) return cudaErrorNotSupported;
     if ((uintptr_t)x % 16 != 0) return cudaErrorInvalidValue;
     const Tiling t = tiling_of(d);
-    CUtensorMap tmY, tmW, tmX;
+    CUtensorMap tmY, tmW, tmX, tmO;
     const cuuint64_t dimY[3] = {(cuuint64_t)d.HW, (cuuint64_t)d.C, (cuuint64_t)d.B};
     const cuuint64_t strY[2] = {(cuuint64_t)d.HW * 2, (cuuint64_t)d.HW * d.C * 2};
     const cuuint32_t boxY[3] = {64, (cuuint32_t)kKPad, 1};
@@ -422,6 +473,10 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
         return cudaErrorInvalidValue;
     if (!bwdtc::encode_nchw(&tmX, x, d, d.C, (uint32_t)t.WC, (uint32_t)t.WH, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
+    // output [B, 4C, H, W]: boxes of 8 channels x one tile, written from the staging blocks
+    if ((uintptr_t)out % 16 != 0 ||
+        !bwdtc::encode_nchw(&tmO, out, d, 4 * d.C, (uint32_t)t.TW, (uint32_t)t.TH, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
 
     FwdTcParams P;
     P.d = d;
@@ -431,7 +486,7 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
     P.tiles_per_img = t.tiles_per_img;
     P.n_tiles = d.B * t.tiles_per_img;
     P.n_groups = (d.C + kCG - 1) / kCG;
-    const int sms = num_sms();
+    const int sms = num_sms() * kCtasPerSm;
     int cpg = sms / P.n_groups;
     if (cpg < 1) cpg = 1;
     if (cpg > P.n_tiles) cpg = P.n_tiles;
@@ -440,11 +495,10 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
     P.WH = t.WH;
     P.WC = t.WC;
     P.bias = static_cast<const bf16*>(bias);
-    P.out = static_cast<bf16*>(out);
     P.err = device_error_word();
     if (P.err == nullptr) return cudaErrorUnknown;
     trace_begin(s, kKForwardTc);
-    forward_tc_kernel<<<P.n_groups * cpg, kThreads, kSmemBytes, s>>>(tmY, tmW, tmX, P);
+    forward_tc_kernel<<<P.n_groups * cpg, kThreads, kSmemBytes, s>>>(tmY, tmW, tmX, tmO, P);
     trace_end(s);
     return cudaGetLastError();
 }
