@@ -297,8 +297,14 @@ __global__ void __launch_bounds__(256) dw_reduce_kernel(Dims d, const float* __r
     const long long n = d.O * (d.C + 1);
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (long long)gridDim.x * blockDim.x) {
+        // all partial loads are issued before the sum, which then runs in the fixed order s = 0, 1, ...
+        float part[kMaxSplits];
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s) part[s] = s < S ? __ldcs(ws + (long long)s * n + e) : 0.0f;
         float v = 0.0f;
-        for (int s = 0; s < S; ++s) v += ws[(long long)s * n + e];
+#pragma unroll
+        for (int s = 0; s < kMaxSplits; ++s)
+            if (s < S) v += part[s];
         const long long o = e / (d.C + 1);
         const int j = (int)(e % (d.C + 1));
         if (j < d.C) dw[o * d.C + j] = from_f<T>(v);
