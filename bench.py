@@ -32,6 +32,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "DDPM fused fwd+bwd Mpixel/s (C=64,K=3,256² bf16, 1 GB300); % of roofline"
+# metric names of the other steps (--step forward / filter), same unit
+STEP_METRIC = {"train": METRIC,
+               "forward": "DDPM fused generator+filter forward Mpixel/s (1 GB300); % of roofline",
+               "filter": "DDPM filter with pregenerated taps Mpixel/s (1 GB300); % of HBM roofline"}
 UNIT = "Mpixel/s"
 DEFAULT_WORKLOAD = "b1_c64_256x256_k3"
 FLUSH_BYTES = 256 << 20
@@ -85,17 +89,25 @@ def kernel_work(name: str, p, es: int, splits: int):
     return "unknown", 0.0, "flops"
 
 
-def step_roofline_us(p, es: int, peaks) -> dict:
-    """Roofline of one fwd+bwd step: max(GEMM flops at the bf16 tensor peak,
-    minimum bytes at the HBM peak).  Four contractions of 2*O*C flops per pixel
-    (generator, generator recompute for dX, dY, dW); bytes: x, y, weight, bias
-    and grad read once, out / dx / dy / dW / dbias written once."""
+def step_roofline_us(p, es: int, peaks, step: str = "train") -> dict:
+    """Roofline of one step: max(GEMM flops at the bf16 tensor peak, minimum
+    bytes at the HBM peak).
+      train   (fwd+bwd): four contractions of 2*O*C flops per pixel (generator,
+              generator recompute for dX, dY, dW); x, y, weight, bias and grad
+              read once, out / dx / dy / dW / dbias written once;
+      forward: one contraction; x, y, weight, bias read, out written;
+      filter:  no contraction; x and the taps read, out written."""
     P = p.B * p.H * p.W
-    flops = 4 * 2.0 * p.O * p.C * P
-    fwd_bytes = P * (2 * p.C + 4 * p.C) * es
-    bwd_bytes = P * (4 * p.C + 2 * p.C + 2 * p.C) * es
-    w_bytes = 2 * (p.O * p.C + p.O) * es * 2
-    nbytes = fwd_bytes + bwd_bytes + w_bytes
+    w_bytes = (p.O * p.C + p.O) * es
+    if step == "train":
+        flops = 4 * 2.0 * p.O * p.C * P
+        nbytes = P * (2 * p.C + 4 * p.C) * es + P * (4 * p.C + 2 * p.C + 2 * p.C) * es + 4 * w_bytes
+    elif step == "forward":
+        flops = 2.0 * p.O * p.C * P
+        nbytes = P * (2 * p.C + 4 * p.C) * es + w_bytes
+    else:
+        flops = 0.0
+        nbytes = P * (p.C + p.O + 4 * p.C) * es
     t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
     return {"flops": flops, "bytes": nbytes, "tensor_us": t_tc, "hbm_us": t_hbm, "roofline_us": max(t_tc, t_hbm)}
@@ -217,26 +229,32 @@ def max_over_ranks(world, value: float) -> float:
     return float(t.item())
 
 
-def cpu_baseline(p, dtype: str, target_s: float = 10.0) -> dict:
-    """The oracle as it stands, on the host cores: fwd+bwd of the full image,
-    repeated until about target_s of CPU time (at most 3 repetitions)."""
+def cpu_baseline(p, dtype: str, target_s: float = 10.0, step: str = "train") -> dict:
+    """The oracle as it stands, on the host cores: the step on the full image
+    (one image of the batch), repeated until about target_s of CPU time (at most
+    5 repetitions)."""
     import oracle
     from dynamic_dilated_depthwise_gb300.inputs import Problem, SEEDS, make_inputs
     one = Problem(1, p.C, p.H, p.W, p.K, p.dilations)
-    h = make_inputs(one, SEEDS.get(p.name, 1000), dtype)
+    h = make_inputs(one, SEEDS.get(p.name, 1000), dtype, grad=step == "train", taps=step == "filter")
     h = {k: v.double().numpy() for k, v in h.items()}
     bf = dtype == "bfloat16"
     oracle.build()
     reps, t_total = 0, 0.0
-    while reps < 3 and (reps == 0 or t_total < target_s):
+    while reps < 5 and (reps == 0 or t_total < target_s):
         t0 = time.perf_counter()
-        oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
-        oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
+        if step == "filter":
+            oracle.filter_pregenerated(h["x"], h["taps"], p.K, p.dilations)
+        else:
+            oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
+        if step == "train":
+            oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
         t_total += time.perf_counter() - t0
         reps += 1
     px = reps * one.pixels
+    what = {"train": "fwd+bwd", "forward": "forward", "filter": "filter-only"}[step]
     return {"value": px / t_total / 1e6, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{reps} x fwd+bwd of one {p.H}x{p.W} image (C={p.C}, K={p.K}, {dtype}-valued inputs, FP64 math)",
+            "sample": f"{reps} x {what} of one {p.H}x{p.W} image (C={p.C}, K={p.K}, {dtype}-valued inputs, FP64 math)",
             "seconds": round(t_total, 3)}
 
 
@@ -252,15 +270,21 @@ def run_ours(args, world, rank, local):
     p = WORKLOADS[args.workload]
     dtype = args.dtype
     es = 2 if dtype == "bfloat16" else 4
-    h = make_inputs(p, SEEDS[p.name] + rank, dtype)
+    step_kind = args.step
+    h = make_inputs(p, SEEDS[p.name] + rank, dtype, grad=step_kind == "train", taps=step_kind == "filter")
+    if step_kind == "filter":
+        h = {k: h[k] for k in ("x", "taps")}
+    elif step_kind == "forward":
+        h = {k: h[k] for k in ("x", "y", "weight", "bias")}
     d = {k: v.to(dev) for k, v in h.items()}
     flags = binding.DDPM_FLAG_TF32_BACKWARD
     prob = binding.make_problem(p.B, p.C, p.H, p.W, p.K, p.dilations,
                                 binding.DDPM_BFLOAT16 if dtype == "bfloat16" else binding.DDPM_FLOAT32, flags)
     out = torch.empty((p.B, 4 * p.C, p.H, p.W), dtype=d["x"].dtype, device=dev)
-    dx, dy = torch.empty_like(d["x"]), torch.empty_like(d["y"])
-    dw, db = torch.empty_like(d["weight"]), torch.empty_like(d["bias"])
-    ws_bytes = binding.ddpm_backward_workspace_size(prob)
+    dx, dy = torch.empty_like(d["x"]), torch.empty_like(d["x"])
+    dw = torch.empty((p.O, p.C), dtype=d["x"].dtype, device=dev)
+    db = torch.empty((p.O,), dtype=d["x"].dtype, device=dev)
+    ws_bytes = binding.ddpm_backward_workspace_size(prob) if step_kind == "train" else 0
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -271,10 +295,15 @@ def run_ours(args, world, rank, local):
     pref = ctypes.byref(prob)
 
     def step():
-        s1 = lib.ddpm_forward(pref, ptr["x"], ptr["y"], ptr["weight"], ptr["bias"], out.data_ptr(), sh)
-        s2 = lib.ddpm_backward(pref, ptr["grad_out"], ptr["x"], ptr["y"], ptr["weight"], ptr["bias"],
-                               dx.data_ptr(), dy.data_ptr(), dw.data_ptr(), db.data_ptr(), ws.data_ptr(),
-                               ws.numel(), sh)
+        if step_kind == "filter":
+            s1, s2 = lib.ddpm_filter_pregenerated(pref, ptr["x"], ptr["taps"], out.data_ptr(), sh), 0
+        else:
+            s1 = lib.ddpm_forward(pref, ptr["x"], ptr["y"], ptr["weight"], ptr["bias"], out.data_ptr(), sh)
+            s2 = 0
+        if step_kind == "train":
+            s2 = lib.ddpm_backward(pref, ptr["grad_out"], ptr["x"], ptr["y"], ptr["weight"], ptr["bias"],
+                                   dx.data_ptr(), dy.data_ptr(), dw.data_ptr(), db.data_ptr(), ws.data_ptr(),
+                                   ws.numel(), sh)
         if s1 or s2:
             raise RuntimeError(f"library error {binding.status_string(s1 or s2)}")
 
@@ -337,7 +366,7 @@ def run_ours(args, world, rank, local):
     kernels = {k: {"launches_per_step": len(v) / args.steps, "avg_us": round(sum(v) / len(v) * 1e3, 3),
                    "share": round(sum(v) / sum(sum(x) for x in per_kernel.values()), 4)}
                for k, v in per_kernel.items()}
-    sr = step_roofline_us(p, es, peaks)
+    sr = step_roofline_us(p, es, peaks, step_kind)
     step_roof = {"roofline_us": round(sr["roofline_us"], 3), "tensor_us": round(sr["tensor_us"], 3),
                  "hbm_us": round(sr["hbm_us"], 3), "measured_us": round(ms_per_step * 1e3, 3),
                  "frac": round(sr["roofline_us"] / (ms_per_step * 1e3), 4)}
@@ -351,6 +380,9 @@ def run_ours(args, world, rank, local):
             "dw": torch.empty(dw.shape, dtype=dw.dtype).pin_memory(),
             "db": torch.empty(db.shape, dtype=db.dtype).pin_memory()}
     dres = {"out": out, "dx": dx, "dy": dy, "dw": dw, "db": db}
+    if step_kind != "train":
+        hout = {"out": hout["out"]}
+        dres = {"out": out}
     bi = sum(v.numel() * v.element_size() for v in hin.values())
     bo = sum(v.numel() * v.element_size() for v in hout.values())
     es_, ee_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -372,13 +404,15 @@ def run_ours(args, world, rank, local):
            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": round(e2e_ms, 4)}
     assert binding.ddpm_get_device_error() == 0
 
-    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+    line = {"metric": STEP_METRIC[step_kind], "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dtype == "bfloat16" else "f32",
             "data": "synthetic (seeded N(0,1) x, y, grad; weight N(0,1/C); bias N(0,0.01))",
             "config": {"workload": p.name, "B": p.B, "C": p.C, "H": p.H, "W": p.W, "K": p.K,
                        "dilations": list(p.dilations), "dtype": dtype,
-                       "step": "ddpm_forward + ddpm_backward (dx, dy, dweight, dbias)",
+                       "step": {"train": "ddpm_forward + ddpm_backward (dx, dy, dweight, dbias)",
+                                "forward": "ddpm_forward (fused generator + filter)",
+                                "filter": "ddpm_filter_pregenerated (taps given)"}[step_kind],
                        "l2": "flushed: 256 MiB write before each step, outside the timed events",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
@@ -386,7 +420,7 @@ def run_ours(args, world, rank, local):
             "e2e": e2e, "wall_s_timed_loop": round(t_wall, 4)}
     line["clocks"] = clk.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(p, dtype)
+        line["cpu_baseline"] = cpu_baseline(p, dtype, step=step_kind)
     return line
 
 
@@ -435,6 +469,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--dtype", choices=("bfloat16", "float32"), default="bfloat16")
+    ap.add_argument("--step", choices=("train", "forward", "filter"), default="train",
+                    help="what one timed step runs (default: the fwd+bwd training step)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (faster runs)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -99,9 +99,164 @@ __global__ void __launch_bounds__(256) filter_pregenerated_kernel(Dims d, const 
     }
 }
 
+// ------------------------------------------------------------------ tiled
+// The vectorised kernel.  A block owns one (b, c) plane tile of kFTH(T) rows x 64
+// columns and first stages x over it with a halo of R rows and 16 columns on each
+// side in shared memory, zeros outside the image, so the inner loop has no bounds
+// checks.  A thread owns VEC consecutive pixels of a row: each tap plane is read
+// with one 16-byte load, and the VEC neighbours of tap (ky, kx) -- a row segment
+// shifted by o = (kx - r) * d columns -- come from the two aligned 16-byte vectors
+// of shared memory that cover it, cut at o mod VEC, which is the same for every
+// thread of the block (a uniform switch, no divergence).
+constexpr int kFTW = 64;          // tile columns
+constexpr int kFHalo = 16;        // staged columns left and right of the tile (R <= 16)
+constexpr int kFRowElems = kFTW + 2 * kFHalo;
+constexpr int kFThreads = 256;
+
+template <typename T> struct FilterTile;
+template <> struct FilterTile<__nv_bfloat16> { static constexpr int VEC = 8, TH = 32; };
+template <> struct FilterTile<float> { static constexpr int VEC = 4, TH = 16; };
+
+// VEC elements starting `sh` elements into the 2*VEC elements (v0, v1), as raw 32-bit words
+template <typename T>
+__device__ __forceinline__ uint4 cut_vec(const uint4& v0, const uint4& v1, int sh) {
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint4 r;
+    if constexpr (sizeof(T) == 4) {
+        switch (sh) {
+            case 0: r = v0; break;
+            case 1: r = make_uint4(w[1], w[2], w[3], w[4]); break;
+            case 2: r = make_uint4(w[2], w[3], w[4], w[5]); break;
+            default: r = make_uint4(w[3], w[4], w[5], w[6]); break;
+        }
+    } else {
+#define DDPM_CUT(S)                                                                                        \
+    case S: {                                                                                              \
+        constexpr int q = (S) >> 1;                                                                        \
+        if constexpr (((S) & 1) == 0) r = make_uint4(w[q], w[q + 1], w[q + 2], w[q + 3]);                 \
+        else r = make_uint4(__byte_perm(w[q], w[q + 1], 0x5432), __byte_perm(w[q + 1], w[q + 2], 0x5432),  \
+                            __byte_perm(w[q + 2], w[q + 3], 0x5432), __byte_perm(w[q + 3], w[q + 4], 0x5432)); \
+        break;                                                                                             \
+    }
+        switch (sh) {
+            DDPM_CUT(0) DDPM_CUT(1) DDPM_CUT(2) DDPM_CUT(3) DDPM_CUT(4) DDPM_CUT(5) DDPM_CUT(6)
+            default: r = make_uint4(__byte_perm(w[3], w[4], 0x5432), __byte_perm(w[4], w[5], 0x5432),
+                                    __byte_perm(w[5], w[6], 0x5432), __byte_perm(w[6], w[7], 0x5432));
+        }
+#undef DDPM_CUT
+    }
+    return r;
+}
+
+// acc[i] += tap[i] * x[i] for the VEC elements packed in two 16-byte words
+__device__ __forceinline__ void fma_vec(float (&acc)[4], const uint4& t, const uint4& x) {
+    acc[0] = fmaf(__uint_as_float(t.x), __uint_as_float(x.x), acc[0]);
+    acc[1] = fmaf(__uint_as_float(t.y), __uint_as_float(x.y), acc[1]);
+    acc[2] = fmaf(__uint_as_float(t.z), __uint_as_float(x.z), acc[2]);
+    acc[3] = fmaf(__uint_as_float(t.w), __uint_as_float(x.w), acc[3]);
+}
+// bf16 operands, exact product, FP32 accumulate (fma.rn.f32.bf16)
+__device__ __forceinline__ void fma_pair_bf16(float& a0, float& a1, uint32_t t, uint32_t x) {
+    asm("{\n\t.reg .b16 tl, th, xl, xh;\n\t"
+        "mov.b32 {tl, th}, %2;\n\t"
+        "mov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, tl, xl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, th, xh, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(t), "r"(x));
+}
+__device__ __forceinline__ void fma_vec(float (&acc)[8], const uint4& t, const uint4& x) {
+    fma_pair_bf16(acc[0], acc[1], t.x, x.x);
+    fma_pair_bf16(acc[2], acc[3], t.y, x.y);
+    fma_pair_bf16(acc[4], acc[5], t.z, x.z);
+    fma_pair_bf16(acc[6], acc[7], t.w, x.w);
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kFThreads) filter_tiled_kernel(Dims d, const T* __restrict__ x,
+                                                                 const T* __restrict__ taps, T* __restrict__ out,
+                                                                 int tiles_w, int tiles_h) {
+    constexpr int VEC = FilterTile<T>::VEC, TH = FilterTile<T>::TH;
+    constexpr int K2 = K * K, r = K / 2;
+    constexpr int TPR = kFTW / VEC;                       // threads per tile row
+    extern __shared__ __align__(16) unsigned char fsm[];
+    T* xs = reinterpret_cast<T*>(fsm);                    // [(TH + 2R) rows][kFRowElems]
+    const int R = d.R();
+    const int tile = blockIdx.x % (tiles_w * tiles_h);
+    const long long bc = blockIdx.x / (tiles_w * tiles_h);
+    const int c = (int)(bc % d.C), b = (int)(bc / d.C);
+    const int h0 = (tile / tiles_w) * TH, w0 = (tile % tiles_w) * kFTW;
+    const T* xp = x + bc * d.HW;
+
+    // stage x rows h0-R .. h0+TH+R-1, columns w0-16 .. w0+64+15, zeros outside the image
+    const int srows = TH + 2 * R;
+    constexpr int VPR = kFRowElems / VEC;                 // vectors per staged row
+    for (int i = threadIdx.x; i < srows * VPR; i += kFThreads) {
+        const int sr = i / VPR, sv = i % VPR;
+        const int hh = h0 - R + sr, ww = w0 - kFHalo + sv * VEC;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (hh >= 0 && hh < d.H && ww >= 0 && ww + VEC <= d.W)
+            v = __ldg(reinterpret_cast<const uint4*>(xp + (long long)hh * d.W + ww));
+        *reinterpret_cast<uint4*>(xs + sr * kFRowElems + sv * VEC) = v;
+    }
+    __syncthreads();
+
+    const int tr = threadIdx.x / TPR, tc = (threadIdx.x % TPR) * VEC;
+    const int h = h0 + tr, w = w0 + tc;
+    if (h >= d.H || w >= d.W) return;                     // W is a multiple of VEC: vectors are whole
+    const long long p0 = (long long)h * d.W + w;
+    const T* xrow0 = xs + (tr + R) * kFRowElems + kFHalo + tc;   // this thread's pixels in the stage
+    T* ob = out + ((long long)b * 4 * d.C) * d.HW + p0;
+    // channel c of the output is x itself (bit-exact copy)
+    *reinterpret_cast<uint4*>(ob + (long long)c * d.HW) = *reinterpret_cast<const uint4*>(xrow0);
+#pragma unroll 1
+    for (int di = 0; di < 3; ++di) {
+        const int dil = dil_of(d, di);
+        const T* tp = taps + ((long long)b * d.O + (long long)(di * d.C + c) * K2) * d.HW + p0;
+        float acc[VEC];
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int ky = 0; ky < K; ++ky) {
+            uint4 tv[K];                                  // one tap row: K 16-byte loads in flight
+#pragma unroll
+            for (int kx = 0; kx < K; ++kx)
+                tv[kx] = __ldg(reinterpret_cast<const uint4*>(tp + (long long)(ky * K + kx) * d.HW));
+            const T* xrow = xrow0 + (ky - r) * dil * kFRowElems;
+#pragma unroll
+            for (int kx = 0; kx < K; ++kx) {
+                const int o = (kx - r) * dil;             // column shift, |o| <= R <= 16
+                const int sh = (o + kFHalo) & (VEC - 1);  // the same for every thread
+                const T* row = xrow + (o - sh);           // o - sh: a multiple of VEC
+                const uint4 v0 = *reinterpret_cast<const uint4*>(row);
+                const uint4 v1 = *reinterpret_cast<const uint4*>(row + VEC);
+                fma_vec(acc, tv[kx], cut_vec<T>(v0, v1, sh));
+            }
+        }
+        T res[VEC];
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) res[i] = from_f<T>(acc[i]);
+        *reinterpret_cast<uint4*>(ob + (long long)((1 + di) * d.C + c) * d.HW) = *reinterpret_cast<const uint4*>(res);
+    }
+}
+
 template <typename T, int K>
 cudaError_t launch_k(const Dims& d, const void* x, const void* taps, void* out, cudaStream_t s, bool vec_ok) {
     constexpr int V = 16 / sizeof(T);
+    if (vec_ok && d.R() <= kFHalo) {
+        constexpr int TH = FilterTile<T>::TH;
+        const int tiles_w = (d.W + kFTW - 1) / kFTW, tiles_h = (d.H + TH - 1) / TH;
+        const long long blocks = (long long)d.B * d.C * tiles_w * tiles_h;
+        // + one vector: the second vector of the last row's rightmost cut is read (and unused)
+        const size_t smem = ((size_t)(TH + 2 * d.R()) * kFRowElems + V) * sizeof(T);
+        if (blocks <= 0x7fffffffLL && smem <= 48 * 1024) {
+            trace_begin(s, kKFilterSimt);
+            filter_tiled_kernel<T, K><<<(unsigned)blocks, kFThreads, smem, s>>>(d, (const T*)x, (const T*)taps,
+                                                                               (T*)out, tiles_w, tiles_h);
+            trace_end(s);
+            return cudaGetLastError();
+        }
+    }
     const int threads = 256;
     const int vec = vec_ok ? V : 1;
     const long long items = (long long)d.B * d.C * (d.HW / vec);

@@ -121,6 +121,43 @@ def test_backward_matches_oracle(p, dtype):
         assert_grad_close(got, want, dtype, name)
 
 
+# Shapes whose rows are whole 16-byte vectors (W % 8 == 0): the filter takes its tiled
+# shared-memory kernel.  Ragged 64-column and row tiles, halo radius 10 (K = 5) and 15
+# (K = 7), a 1-row image, and other dilations.
+FILTER_TILED = TC_SHAPES + [
+    Problem(1, 8, 40, 72, 5),                # K = 5: halo radius 10
+    Problem(1, 4, 19, 24, 7),                # K = 7: halo radius 15
+    Problem(2, 6, 33, 64, 3, (2, 3, 4)),
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", FILTER_TILED, ids=_id)
+def test_filter_tiled_matches_oracle(p, dtype):
+    h = make_inputs(p, 250, dtype, grad=False, taps=True)
+    d = _dev(h)
+    out = binding.filter_pregenerated(d["x"], d["taps"], p.K, p.dilations)
+    torch.cuda.synchronize()
+    ref = oracle.filter_pregenerated(h["x"], h["taps"], p.K, p.dilations)
+    assert_forward_close(out, ref, dtype)
+    assert torch.equal(out[:, :p.C].cpu(), h["x"])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", FILTER_TILED[:4], ids=_id)
+def test_filter_tiled_integer_bit_exact(p, dtype):
+    """Integer-valued x and taps: every product and sum is exact, so the tiled
+    kernel's neighbour addressing must match the oracle bit for bit."""
+    g = torch.Generator().manual_seed(11)
+    x = torch.randint(-2, 3, (p.B, p.C, p.H, p.W), generator=g).to(torch.float32)
+    taps = torch.randint(-2, 3, (p.B, p.O, p.H, p.W), generator=g).to(torch.float32)
+    td = torch.bfloat16 if dtype == "bfloat16" else torch.float32
+    out = binding.filter_pregenerated(x.to(td).cuda(), taps.to(td).cuda(), p.K, p.dilations)
+    torch.cuda.synchronize()
+    ref = oracle.filter_pregenerated(x.double().numpy(), taps.double().numpy(), p.K, p.dilations)
+    np.testing.assert_array_equal(out.double().cpu().numpy(), ref)
+
+
 # ------------------------------------------------- tensor-core forward path --
 
 def _traced_kernels(fn):
