@@ -111,11 +111,12 @@ __global__ void __launch_bounds__(256) filter_pregenerated_kernel(Dims d, const 
 constexpr int kFTW = 64;          // tile columns
 constexpr int kFHalo = 16;        // staged columns left and right of the tile (R <= 16)
 constexpr int kFRowElems = kFTW + 2 * kFHalo;
-constexpr int kFThreads = 256;
+constexpr int kFThreads = 128;   // (64 / VEC) threads per row x TH rows
 
 template <typename T> struct FilterTile;
-template <> struct FilterTile<__nv_bfloat16> { static constexpr int VEC = 8, TH = 32; };
-template <> struct FilterTile<float> { static constexpr int VEC = 4, TH = 16; };
+template <> struct FilterTile<__nv_bfloat16> { static constexpr int VEC = 8, TH = 16; };
+template <> struct FilterTile<float> { static constexpr int VEC = 4, TH = 8; };
+static_assert((kFTW / 8) * 16 == kFThreads && (kFTW / 4) * 8 == kFThreads, "one thread per vector of the tile");
 
 // VEC elements starting `sh` elements into the 2*VEC elements (v0, v1), as raw 32-bit words
 template <typename T>

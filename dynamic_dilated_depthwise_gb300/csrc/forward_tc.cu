@@ -25,6 +25,8 @@
 //               window at immediate offsets.
 // Three TMEM regions (one per dilation, 144 columns each) form the MMA /
 // epilogue pipeline: a region is released as soon as its taps are in registers.
+#include <utility>
+
 #include "bwd_tc_common.cuh"
 #include "tc.cuh"
 
@@ -33,44 +35,63 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kCG = 8;                   // output channels per CTA group
-constexpr int kTaps = 9;                 // K = 3
-constexpr int kN = 80;                   // MMA N per dilation: the group's 72 taps, padded to a multiple of 16
 constexpr int kTile = 128;               // pixels per tile (MMA M)
 constexpr int kKPad = 64;                // generator K (channels of y), zero padded
-constexpr int kEpiWarps = 8;             // 4 TMEM lane quadrants x (kCG / kCPT) channel sets
 constexpr int kEpi0 = 3;                 // first epilogue warp
-constexpr int kCPT = kCG / (kEpiWarps / 4);   // channels per epilogue thread
-constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
-constexpr int kCtasPerSm = 2;            // two co-resident CTAs: one's MMAs overlap the other's epilogue
-constexpr int kTmemCols = 256;           // 3 x kN columns, rounded up to a power of two
-constexpr int kWinMax = 960;             // x window positions: (TH + 2R) x (TW + 16) <= 960
-constexpr int kSlot = kWinMax * 2;       // bytes per channel slot of an x window buffer
-constexpr int kRawBufs = 2;              // x window buffers
-static_assert(kCG * kTaps <= kN && kN % 16 == 0 && 3 * kN <= kTmemCols, "MMA N and TMEM columns");
-static_assert(kCPT % 2 == 0 && kEpiWarps % 4 == 0, "channel pairs per thread");
 
-// shared-memory carve-up (bytes, from a 1024-aligned base).  The 128-byte
-// swizzled operands come first so that every swizzle atom starts on 1024 B.
-constexpr int kSW = 0;                                 // W slice, 3 x [144 x 128 B], SW128 K-major
-constexpr int kSWBytes = 3 * kN * 128;                 // 30720
-constexpr int kSY = kSW + kSWBytes;                    // y tiles, 2 x [64 j x 128 px] SW128 MN-major
-constexpr int kSYBytes = 2 * kTile * kKPad * 2;        // 32768
-constexpr int kSBias = kSY + kSYBytes;                 // bias B operand, 3 x [144 x 16] no swizzle
-constexpr int kSBiasBytes = 3 * kN * 32;               // 7680
-constexpr int kSOnes = kSBias + kSBiasBytes;           // ones A operand [128 x 16] no swizzle
-constexpr int kSOnesBytes = kTile * 32;                // 4096
-constexpr int kSRaw = kSOnes + kSOnesBytes;            // 2 x x window [8 slots of kSlot B][rows][cols] bf16
-constexpr int kRawBuf = kCG * kSlot;                   // 15360
-constexpr int kSStage = kSRaw + kRawBufs * kRawBuf;    // output staging, 4 blocks x [8 ch][TH][TW] bf16
-constexpr int kStageBlk = kCG * kTile * 2;             // 2048
-constexpr int kSmemBytes = kSStage + 4 * kStageBlk + 1024;   // + alignment slack
-static_assert(kSW % 1024 == 0 && kSY % 1024 == 0 && (kSY + kSYBytes / 2) % 1024 == 0, "SW128 atoms need 1 KiB");
-static_assert(kSBias % 16 == 0 && kSOnes % 16 == 0 && kSRaw % 128 == 0 && kSlot % 128 == 0 && kSStage % 128 == 0,
-              "operand alignment");
-static_assert(kCPT == 4, "the epilogue's load / store sequences are written out for four channels");
-// two blocks per SM: 2 x (dynamic + ~0.2 KiB static + 1 KiB reserved) within the SM's 228 KiB
-static_assert(kCtasPerSm * (kSmemBytes + 256 + 1024) <= 228 * 1024, "shared memory of two co-resident blocks");
+// Per-kernel-size configuration.  A CTA owns CG output channels: its MMA N per
+// dilation is the group's CG*K*K taps padded to a multiple of 16, and its x window
+// keeps HALO columns left and right of the tile (the tile start minus HALO stays a
+// 16-byte TMA coordinate; HALO >= the halo radius R).
+template <int K>
+struct FwdCfg;
+template <>
+struct FwdCfg<3> {
+    static constexpr int CG = 8, N = 80, HALO = 8, WINMAX = 960, CTAS = 2, TMEM_COLS = 256;
+};
+template <>
+struct FwdCfg<5> {
+    static constexpr int CG = 4, N = 112, HALO = 16, WINMAX = 2112, CTAS = 1, TMEM_COLS = 512;
+};
+
+template <int K>
+struct FwdLayout {
+    using F = FwdCfg<K>;
+    static constexpr int kCG = F::CG;                  // output channels per CTA group
+    static constexpr int kTaps = K * K;
+    static constexpr int kN = F::N;                    // MMA N per dilation
+    static constexpr int kEpiWarps = 8;                // 4 TMEM lane quadrants x (kCG / kCPT) channel sets
+    static constexpr int kCPT = kCG / (kEpiWarps / 4); // channels per epilogue thread
+    static constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
+    static constexpr int kCtasPerSm = F::CTAS;
+    static constexpr int kTmemCols = F::TMEM_COLS;
+    static constexpr int kHalo = F::HALO;
+    static constexpr int kWinMax = F::WINMAX;          // x window positions: (TH + 2R) x (TW + 2 HALO)
+    static constexpr int kSlot = kWinMax * 2;          // bytes per channel slot of an x window buffer
+    static constexpr int kRawBufs = 2;                 // x window buffers
+    // shared-memory carve-up (bytes, from a 1024-aligned base).  The 128-byte
+    // swizzled operands come first so that every swizzle atom starts on 1024 B.
+    static constexpr int kSW = 0;                      // W slice, 3 x [N x 128 B], SW128 K-major
+    static constexpr int kSWBytes = 3 * kN * 128;
+    static constexpr int kSY = kSW + kSWBytes;         // y tiles, 2 x [64 j x 128 px] SW128 MN-major
+    static constexpr int kSYBytes = 2 * kTile * kKPad * 2;
+    static constexpr int kSBias = kSY + kSYBytes;      // bias B operand, 3 x [N x 16] no swizzle
+    static constexpr int kSBiasBytes = 3 * kN * 32;
+    static constexpr int kSOnes = kSBias + kSBiasBytes;   // ones A operand [128 x 16] no swizzle
+    static constexpr int kSOnesBytes = kTile * 32;
+    static constexpr int kSRaw = kSOnes + kSOnesBytes; // 2 x x window [CG slots of kSlot B][rows][cols] bf16
+    static constexpr int kRawBuf = kCG * kSlot;
+    static constexpr int kSStage = kSRaw + kRawBufs * kRawBuf;   // output staging, 4 blocks x [CG][TH][TW] bf16
+    static constexpr int kStageBlk = kCG * kTile * 2;
+    static constexpr int kSmemBytes = kSStage + 4 * kStageBlk + 1024;   // + alignment slack
+    static_assert(kCG * kTaps <= kN && kN % 16 == 0 && 3 * kN <= kTmemCols, "MMA N and TMEM columns");
+    static_assert(kCPT % 2 == 0 && kCG % kCPT == 0, "channel pairs per thread");
+    static_assert(kSW % 1024 == 0 && kSY % 1024 == 0 && (kSY + kSYBytes / 2) % 1024 == 0, "SW128 atoms need 1 KiB");
+    static_assert(kSBias % 16 == 0 && kSOnes % 16 == 0 && kSRaw % 128 == 0 && kSlot % 128 == 0 && kSStage % 128 == 0,
+                  "operand alignment");
+    // co-resident blocks: each takes dynamic + ~0.2 KiB static + 1 KiB reserved of the SM's 228 KiB
+    static_assert(kCtasPerSm * (kSmemBytes + 256 + 1024) <= 228 * 1024, "shared memory of co-resident blocks");
+};
 
 struct FwdTcParams {
     Dims d;
@@ -78,10 +99,10 @@ struct FwdTcParams {
     int tiles_per_row;     // W >= 64: ceil(W / 64); else 1
     int tiles_per_img;
     int n_tiles;           // B * tiles_per_img
-    int n_groups;          // C / 8
+    int n_groups;          // C / CG
     int ctas_per_group;
     int R;                 // halo radius = max dilation * (K / 2)
-    int WH, WC;            // x window rows (TH + 2R) / columns (TW + 16, origin w0 - 8)
+    int WH, WC;            // x window rows (TH + 2R) / columns (TW + 2 HALO, origin w0 - HALO)
     const bf16* bias;      // may be null
     unsigned int* err;
 };
@@ -116,7 +137,14 @@ __device__ __forceinline__ void fma_pair(float& a0, float& a1, uint32_t t, unsig
         : "r"(t), "h"(x0), "h"(x1));
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
+template <int NTHREADS>
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory"); }
+
+// v[I] = the 16-bit value at addr + I * SLOT, I = 0 .. N-1 (compile-time offsets)
+template <int SLOT, int... I>
+__device__ __forceinline__ void lds_slots(uint32_t addr, unsigned short* v, std::integer_sequence<int, I...>) {
+    ((v[I] = tc::lds_u16<I * SLOT>(addr)), ...);
+}
 
 // n consecutive TMEM columns of this warp's lane quadrant into r[0..n)
 template <int NCOL>
@@ -124,16 +152,27 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
 #pragma unroll
     for (int c = 0; c + 16 <= NCOL; c += 16) DDPM_TMEM_LD_X16(taddr + c, (r + c));
     constexpr int rem = NCOL % 16;
-    if constexpr (rem == 8) DDPM_TMEM_LD_X8(taddr + (NCOL - 8), (r + NCOL - 8));
-    if constexpr (rem == 4) DDPM_TMEM_LD_X4(taddr + (NCOL - 4), (r + NCOL - 4));
-    static_assert(rem == 0 || rem == 4 || rem == 8, "column count");
+    constexpr int b8 = NCOL - rem;
+    if constexpr ((rem & 8) != 0) DDPM_TMEM_LD_X8(taddr + b8, (r + b8));
+    constexpr int b4 = b8 + (rem & 8);
+    if constexpr ((rem & 4) != 0) DDPM_TMEM_LD_X4(taddr + b4, (r + b4));
+    constexpr int b2 = b4 + (rem & 4);
+    if constexpr ((rem & 2) != 0) DDPM_TMEM_LD_X2(taddr + b2, (r + b2));
+    constexpr int b1 = b2 + (rem & 2);
+    if constexpr ((rem & 1) != 0) DDPM_TMEM_LD_X1(taddr + b1, (r + b1));
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+template <int K>
+__global__ void __launch_bounds__(FwdLayout<K>::kThreads, FwdLayout<K>::kCtasPerSm)
     forward_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
                       const FwdTcParams P) {
     using namespace tc;
+    using L = FwdLayout<K>;
+    constexpr int kCG = L::kCG, kTaps = L::kTaps, kN = L::kN, kEpiWarps = L::kEpiWarps, kCPT = L::kCPT;
+    constexpr int kTmemCols = L::kTmemCols, kHalo = L::kHalo, kSlot = L::kSlot, kRawBufs = L::kRawBufs;
+    constexpr int kSW = L::kSW, kSY = L::kSY, kSBias = L::kSBias, kSOnes = L::kSOnes, kSRaw = L::kSRaw;
+    constexpr int kRawBuf = L::kRawBuf, kSStage = L::kSStage, kStageBlk = L::kStageBlk;
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB-aligned base, derived by pointer arithmetic on the shared array so that every
     // access through it stays a shared-memory access (an integer round trip would make
@@ -234,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 mbar_arrive_expect_tx(&bar_raw_full[s], raw_bytes);
                 uint8_t* rb = sm + kSRaw + s * kRawBuf;
                 for (int c = 0; c < nch; ++c)
-                    tma_load_4d(rb + c * kSlot, &tmX, &bar_raw_full[s], tcd.w0 - 8, tcd.h0 - P.R, c0 + c, tcd.b);
+                    tma_load_4d(rb + c * kSlot, &tmX, &bar_raw_full[s], tcd.w0 - kHalo, tcd.h0 - P.R, c0 + c, tcd.b);
                 issued_x = i + 1;
                 if (++s == kRawBufs) {
                     s = 0;
@@ -299,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const bool in_tile = s < tpix;
         const int rr = in_tile ? s / P.TW : 0, cc = in_tile ? s % P.TW : 0;
         const int WC = P.WC;
-        const int center = (rr + P.R) * WC + cc + 8;   // window position of this pixel
+        const int center = (rr + P.R) * WC + cc + kHalo;   // window position of this pixel
         const uint32_t ch_stride = (uint32_t)tpix * 2;   // staging bytes per channel
         // this thread's first staging element of block 0
         const uint32_t st0 = smem_u32(sm + kSStage) + (uint32_t)cl0 * ch_stride + (uint32_t)(in_tile ? s : 0) * 2;
@@ -312,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         auto flush_block = [&](int blk, const TileCoord& tcd) {
             fence_proxy_async_smem();
             if (leader) bulk_wait_read<2>();
-            epi_bar();
+            epi_bar<32 * kEpiWarps>();
             if (leader && ok) {
                 const int cbase = (blk == 0 ? 0 : blk * C) + c0;
                 const uint8_t* src = sm + kSStage + blk * kStageBlk;
@@ -329,12 +368,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw_full[buf], bph, P.err, abort_v));
             // channels c0 .. c0+7 of the output are x itself
             if (ok && in_tile) {
-                const unsigned short v0 = lds_u16<0 * kSlot>(xa), v1 = lds_u16<1 * kSlot>(xa);
-                const unsigned short v2 = lds_u16<2 * kSlot>(xa), v3 = lds_u16<3 * kSlot>(xa);
-                asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0), "h"(v0) : "memory");
-                asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0 + ch_stride), "h"(v1) : "memory");
-                asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0 + 2 * ch_stride), "h"(v2) : "memory");
-                asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0 + 3 * ch_stride), "h"(v3) : "memory");
+                unsigned short v[kCPT];
+                lds_slots<kSlot>(xa, v, std::make_integer_sequence<int, kCPT>{});
+#pragma unroll
+                for (int c = 0; c < kCPT; ++c)
+                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0 + c * ch_stride), "h"(v[c]) : "memory");
             }
             flush_block(0, tcd);
             for (int dd = 0; dd < 3; ++dd) {
@@ -354,11 +392,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 unsigned short xv[kTaps][kCPT];
 #pragma unroll
                 for (int k = 0; k < kTaps; ++k) {
-                    const uint32_t a = xa + (uint32_t)(((k / 3 - 1) * WC + (k % 3 - 1)) * dil * 2);
-                    xv[k][0] = lds_u16<0 * kSlot>(a);
-                    xv[k][1] = lds_u16<1 * kSlot>(a);
-                    xv[k][2] = lds_u16<2 * kSlot>(a);
-                    xv[k][3] = lds_u16<3 * kSlot>(a);
+                    constexpr int r0 = K / 2;
+                    const uint32_t a = xa + (uint32_t)(((k / K - r0) * WC + (k % K - r0)) * dil * 2);
+                    lds_slots<kSlot>(a, xv[k], std::make_integer_sequence<int, kCPT>{});
                 }
                 float acc[kCPT];
 #pragma unroll
@@ -372,13 +408,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                 }
                 if (in_tile) {
-                    const uint32_t o01 = round_pair(__float_as_uint(acc[0]), __float_as_uint(acc[1]));
-                    const uint32_t o23 = round_pair(__float_as_uint(acc[2]), __float_as_uint(acc[3]));
                     const uint32_t sa = st0 + (uint32_t)(1 + dd) * kStageBlk;
-                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa), "h"((unsigned short)(o01 & 0xFFFFu)) : "memory");
-                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa + ch_stride), "h"((unsigned short)(o01 >> 16)) : "memory");
-                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa + 2 * ch_stride), "h"((unsigned short)(o23 & 0xFFFFu)) : "memory");
-                    asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa + 3 * ch_stride), "h"((unsigned short)(o23 >> 16)) : "memory");
+#pragma unroll
+                    for (int c = 0; c < kCPT; c += 2) {
+                        const uint32_t o = round_pair(__float_as_uint(acc[c]), __float_as_uint(acc[c + 1]));
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa + c * ch_stride), "h"((unsigned short)(o & 0xFFFFu))
+                                     : "memory");
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa + (c + 1) * ch_stride), "h"((unsigned short)(o >> 16))
+                                     : "memory");
+                    }
                 }
                 if (dd == 2) {
                     // the window has been read for the last time
@@ -407,7 +445,7 @@ struct Tiling {
     int TH, TW, tiles_per_row, tiles_per_img, R, WH, WC;
 };
 
-Tiling tiling_of(const Dims& d) {
+Tiling tiling_of(const Dims& d, int halo) {
     Tiling t;
     if (d.W >= 64) {
         t.TW = 64;
@@ -421,39 +459,38 @@ Tiling tiling_of(const Dims& d) {
     t.tiles_per_img = ((d.H + t.TH - 1) / t.TH) * t.tiles_per_row;
     t.R = d.R();
     t.WH = t.TH + 2 * t.R;
-    t.WC = t.TW + 16;
+    t.WC = t.TW + 2 * halo;
     return t;
 }
 
-}  // namespace
-
-bool forward_tc_eligible(const Dims& d, const void* y, const void* w) {
-    if (d.dtype != 1 || d.K != 3 || (d.flags & kFlagCudaCores)) return false;
-    if (d.C % 8 != 0 || d.C > kKPad) return false;      // TMA row stride of W; one 64-wide K block
-    if (d.W % 8 != 0) return false;                     // every tile start is a 16-byte TMA coordinate
-    if ((uintptr_t)y % 16 != 0 || (uintptr_t)w % 16 != 0) return false;
-    if (d.R() > 8) return false;                        // the x window spans w0 - 8 .. w0 + TW + 8
-    const Tiling t = tiling_of(d);
-    if ((long long)t.WH * t.WC > kWinMax || t.WH > 256) return false;
+template <int K>
+bool eligible_k(const Dims& d) {
+    using L = FwdLayout<K>;
+    if (d.C % 8 != 0 || d.C % L::kCG != 0 || d.C > kKPad) return false;   // TMA row stride of W; one 64-wide K block
+    if (d.R() > L::kHalo) return false;                 // the x window spans w0 - HALO .. w0 + TW + HALO
+    const Tiling t = tiling_of(d, L::kHalo);
+    if ((long long)t.WH * t.WC > L::kWinMax || t.WH > 256) return false;
     const long long tiles = (long long)d.B * t.tiles_per_img;
-    if (tiles > (1LL << 30) || d.O > (1LL << 30) || d.HW > (1LL << 31) - 1024) return false;
-    return bwdtc::encode_fn() != nullptr;
+    return tiles <= (1LL << 30) && d.O <= (1LL << 30) && d.HW <= (1LL << 31) - 1024;
 }
 
-cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const void* w, const void* bias,
-                              void* out, cudaStream_t s) {
+template <int K>
+cudaError_t launch_k(const Dims& d, const void* x, const void* y, const void* w, const void* bias, void* out,
+                     cudaStream_t s) {
+    using L = FwdLayout<K>;
     static int attr_done = 0;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(forward_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e =
+            cudaFuncSetAttribute(forward_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(forward_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+            e = cudaFuncSetAttribute(forward_tc_kernel<K>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         attr_done = 1;
     }
     auto enc = bwdtc::encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     if ((uintptr_t)x % 16 != 0) return cudaErrorInvalidValue;
-    const Tiling t = tiling_of(d);
+    const Tiling t = tiling_of(d, L::kHalo);
     CUtensorMap tmY, tmW, tmX, tmO;
     const cuuint64_t dimY[3] = {(cuuint64_t)d.HW, (cuuint64_t)d.C, (cuuint64_t)d.B};
     const cuuint64_t strY[2] = {(cuuint64_t)d.HW * 2, (cuuint64_t)d.HW * d.C * 2};
@@ -465,7 +502,7 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
         return cudaErrorInvalidValue;
     const cuuint64_t dimW[2] = {(cuuint64_t)d.C, (cuuint64_t)d.O};
     const cuuint64_t strW[1] = {(cuuint64_t)d.C * 2};
-    const cuuint32_t boxW[2] = {(cuuint32_t)kKPad, (cuuint32_t)kN};
+    const cuuint32_t boxW[2] = {(cuuint32_t)kKPad, (cuuint32_t)L::kN};
     const cuuint32_t one2[2] = {1, 1};
     if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w), dimW, strW, boxW, one2,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -473,9 +510,9 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
         return cudaErrorInvalidValue;
     if (!bwdtc::encode_nchw(&tmX, x, d, d.C, (uint32_t)t.WC, (uint32_t)t.WH, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    // output [B, 4C, H, W]: boxes of 8 channels x one tile, written from the staging blocks
-    if ((uintptr_t)out % 16 != 0 ||
-        !bwdtc::encode_nchw(&tmO, out, d, 4 * d.C, (uint32_t)t.TW, (uint32_t)t.TH, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+    // output [B, 4C, H, W]: boxes of CG channels x one tile, written from the staging blocks
+    if ((uintptr_t)out % 16 != 0 || !bwdtc::encode_nchw(&tmO, out, d, 4 * d.C, (uint32_t)t.TW, (uint32_t)t.TH,
+                                                        (uint32_t)L::kCG, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
     FwdTcParams P;
@@ -485,9 +522,9 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
     P.tiles_per_row = t.tiles_per_row;
     P.tiles_per_img = t.tiles_per_img;
     P.n_tiles = d.B * t.tiles_per_img;
-    P.n_groups = (d.C + kCG - 1) / kCG;
-    const int sms = num_sms() * kCtasPerSm;
-    int cpg = sms / P.n_groups;
+    P.n_groups = d.C / L::kCG;
+    const int ctas = num_sms() * L::kCtasPerSm;
+    int cpg = ctas / P.n_groups;
     if (cpg < 1) cpg = 1;
     if (cpg > P.n_tiles) cpg = P.n_tiles;
     P.ctas_per_group = cpg;
@@ -498,9 +535,26 @@ cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const
     P.err = device_error_word();
     if (P.err == nullptr) return cudaErrorUnknown;
     trace_begin(s, kKForwardTc);
-    forward_tc_kernel<<<P.n_groups * cpg, kThreads, kSmemBytes, s>>>(tmY, tmW, tmX, tmO, P);
+    forward_tc_kernel<K><<<P.n_groups * cpg, L::kThreads, L::kSmemBytes, s>>>(tmY, tmW, tmX, tmO, P);
     trace_end(s);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+bool forward_tc_eligible(const Dims& d, const void* y, const void* w) {
+    if (d.dtype != 1 || (d.flags & kFlagCudaCores)) return false;
+    if (d.W % 8 != 0) return false;                     // every tile start is a 16-byte TMA coordinate
+    if ((uintptr_t)y % 16 != 0 || (uintptr_t)w % 16 != 0) return false;
+    const bool shape = d.K == 3 ? eligible_k<3>(d) : d.K == 5 ? eligible_k<5>(d) : false;
+    return shape && bwdtc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const void* w, const void* bias,
+                              void* out, cudaStream_t s) {
+    if (d.K == 3) return launch_k<3>(d, x, y, w, bias, out, s);
+    if (d.K == 5) return launch_k<5>(d, x, y, w, bias, out, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace ddpm

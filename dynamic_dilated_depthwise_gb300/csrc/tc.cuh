@@ -244,6 +244,9 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])                                         \
                  : "r"(taddr))
 
+#define DDPM_TMEM_LD_X2(taddr, r)                                                               \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr))
+
 #define DDPM_TMEM_LD_X1(taddr, r) \
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr))
 

@@ -187,7 +187,22 @@ def test_tc_forward_matches_oracle_and_cuda_cores(p):
     assert torch.equal(out[:, :p.C].cpu(), h["x"])
 
 
-@pytest.mark.parametrize("p", TC_SHAPES[:5], ids=_id)
+# K = 5 shapes the tensor-core forward takes (4-channel groups, halo radius up to 10)
+TC_SHAPES_K5 = [
+    Problem(1, 8, 12, 64, 5),                # one row of 64-column tiles, halo radius 10
+    Problem(2, 16, 9, 136, 5),               # ragged row tile, odd row count
+    Problem(1, 64, 20, 128, 5),              # C = 64 as in the K = 5 workload
+    Problem(1, 24, 5, 24, 5, (1, 2, 3)),     # whole-row tiles, other dilations
+    Problem(1, 8, 7, 40, 5, (2, 4, 5)),      # whole-row tiles of 3 rows, halo radius 10
+]
+
+
+@pytest.mark.parametrize("p", TC_SHAPES_K5, ids=_id)
+def test_tc_forward_k5_matches_oracle_and_cuda_cores(p):
+    test_tc_forward_matches_oracle_and_cuda_cores(p)
+
+
+@pytest.mark.parametrize("p", TC_SHAPES[:5] + TC_SHAPES_K5[:3], ids=_id)
 def test_tc_forward_integer_bit_exact(p):
     h = make_integer_inputs(p, 9, "bfloat16", grad=False)
     out = run_forward(_dev(h), p)
