@@ -166,32 +166,40 @@ __global__ void __launch_bounds__(kThreads) dy_kernel(Dims d, const T* __restric
 // Partial sums over split s of the flattened pixels (b, p):
 //   ws[s][o][j] = sum_{(b,p) in s} dK[b,o,p] * y[b,j,p]   (j < C)
 //   ws[s][o][C] = sum_{(b,p) in s} dK[b,o,p]               (the dbias column)
-// Block (c, di*JT + jt, s): the K*K taps of (di, c) x 64 columns of j (tile jt)
-// plus a column of ones that yields dbias.  Each pixel tile of kPT pixels is
-// staged as dK_s[k][pp] and y_s[jj][pp]; threads own 4x4 output micro-tiles and
-// a strided subset of the tile's pixel quads (register tiling, 16-byte shared
-// loads), and the lanes sharing a micro-tile are summed in a fixed order.
+// A block is a small GEMM: M = the taps of CGW channels of one dilation (CGW*K*K,
+// about 72 rows), N = 64 columns of j plus a column of ones that yields dbias, and
+// the split's pixels as the reduction, walked in tiles of kPT pixels.  Per tile the
+// block stages dK_s[m][pp] (formed from grad and shifted x) and y_s[n][pp] once --
+// so y is read once per CGW channels, not once per channel -- and each thread owns
+// one 4x4 output micro-tile that it accumulates over the tile's pixels in order
+// (16-byte shared loads, no cross-thread reduction).
 constexpr int kPT = 64;
 constexpr int kNJ = 68;  // 64 j columns + ones column + 3 zero columns
-constexpr int kDwThreads = 256;
+constexpr int kRS = kPT + 4;   // shared row stride (floats): consecutive rows start one 16-byte bank group apart
+
+template <int K>
+struct DwTile {
+    static constexpr int K2 = K * K;
+    static constexpr int CGW = (72 / K2) > 1 ? 72 / K2 : 1;        // channels per block
+    static constexpr int MT = (CGW * K2 + 3) / 4 * 4;              // tap rows, padded to the micro-tile
+    static constexpr int NM = (MT / 4) * (kNJ / 4);                // 4x4 micro-tiles
+    static constexpr int THREADS = (NM + 31) / 32 * 32;
+};
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kDwThreads) dw_partial_kernel(Dims d, const T* __restrict__ g,
-                                                                const T* __restrict__ x,
-                                                                const T* __restrict__ y,
-                                                                float* __restrict__ ws, long long chunk) {
-    constexpr int K2 = K * K;
-    constexpr int KP = (K2 + 3) / 4 * 4;
-    constexpr int NM = (KP / 4) * (kNJ / 4);
-    constexpr int L = (kDwThreads / NM) > 0 ? (kDwThreads / NM) : 1;
-    static_assert(NM * L <= kDwThreads, "micro-tiles must fit the block");
-    __shared__ __align__(16) float dK_s[KP * kPT];
-    __shared__ __align__(16) float y_s[kNJ * kPT];
-    __shared__ float red[NM * 16 * L];
+__global__ void __launch_bounds__(DwTile<K>::THREADS, 2) dw_partial_kernel(Dims d, const T* __restrict__ g,
+                                                                       const T* __restrict__ x,
+                                                                       const T* __restrict__ y,
+                                                                       float* __restrict__ ws, long long chunk) {
+    using Tl = DwTile<K>;
+    constexpr int K2 = K * K, CGW = Tl::CGW, MT = Tl::MT, NM = Tl::NM, NT = Tl::THREADS;
+    __shared__ __align__(16) float dK_s[MT * kRS];
+    __shared__ __align__(16) float y_s[kNJ * kRS];
+    __shared__ int pix_b[kPT], pix_h[kPT], pix_w[kPT];
 
     const int r = K / 2;
     const int C = d.C;
-    const int c = blockIdx.x;
+    const int c0 = blockIdx.x * CGW;
     const int JT = (C + 63) / 64;
     const int di = blockIdx.y / JT;
     const int jt = blockIdx.y % JT;
@@ -202,9 +210,8 @@ __global__ void __launch_bounds__(kDwThreads) dw_partial_kernel(Dims d, const T*
     const long long P0 = (long long)s * chunk;
     const long long P1 = P0 + chunk < NP ? P0 + chunk : NP;
     const int tid = threadIdx.x;
-    const int m = tid / L, lane = tid % L;
-    const bool computes = tid < NM * L;
-    const int mr = m / (kNJ / 4), mc = m % (kNJ / 4);
+    const bool computes = tid < NM;
+    const int mr = tid / (kNJ / 4), mc = tid % (kNJ / 4);
 
     float acc[4][4];
 #pragma unroll
@@ -214,45 +221,77 @@ __global__ void __launch_bounds__(kDwThreads) dw_partial_kernel(Dims d, const T*
 
     for (long long base = P0; base < P1; base += kPT) {
         __syncthreads();
-        for (int i = tid; i < KP * kPT; i += kDwThreads) {
-            const int k = i / kPT, pp = i % kPT;
+        // pixel coordinates of the tile (b = -1 past the split)
+        for (int pp = tid; pp < kPT; pp += NT) {
             const long long P = base + pp;
-            float v = 0.0f;
-            if (k < K2 && P < P1) {
+            if (P < P1) {
                 const int b = (int)(P / d.HW);
-                const long long p = P % d.HW;
-                const int h = (int)(p / d.W), w = (int)(p % d.W);
-                const int ky = k / K, kx = k % K;
+                const long long p = P - (long long)b * d.HW;
+                pix_b[pp] = b;
+                pix_h[pp] = (int)(p / d.W);
+                pix_w[pp] = (int)(p - (long long)pix_h[pp] * d.W);
+            } else {
+                pix_b[pp] = -1;
+                pix_h[pp] = 0;
+                pix_w[pp] = 0;
+            }
+        }
+        __syncthreads();
+        // every thread's loads of the tile are issued before any is used (the loops are
+        // unrolled into registers), so their latencies overlap instead of adding up
+        constexpr int ITK = (MT * kPT + NT - 1) / NT, ITY = (kNJ * kPT + NT - 1) / NT;
+        float vk[ITK], vy[ITY];
+#pragma unroll
+        for (int it = 0; it < ITK; ++it) {
+            const int i = tid + it * NT;
+            const int m = i / kPT, pp = i - m * kPT;
+            const int cl = m / K2, k = m - cl * K2;
+            const int c = c0 + cl;
+            const int b = i < MT * kPT ? pix_b[pp] : -1;
+            float v = 0.0f;
+            if (m < CGW * K2 && c < C && b >= 0) {
+                const int h = pix_h[pp], w = pix_w[pp];
+                const int ky = k / K, kx = k - ky * K;
+                const long long p = (long long)h * d.W + w;
                 const float gv = to_f(g[((long long)b * 4 * C + (1 + di) * C + c) * d.HW + p]);
                 v = gv * x_at(x + ((long long)b * C + c) * d.HW, d.H, d.W, h + (ky - r) * dil, w + (kx - r) * dil);
             }
-            dK_s[i] = v;
+            vk[it] = v;
         }
-        for (int i = tid; i < kNJ * kPT; i += kDwThreads) {
-            const int jj = i / kPT, pp = i % kPT;
-            const long long P = base + pp;
+#pragma unroll
+        for (int it = 0; it < ITY; ++it) {
+            const int i = tid + it * NT;
+            const int jj = i / kPT, pp = i - jj * kPT;
+            const int b = i < kNJ * kPT ? pix_b[pp] : -1;
             float v = 0.0f;
-            if (P < P1) {
+            if (b >= 0) {
                 if (jj < 64) {
-                    if (j0 + jj < C) {
-                        const int b = (int)(P / d.HW);
-                        const long long p = P % d.HW;
-                        v = to_f(y[((long long)b * C + j0 + jj) * d.HW + p]);
-                    }
+                    if (j0 + jj < C) v = to_f(y[((long long)b * C + j0 + jj) * d.HW + (long long)pix_h[pp] * d.W + pix_w[pp]]);
                 } else if (jj == 64 && jt == 0) {
                     v = 1.0f;
                 }
             }
-            y_s[i] = v;
+            vy[it] = v;
+        }
+#pragma unroll
+        for (int it = 0; it < ITK; ++it) {
+            const int i = tid + it * NT;
+            if (i < MT * kPT) dK_s[(i / kPT) * kRS + i % kPT] = vk[it];
+        }
+#pragma unroll
+        for (int it = 0; it < ITY; ++it) {
+            const int i = tid + it * NT;
+            if (i < kNJ * kPT) y_s[(i / kPT) * kRS + i % kPT] = vy[it];
         }
         __syncthreads();
         if (computes) {
-            for (int qd = lane; qd < kPT / 4; qd += L) {
+#pragma unroll 4
+            for (int qd = 0; qd < kPT / 4; ++qd) {
                 float4 a[4], bq[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) a[i] = reinterpret_cast<const float4*>(dK_s + (4 * mr + i) * kPT)[qd];
+                for (int i = 0; i < 4; ++i) a[i] = reinterpret_cast<const float4*>(dK_s + (4 * mr + i) * kRS)[qd];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) bq[j] = reinterpret_cast<const float4*>(y_s + (4 * mc + j) * kPT)[qd];
+                for (int j = 0; j < 4; ++j) bq[j] = reinterpret_cast<const float4*>(y_s + (4 * mc + j) * kRS)[qd];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -265,27 +304,22 @@ __global__ void __launch_bounds__(kDwThreads) dw_partial_kernel(Dims d, const T*
             }
         }
     }
-    __syncthreads();
-    if (computes) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) red[(m * 16 + i * 4 + j) * L + lane] = acc[i][j];
-    }
-    __syncthreads();
+    if (!computes) return;
     float* wsb = ws + (long long)s * d.O * (C + 1);
-    for (int e = tid; e < NM * 16; e += kDwThreads) {
-        const int mm = e / 16, i = (e / 4) % 4, j = e % 4;
-        float v = 0.0f;
-        for (int l = 0; l < L; ++l) v += red[e * L + l];
-        const int k = 4 * (mm / (kNJ / 4)) + i;
-        const int jj = 4 * (mm % (kNJ / 4)) + j;
-        if (k >= K2) continue;
-        const long long o = (long long)(di * C + c) * K2 + k;
-        if (jj < 64) {
-            if (j0 + jj < C) wsb[o * (C + 1) + j0 + jj] = v;
-        } else if (jj == 64 && jt == 0) {
-            wsb[o * (C + 1) + C] = v;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int m = 4 * mr + i;
+        const int cl = m / K2, k = m - cl * K2;
+        if (m >= CGW * K2 || c0 + cl >= C) continue;
+        const long long o = (long long)(di * C + c0 + cl) * K2 + k;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int jj = 4 * mc + j;
+            if (jj < 64) {
+                if (j0 + jj < C) wsb[o * (C + 1) + j0 + jj] = acc[i][j];
+            } else if (jj == 64 && jt == 0) {
+                wsb[o * (C + 1) + C] = acc[i][j];
+            }
         }
     }
 }
@@ -348,10 +382,10 @@ template <typename T, int K>
 cudaError_t launch_dw_k(const Dims& d, const void* g, const void* x, const void* y, void* ws, cudaStream_t s) {
     const int S = backward_num_splits(d);
     const int JT = (d.C + 63) / 64;
-    dim3 grid((unsigned)d.C, (unsigned)(3 * JT), (unsigned)S);
+    dim3 grid((unsigned)((d.C + DwTile<K>::CGW - 1) / DwTile<K>::CGW), (unsigned)(3 * JT), (unsigned)S);
     trace_begin(s, kKBwdDwPartialSimt);
-    dw_partial_kernel<T, K><<<grid, kDwThreads, 0, s>>>(d, (const T*)g, (const T*)x, (const T*)y, (float*)ws,
-                                                        split_chunk(d, S));
+    dw_partial_kernel<T, K><<<grid, DwTile<K>::THREADS, 0, s>>>(d, (const T*)g, (const T*)x, (const T*)y,
+                                                                (float*)ws, split_chunk(d, S));
     trace_end(s);
     return cudaGetLastError();
 }
