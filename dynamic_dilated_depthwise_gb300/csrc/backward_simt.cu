@@ -51,16 +51,41 @@ __global__ void __launch_bounds__(kThreads) dx_kernel(Dims d, const T* __restric
     for (int cc = 0; cc < kCG; ++cc)
         acc[cc] = (active && c0 + cc < C) ? to_f(gb[(long long)(c0 + cc) * d.HW + q]) : 0.0f;
 
+    // the generator rows of the next tap are loaded into registers while this tap is
+    // applied (C <= 128: at most 8 values a thread), so the staging latency overlaps
+    constexpr int ITX = 8;
+    const bool ahead = C * kCG <= ITX * kThreads;
+    float wn[ITX];
+    auto load_tap = [&](int di, int k) {
+#pragma unroll
+        for (int it = 0; it < ITX; ++it) {
+            const int i = threadIdx.x + it * kThreads;
+            const int j = i / kCG, cc = i % kCG;
+            const int c = c0 + cc;
+            wn[it] = (i < C * kCG && c < C) ? to_f(wgt[((long long)(di * C + c) * K2 + k) * C + j]) : 0.0f;
+        }
+    };
+    if (ahead) load_tap(0, 0);
 #pragma unroll 1
     for (int di = 0; di < 3; ++di) {
         const int dil = dil_of(d, di);
 #pragma unroll 1
         for (int k = 0; k < K2; ++k) {
             __syncthreads();
-            for (int i = threadIdx.x; i < C * kCG; i += kThreads) {
-                const int j = i / kCG, cc = i % kCG;
-                const int c = c0 + cc;
-                Ws[i] = c < C ? to_f(wgt[((long long)(di * C + c) * K2 + k) * C + j]) : 0.0f;
+            if (ahead) {
+#pragma unroll
+                for (int it = 0; it < ITX; ++it) {
+                    const int i = threadIdx.x + it * kThreads;
+                    if (i < C * kCG) Ws[i] = wn[it];
+                }
+                const int nk = k + 1 < K2 ? k + 1 : 0, ndi = k + 1 < K2 ? di : di + 1;
+                if (ndi < 3) load_tap(ndi, nk);
+            } else {
+                for (int i = threadIdx.x; i < C * kCG; i += kThreads) {
+                    const int j = i / kCG, cc = i % kCG;
+                    const int c = c0 + cc;
+                    Ws[i] = c < C ? to_f(wgt[((long long)(di * C + c) * K2 + k) * C + j]) : 0.0f;
+                }
             }
             if (threadIdx.x < kCG) {
                 const int c = c0 + threadIdx.x;
@@ -124,15 +149,43 @@ __global__ void __launch_bounds__(kThreads) dy_kernel(Dims d, const T* __restric
 #pragma unroll
     for (int jj = 0; jj < kJC; ++jj) acc[jj] = 0.0f;
 
+    // the generator rows of channel c are staged through registers one channel ahead:
+    // channel c+1's loads are in flight while channel c is applied (for K <= 5; K = 7
+    // would need 74 registers a thread and stages directly)
+    constexpr int ITW0 = (3 * K2 * kJC + kThreads - 1) / kThreads;
+    constexpr bool kAhead = ITW0 <= 40;
+    constexpr int ITW = kAhead ? ITW0 : 1;
+    float wn[ITW];
+    auto load_rows = [&](int c) {
+#pragma unroll
+        for (int it = 0; it < ITW; ++it) {
+            const int i = threadIdx.x + it * kThreads;
+            const int row = i / kJC, jj = i % kJC;  // row = di*K2 + k
+            const int di = row / K2, k = row % K2;
+            wn[it] = (i < 3 * K2 * kJC && j0 + jj < C) ? to_f(wgt[((long long)(di * C + c) * K2 + k) * C + j0 + jj])
+                                                        : 0.0f;
+        }
+    };
+    if constexpr (kAhead) load_rows(0);
 #pragma unroll 1
     for (int c = 0; c < C; ++c) {
         __syncthreads();
-        for (int i = threadIdx.x; i < 3 * K2 * kJC; i += kThreads) {
-            const int row = i / kJC, jj = i % kJC;  // row = di*K2 + k
-            const int di = row / K2, k = row % K2;
-            Ws[i] = (j0 + jj < C) ? to_f(wgt[((long long)(di * C + c) * K2 + k) * C + j0 + jj]) : 0.0f;
+        if constexpr (kAhead) {
+#pragma unroll
+            for (int it = 0; it < ITW; ++it) {
+                const int i = threadIdx.x + it * kThreads;
+                if (i < 3 * K2 * kJC) Ws[i] = wn[it];
+            }
+        } else {
+            for (int i = threadIdx.x; i < 3 * K2 * kJC; i += kThreads) {
+                const int row = i / kJC, jj = i % kJC;  // row = di*K2 + k
+                const int di = row / K2, k = row % K2;
+                Ws[i] = (j0 + jj < C) ? to_f(wgt[((long long)(di * C + c) * K2 + k) * C + j0 + jj]) : 0.0f;
+            }
         }
         __syncthreads();
+        if constexpr (kAhead)
+            if (c + 1 < C) load_rows(c + 1);
         if (!active) continue;
         const T* xp = x + ((long long)b * C + c) * d.HW;
 #pragma unroll 1
