@@ -40,6 +40,27 @@ __global__ void __launch_bounds__(kThreads) forward_simt_kernel(Dims d, const T*
     const int w = active ? (int)(p % d.W) : 0;
     const T* yb = y + (long long)b * C * d.HW;
 
+    // y of this pixel stays in registers across the block's channels and dilations when
+    // C <= 64 (one load per input channel instead of one per (channel, dilation, input))
+    constexpr int kYR = 64;
+    const bool y_in_regs = C <= kYR;
+    float yr[kYR];
+#pragma unroll
+    for (int j = 0; j < kYR; ++j) yr[j] = (y_in_regs && active && j < C) ? ldg_f(yb + (long long)j * d.HW + p) : 0.0f;
+    // the generator rows of the next (channel, dilation) are loaded into registers while
+    // the current ones are applied, so the staging latency overlaps
+    constexpr int ITW = (kYR * KP + kThreads - 1) / kThreads;
+    float wn[ITW];
+    auto load_rows = [&](long long o0) {
+#pragma unroll
+        for (int it = 0; it < ITW; ++it) {
+            const int i = threadIdx.x + it * kThreads;
+            const int j = i / KP, k = i % KP;
+            wn[it] = (i < C * KP && k < K2) ? to_f(wgt[(o0 + k) * C + j]) : 0.0f;
+        }
+    };
+    if (y_in_regs) load_rows((long long)c0 * K2);
+
     for (int cc = 0; cc < kCG; ++cc) {
         const int c = c0 + cc;
         if (c >= C) break;  // uniform across the block
@@ -49,25 +70,55 @@ __global__ void __launch_bounds__(kThreads) forward_simt_kernel(Dims d, const T*
         for (int di = 0; di < 3; ++di) {
             __syncthreads();
             const long long o0 = (long long)(di * C + c) * K2;
-            for (int i = threadIdx.x; i < C * KP; i += kThreads) {
-                const int j = i / KP, k = i % KP;
-                Ws[i] = k < K2 ? to_f(wgt[(o0 + k) * C + j]) : 0.0f;
+            if (y_in_regs) {
+#pragma unroll
+                for (int it = 0; it < ITW; ++it) {
+                    const int i = threadIdx.x + it * kThreads;
+                    if (i < C * KP) Ws[i] = wn[it];
+                }
+            } else {
+                for (int i = threadIdx.x; i < C * KP; i += kThreads) {
+                    const int j = i / KP, k = i % KP;
+                    Ws[i] = k < K2 ? to_f(wgt[(o0 + k) * C + j]) : 0.0f;
+                }
             }
             __syncthreads();
+            if (y_in_regs) {
+                // next (channel, dilation) of the block, if any
+                const int ndi = di < 2 ? di + 1 : 0, nc = di < 2 ? c : c + 1;
+                if (nc < C && nc < c0 + kCG) load_rows((long long)(ndi * C + nc) * K2);
+            }
             if (!active) continue;
             float t[KP];
 #pragma unroll
             for (int k = 0; k < KP; ++k) t[k] = (bias != nullptr && k < K2) ? to_f(bias[o0 + k]) : 0.0f;
-            for (int j = 0; j < C; ++j) {
-                const float yv = ldg_f(yb + (long long)j * d.HW + p);
-                const float4* wr = reinterpret_cast<const float4*>(Ws + j * KP);
+            if (y_in_regs) {
 #pragma unroll
-                for (int q = 0; q < KP / 4; ++q) {
-                    const float4 w4 = wr[q];
-                    t[4 * q + 0] = __fmaf_rn(w4.x, yv, t[4 * q + 0]);
-                    t[4 * q + 1] = __fmaf_rn(w4.y, yv, t[4 * q + 1]);
-                    t[4 * q + 2] = __fmaf_rn(w4.z, yv, t[4 * q + 2]);
-                    t[4 * q + 3] = __fmaf_rn(w4.w, yv, t[4 * q + 3]);
+                for (int j = 0; j < kYR; ++j) {
+                    if (j >= C) break;
+                    const float yv = yr[j];
+                    const float4* wr = reinterpret_cast<const float4*>(Ws + j * KP);
+#pragma unroll
+                    for (int q = 0; q < KP / 4; ++q) {
+                        const float4 w4 = wr[q];
+                        t[4 * q + 0] = __fmaf_rn(w4.x, yv, t[4 * q + 0]);
+                        t[4 * q + 1] = __fmaf_rn(w4.y, yv, t[4 * q + 1]);
+                        t[4 * q + 2] = __fmaf_rn(w4.z, yv, t[4 * q + 2]);
+                        t[4 * q + 3] = __fmaf_rn(w4.w, yv, t[4 * q + 3]);
+                    }
+                }
+            } else {
+                for (int j = 0; j < C; ++j) {
+                    const float yv = ldg_f(yb + (long long)j * d.HW + p);
+                    const float4* wr = reinterpret_cast<const float4*>(Ws + j * KP);
+#pragma unroll
+                    for (int q = 0; q < KP / 4; ++q) {
+                        const float4 w4 = wr[q];
+                        t[4 * q + 0] = __fmaf_rn(w4.x, yv, t[4 * q + 0]);
+                        t[4 * q + 1] = __fmaf_rn(w4.y, yv, t[4 * q + 1]);
+                        t[4 * q + 2] = __fmaf_rn(w4.z, yv, t[4 * q + 2]);
+                        t[4 * q + 3] = __fmaf_rn(w4.w, yv, t[4 * q + 3]);
+                    }
                 }
             }
             const int dil = dil_of(d, di);
