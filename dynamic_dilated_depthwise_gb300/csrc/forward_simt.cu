@@ -41,15 +41,16 @@ __global__ void __launch_bounds__(kThreads) forward_simt_kernel(Dims d, const T*
     const T* yb = y + (long long)b * C * d.HW;
 
     // y of this pixel stays in registers across the block's channels and dilations when
-    // C <= 64 (one load per input channel instead of one per (channel, dilation, input))
-    constexpr int kYR = 64;
-    const bool y_in_regs = C <= kYR;
+    // C <= 64 and K <= 3 (one load per input channel instead of one per (channel,
+    // dilation, input)); larger kernels need the registers for their taps
+    constexpr int kYR = K <= 3 ? 64 : 1;
+    const bool y_in_regs = K <= 3 && C <= kYR;
     float yr[kYR];
 #pragma unroll
     for (int j = 0; j < kYR; ++j) yr[j] = (y_in_regs && active && j < C) ? ldg_f(yb + (long long)j * d.HW + p) : 0.0f;
     // the generator rows of the next (channel, dilation) are loaded into registers while
     // the current ones are applied, so the staging latency overlaps
-    constexpr int ITW = (kYR * KP + kThreads - 1) / kThreads;
+    constexpr int ITW = K <= 3 ? (kYR * KP + kThreads - 1) / kThreads : 1;
     float wn[ITW];
     auto load_rows = [&](long long o0) {
 #pragma unroll
