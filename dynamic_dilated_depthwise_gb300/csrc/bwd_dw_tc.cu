@@ -256,11 +256,10 @@ int bwd_dw_tc_splits(const Dims& d, size_t workspace_bytes) {
 
 cudaError_t launch_bwd_dw_tc(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S,
                              cudaStream_t s) {
-    static int attr_done = 0;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_dw_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    static int attr_done[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dw_tc_kernel, kSmemBytes, attr_done);
         if (e != cudaSuccess) return e;
-        attr_done = 1;
     }
     DwTcParams P;
     P.d = d;

@@ -453,12 +453,10 @@ cudaError_t launch_bwd_dx_packed(const Dims& d, const void* g, const void* y, co
                                  void* dx, void* packed, cudaStream_t s) {
     const DxPackedLayout L = dx_packed_layout(d);
     if (L.stages == 0) return cudaErrorInvalidValue;
-    static int attr_bytes = 0;
-    if (attr_bytes < L.bytes) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_dx_tc_packed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             L.bytes);
+    static int attr_bytes[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dx_tc_packed_kernel, L.bytes, attr_bytes);
         if (e != cudaSuccess) return e;
-        attr_bytes = L.bytes;
     }
     bf16* yc = static_cast<bf16*>(packed);
     bf16* gc = yc + (size_t)d.B * d.C * d.HW;

@@ -381,11 +381,10 @@ bool bwd_dx_tc_eligible(const Dims& d, const void* g, const void* y, const void*
 
 cudaError_t launch_bwd_dx_tc(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
                              cudaStream_t s) {
-    static int attr_done = 0;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_dx_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    static int attr_done[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dx_tc_kernel, kSmemBytes, attr_done);
         if (e != cudaSuccess) return e;
-        attr_done = 1;
     }
     DxTcParams P;
     P.d = d;

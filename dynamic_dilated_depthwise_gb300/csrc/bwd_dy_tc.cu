@@ -251,11 +251,10 @@ bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void*
 }
 
 cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
-    static int attr_done = 0;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_dy_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    static int attr_done[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dy_tc_kernel, kSmemBytes, attr_done);
         if (e != cudaSuccess) return e;
-        attr_done = 1;
     }
     DyTcParams P;
     P.d = d;

@@ -478,14 +478,10 @@ template <int K>
 cudaError_t launch_k(const Dims& d, const void* x, const void* y, const void* w, const void* bias, void* out,
                      cudaStream_t s) {
     using L = FwdLayout<K>;
-    static int attr_done = 0;
-    if (!attr_done) {
-        cudaError_t e =
-            cudaFuncSetAttribute(forward_tc_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(forward_tc_kernel<K>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    static int attr_done[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)forward_tc_kernel<K>, L::kSmemBytes, attr_done, true);
         if (e != cudaSuccess) return e;
-        attr_done = 1;
     }
     auto enc = bwdtc::encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;

@@ -36,6 +36,19 @@ constexpr unsigned kFlagCudaCores = 0x2u;
 // Multiprocessor count of the current device (cached per device).
 int num_sms();
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device,
+// once per device (done[] remembers the largest value set on each device).  With
+// prefer_max the kernel also asks for the largest shared-memory carve-out.
+inline cudaError_t set_max_dynamic_smem(const void* func, int bytes, int (&done)[64], bool prefer_max = false) {
+    int dev = 0;
+    const bool cached = cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64;
+    if (cached && done[dev] >= bytes) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && prefer_max) e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess && cached) done[dev] = bytes;
+    return e;
+}
+
 // Device address of the library's error word (set by kernels whose bounded
 // waits expire).
 unsigned int* device_error_word();
