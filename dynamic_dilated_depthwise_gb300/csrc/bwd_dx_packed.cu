@@ -22,6 +22,10 @@
 //   - the bias is a last K=16 step: A is a one-hot row selecting tap k (the same
 //     eight rows for every slot group: row-group stride 0), B a resident table of
 //     bias[d, c, k];
+//   - two threads in different warps issue the MMAs, even and odd taps: tcgen05.mma
+//     issue waits for the tensor pipe to accept the instruction, so one thread's waits
+//     and bookkeeping between taps would leave the pipe idle; the other thread's taps
+//     fill those gaps (each thread commits its own MMAs);
 //   - D of each tap lands in one of eight TMEM buffers [128 x 64]; eight worker
 //     warps round it to bf16 and accumulate tap * grad in FP32 with one
 //     mixed-precision FMA per channel (bf16 operands, exact product).
@@ -37,10 +41,12 @@ constexpr int kPTH = 16, kPTW = 8;         // pixel tile
 constexpr int kPN = 64;                    // MMA N: channels (zero padded beyond C)
 constexpr int kPTaps = 27;
 constexpr int kPWork = 8;                  // worker warps
-constexpr int kPThreads = 32 * (2 + kPWork);
+constexpr int kPIssuers = 2;               // MMA-issuing threads (warp 1 and the last warp), alternate taps
+constexpr int kPIssuer2 = 2 + kPWork;      // warp of the second issuer
+constexpr int kPThreads = 32 * (3 + kPWork);
 constexpr int kPDBufs = 8;                 // TMEM accumulators of 64 columns
 constexpr int kPMaxStages = 8;             // W ring depth cap
-constexpr int kPMinStages = 3;
+constexpr int kPMinStages = 2;
 constexpr int kPMaxR = 6;
 constexpr int kPWTile = 8192;              // W rows of one tap: [64 c][64 j] bf16, SW128
 constexpr int kPOneHot = 9 * 256;          // one-hot A rows, 9 taps x 2 chunks x 8 rows x 16 B
@@ -78,6 +84,9 @@ DxPackedLayout dx_packed_layout(const Dims& d) {
     rest += kPOneHot + kPBiasTab;
     int stages = (kPSmemCap - 1024 - rest) / kPWTile;
     if (stages > kPMaxStages) stages = kPMaxStages;
+    // an even number of stages: tap i uses stage i % stages, so every use of a stage falls
+    // to the same issuer (taps alternate between the two) and its phase waits stay in order
+    stages &= ~1;
     if (stages < kPMinStages || R > kPMaxR) return L;
     L.stages = stages;
     L.oyw = stages * kPWTile;
@@ -164,7 +173,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // them generic loads and stores with 64-bit addresses)
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ uint64_t wt_full[kPMaxStages], wt_empty[kPMaxStages], d_full[kPDBufs], d_empty[kPDBufs];
-    __shared__ uint64_t yw_full, yw_empty, gw_full[3], gw_empty[3], mma_done;
+    __shared__ uint64_t yw_full, yw_empty, gw_full[3], gw_empty[3], mma_done[kPIssuers];
     __shared__ uint32_t tmem_slot;
     __shared__ uint32_t a_shift[kPTaps];   // per-tap start offset of the A operand in the y window, bytes
     __shared__ int abort_flag;
@@ -193,16 +202,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(&d_empty[i], kPWork);
         }
         mbar_init(&yw_full, 1);
-        mbar_init(&yw_empty, 1);
+        mbar_init(&yw_empty, kPIssuers);   // each issuer commits once per tile
         for (int i = 0; i < 3; ++i) {
             mbar_init(&gw_full[i], 1);
             mbar_init(&gw_empty[i], kPWork);
         }
-        mbar_init(&mma_done, 1);
+        for (int i = 0; i < kPIssuers; ++i) mbar_init(&mma_done[i], 1);
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(&tmem_slot, 512);
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 2 + kPWork) {
         // constant operands: one-hot tap selectors, bias tables, zero chunks of the y window
         const int et = threadIdx.x - 64, nt = 32 * kPWork;
         unsigned short* oh = reinterpret_cast<unsigned short*>(sm + P.ooh);
@@ -283,8 +292,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int dd = 0; dd < 3; ++dd)
                 if (ng[dd] > 0) mbar_wait(&gw_full[dd], (ng[dd] - 1) & 1, P.err, &never);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == kPIssuer2) {
+        // ------------------------------------------------------- MMA issuers: taps of parity `par`
+        const int par = warp == 1 ? 0 : 1;
         if (lane == 0 && n_my > 0) {
             // descriptors are built once; each MMA only moves a start address (desc_advance)
             const uint32_t idesc = instr_desc(1, 0, 0, 128, kPN);
@@ -294,45 +304,40 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint64_t oh_base = smem_desc(smem_u32(sm + P.ooh), 128, 0, kSwizzleNone);
             const uint64_t bt_base = smem_desc(smem_u32(sm + P.obt), 128, 256, kSwizzleNone);
             const int nks = P.nks;
-            int st = 0, sph = 0, buf = 0, bph = 0;    // W ring stage / TMEM buffer and their phase parities
             bool ok = true;
             for (int tl = 0; tl < n_my && ok; ++tl) {
                 if (!mbar_wait(&yw_full, tl & 1, P.err, abort_v)) break;
                 tc_fence_after();
-                for (int dd = 0; dd < 3 && ok; ++dd) {
-                    for (int k = 0; k < 9; ++k) {
-                        if (!mbar_wait(&wt_full[st], sph, P.err, abort_v) ||
-                            !mbar_wait(&d_empty[buf], bph ^ 1, P.err, abort_v)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t a = desc_advance(a_base, a_shift[dd * 9 + k]);
-                        const uint64_t b = desc_advance(w_base, (uint32_t)st * kPWTile);
-                        const uint32_t dt = tmem + buf * kPN;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            if (kk < nks)
-                                mma_f16(dt, desc_advance(a, 2 * kk * lbo_y), desc_advance(b, kk * 32), idesc,
-                                        kk > 0 ? 1u : 0u);
-                        mma_f16(dt, desc_advance(oh_base, k * 256), desc_advance(bt_base, dd * 2048), idesc, 1u);
-                        mma_commit(&d_full[buf]);
-                        mma_commit(&wt_empty[st]);
-                        if (++st == S) {
-                            st = 0;
-                            sph ^= 1;
-                        }
-                        if (++buf == kPDBufs) {
-                            buf = 0;
-                            bph ^= 1;
-                        }
+                for (int u = 0; u < kPTaps; ++u) {
+                    const int i = tl * kPTaps + u;             // global tap counter of this CTA
+                    if ((i & 1) != par) continue;
+                    const int dd = u / 9, k = u - dd * 9;
+                    const int st = i % S, sph = (i / S) & 1;   // W ring stage and its phase parity
+                    const int buf = i % kPDBufs, bph = (i / kPDBufs) & 1;
+                    if (!mbar_wait(&wt_full[st], sph, P.err, abort_v) ||
+                        !mbar_wait(&d_empty[buf], bph ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint64_t a = desc_advance(a_base, a_shift[dd * 9 + k]);
+                    const uint64_t b = desc_advance(w_base, (uint32_t)st * kPWTile);
+                    const uint32_t dt = tmem + buf * kPN;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        if (kk < nks)
+                            mma_f16(dt, desc_advance(a, 2 * kk * lbo_y), desc_advance(b, kk * 32), idesc,
+                                    kk > 0 ? 1u : 0u);
+                    mma_f16(dt, desc_advance(oh_base, k * 256), desc_advance(bt_base, dd * 2048), idesc, 1u);
+                    mma_commit(&d_full[buf]);
+                    mma_commit(&wt_empty[st]);
                 }
                 if (ok) mma_commit(&yw_empty);
             }
-            mma_commit(&mma_done);
+            // every MMA this thread issued retires before TMEM is released
+            mma_commit(&mma_done[par]);
             int never = 0;
-            mbar_wait(&mma_done, 0, P.err, &never);
+            mbar_wait(&mma_done[par], 0, P.err, &never);
         }
     } else {
         // ------------------------------------------------------- workers: round, gather, accumulate
