@@ -11,10 +11,13 @@
 // GB300 design.  A CTA owns a block of taps -- 14 channels of one dilation,
 // 126 taps, padded to the MMA M of 128 -- and one pixel split.  Per 2x64
 // pixel tile:
-//   - TMA brings y [64 j x 128 px] (one 128-byte row per channel and tile row,
-//     128B-swizzled: a K-major operand), the block's 14 grad planes [16 x 128
-//     px] and the matching x windows [(2+2R) x 80 px], zero-filled outside the
-//     image;
+//   - one producer warp's TMA brings y [64 j x 128 px] (one 128-byte row per
+//     channel and tile row, 128B-swizzled: a K-major operand) into a 3-stage
+//     ring that the MMA releases;
+//   - another brings the block's 14 grad planes [14 x 128 px] and the matching
+//     x windows [14 x (2+2R) x 80 px], zero-filled outside the image, into a
+//     ring of 2-4 stages (as many as shared memory holds for the halo) that
+//     the formers release as soon as dK is formed;
 //   - eight warps form dK^T[o, px] (bwdtc::form_dk_tile) into a 128B-swizzled
 //     K-major operand;
 //   - one thread issues D[o, n] += dK^T[o, px] * Y[n, px] with N = 80 rows: the
@@ -30,21 +33,38 @@ using namespace bwdtc;
 
 constexpr int kNY = 80;           // MMA N: 64 y channels + ones row + 15 zero rows
 constexpr int kFormWarps = 8;
-constexpr int kThreads = 32 * (2 + kFormWarps);
-constexpr int kWinRowsMax = kTH + 2 * kMaxR;   // 18
+constexpr int kThreads = 32 * (3 + kFormWarps);   // x/grad producer, MMA, formers, y producer
+constexpr int kYWarp = 2 + kFormWarps;             // warp of the y producer
+constexpr int kYStages = 3;
+constexpr int kMaxXgStages = 4;
+constexpr int kSmemCap = 232448 - 1024;            // dynamic shared memory: the opt-in 227 KiB less the static part
 
-// shared memory (bytes from a 1024-aligned base)
+// shared memory (bytes from a 1024-aligned base): two dK^T tiles, the y ring, then the
+// x/grad ring (its stage size depends on the halo radius)
 constexpr int kDK = 0;                               // 2 x dK^T tiles
-constexpr int kYS = kDK + 2 * kDKBytes;              // 2 stages x 2 halves x [80 rows x 128 B]
+constexpr int kYS = kDK + 2 * kDKBytes;              // y ring: stages x 2 halves x [80 rows x 128 B]
 constexpr int kYHalf = kNY * 128;                    // 10240
 constexpr int kYStage = 2 * kYHalf;                  // 20480
-constexpr int kGS = kYS + 2 * kYStage;               // 2 stages x [16 slots x 128 px] bf16
-constexpr int kGStage = kSlots * kPx * 2;            // 4096
-constexpr int kXS = kGS + 2 * kGStage;               // 2 stages x [16 slots x rows x 80] bf16
-constexpr int kXStage = kSlots * kWinRowsMax * kWinCols * 2;  // 46080
-constexpr int kSmemBytes = kXS + 2 * kXStage + 1024 + 128;   // + alignment slack + over-read margin
+constexpr int kXG = kYS + kYStages * kYStage;        // x/grad ring
+constexpr int kGStage = kCB * kPx * 2;               // grad planes of the block [14 x 128 px] bf16
+constexpr int kSlack = 1024 + 128;                   // alignment slack + over-read margin
 static_assert(kYS % 1024 == 0 && kYStage % 1024 == 0 && kYHalf % 1024 == 0, "SW128 atoms need 1 KiB");
-static_assert(kGS % 128 == 0 && kXS % 128 == 0 && kGStage % 128 == 0 && kXStage % 128 == 0, "TMA dst 128 B");
+static_assert(kXG % 128 == 0 && kGStage % 128 == 0, "TMA dst 128 B");
+
+struct XgLayout {
+    int stage_bytes;   // grad planes + x windows, rounded up to 128 B
+    int stages;        // 0 when even two stages do not fit
+};
+
+// The x/grad stage holds the block's grad planes and its x windows [14 x (2+2R) x 80].
+inline XgLayout xg_layout(int R) {
+    XgLayout L;
+    const int xbytes = kCB * (kTH + 2 * R) * kWinCols * 2;
+    L.stage_bytes = (kGStage + xbytes + 127) / 128 * 128;
+    int n = (kSmemCap - kSlack - kXG) / L.stage_bytes;
+    L.stages = n > kMaxXgStages ? kMaxXgStages : (n < 2 ? 0 : n);
+    return L;
+}
 
 struct DwTcParams {
     Dims d;
@@ -54,10 +74,16 @@ struct DwTcParams {
     int tiles_per_split;
     int R, WHx;        // halo radius, window rows (2 + 2R)
     int xslot_bytes;   // WHx * 80 * 2
+    int xg_stage, xg_stages;
     float* ws;         // [S][O][C+1]
     unsigned int* err;
 };
 
+// Pipeline per pixel tile i:
+//   x/grad producer --xg_full--> formers --dk_full--> MMA <--y_full-- y producer
+// The formers release the x/grad stage (xg_empty) as soon as dK^T is formed, and the
+// MMA releases the y stage and the dK^T buffer through commits, so the next windows
+// load while the tensor cores still read the previous tile.
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dw_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmG,
                      const __grid_constant__ CUtensorMap tmX, const DwTcParams P) {
@@ -67,7 +93,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // access through it stays a shared-memory access (an integer round trip would make
     // them generic loads and stores with 64-bit addresses)
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t in_full[2], in_empty[2], dk_full[2], dk_empty[2], acc_done, mma_done;
+    __shared__ uint64_t y_full[kYStages], y_empty[kYStages], xg_full[kMaxXgStages], xg_empty[kMaxXgStages];
+    __shared__ uint64_t dk_full[2], dk_empty[2], acc_done, mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -80,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_begin = split * P.tiles_per_split;
     const int t_end = min(t_begin + P.tiles_per_split, P.n_tiles);
     const int n_my = max(0, t_end - t_begin);
+    const int NX = P.xg_stages;
 
     // this block of taps: dilation dd, channels [c_first, c_first + nc)
     const int dd = ob / P.n_cblk;
@@ -90,9 +118,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        for (int s = 0; s < kYStages; ++s) {
+            mbar_init(&y_full[s], 1);
+            mbar_init(&y_empty[s], 1);
+        }
+        for (int s = 0; s < NX; ++s) {
+            mbar_init(&xg_full[s], 1);
+            mbar_init(&xg_empty[s], kFormWarps);
+        }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&in_full[s], 1);
-            mbar_init(&in_empty[s], kFormWarps + 1);
             mbar_init(&dk_full[s], kFormWarps);
             mbar_init(&dk_empty[s], 1);
         }
@@ -101,10 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(&tmem_slot, 128);
-    if (warp >= 2) {
-        // rows 64..79 of both y stages / halves: a row of ones (dbias) and 15 zero rows
+    if (warp >= 2 && warp < 2 + kFormWarps) {
+        // rows 64..79 of every y stage / half: a row of ones (dbias) and 15 zero rows
         const int et = threadIdx.x - 64;
-        for (int i = et; i < 2 * 2 * 16 * 32; i += 32 * kFormWarps) {
+        for (int i = et; i < kYStages * 2 * 16 * 32; i += 32 * kFormWarps) {
             const int word = i % 32, row = (i / 32) % 16, half = (i / 512) % 2, st = i / 1024;
             const uint32_t v = row == 0 ? 0x3F803F80u : 0u;  // bf16 pair (1.0, 1.0)
             reinterpret_cast<uint32_t*>(sm + kYS + st * kYStage + half * kYHalf + (64 + row) * 128)[word] = v;
@@ -119,31 +153,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------- TMA producer
+        // ------------------------------------------------------- x / grad producer
         if (lane == 0) {
-            prefetch_tmap(&tmY);
             prefetch_tmap(&tmG);
             prefetch_tmap(&tmX);
-            const uint32_t bytes = 2 * 8192 + kGStage + kSlots * P.xslot_bytes;
+            const uint32_t bytes = kGStage + kCB * P.xslot_bytes;
             int issued = 0;
             for (int i = 0; i < n_my; ++i) {
-                const int s = i & 1, ph = (i >> 1) & 1;
-                if (!mbar_wait(&in_empty[s], ph ^ 1, P.err, abort_v)) break;
+                const int s = i % NX, ph = (i / NX) & 1;
+                if (!mbar_wait(&xg_empty[s], ph ^ 1, P.err, abort_v)) break;
+                const int t = t_begin + i;
+                const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
+                const int h0 = (ti / P.tiles_w) * kTH, w0 = (ti % P.tiles_w) * kTW;
+                uint8_t* st = sm + kXG + s * P.xg_stage;
+                mbar_arrive_expect_tx(&xg_full[s], bytes);
+                tma_load_4d(st, &tmG, &xg_full[s], w0, h0, (1 + dd) * C + c_first, b);
+                tma_load_4d(st + kGStage, &tmX, &xg_full[s], w0 - 8, h0 - P.R, c_first, b);
+                issued = i + 1;
+            }
+            // drain: every copy this thread started lands before its shared memory is released
+            int never = 0;
+            for (int i = issued > NX ? issued - NX : 0; i < issued; ++i)
+                mbar_wait(&xg_full[i % NX], (i / NX) & 1, P.err, &never);
+        }
+    } else if (warp == kYWarp) {
+        // ------------------------------------------------------- y producer
+        if (lane == 0) {
+            prefetch_tmap(&tmY);
+            int issued = 0;
+            for (int i = 0; i < n_my; ++i) {
+                const int s = i % kYStages, ph = (i / kYStages) & 1;
+                if (!mbar_wait(&y_empty[s], ph ^ 1, P.err, abort_v)) break;
                 const int t = t_begin + i;
                 const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
                 const int h0 = (ti / P.tiles_w) * kTH, w0 = (ti % P.tiles_w) * kTW;
                 uint8_t* ys = sm + kYS + s * kYStage;
-                mbar_arrive_expect_tx(&in_full[s], bytes);
-                tma_load_4d(ys, &tmY, &in_full[s], w0, h0, 0, b);
-                tma_load_4d(ys + kYHalf, &tmY, &in_full[s], w0, h0 + 1, 0, b);
-                tma_load_4d(sm + kGS + s * kGStage, &tmG, &in_full[s], w0, h0, (1 + dd) * C + c_first, b);
-                tma_load_4d(sm + kXS + s * kXStage, &tmX, &in_full[s], w0 - 8, h0 - P.R, c_first, b);
+                mbar_arrive_expect_tx(&y_full[s], 2 * 8192);
+                tma_load_4d(ys, &tmY, &y_full[s], w0, h0, 0, b);
+                tma_load_4d(ys + kYHalf, &tmY, &y_full[s], w0, h0 + 1, 0, b);
                 issued = i + 1;
             }
-            // drain: every copy this CTA started lands before its shared memory is released
             int never = 0;
-            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-                mbar_wait(&in_full[i & 1], (i >> 1) & 1, P.err, &never);
+            for (int i = issued > kYStages ? issued - kYStages : 0; i < issued; ++i)
+                mbar_wait(&y_full[i % kYStages], (i / kYStages) & 1, P.err, &never);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -155,13 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int i = 0; i < n_my && ok; ++i) {
                 const int s = i & 1, ph = (i >> 1) & 1;
-                if (!mbar_wait(&dk_full[s], ph, P.err, abort_v) || !mbar_wait(&in_full[s], ph, P.err, abort_v)) {
+                const int sy = i % kYStages, yph = (i / kYStages) & 1;
+                if (!mbar_wait(&dk_full[s], ph, P.err, abort_v) || !mbar_wait(&y_full[sy], yph, P.err, abort_v)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint64_t da = desc_advance(dk_base, (uint32_t)s * kDKBytes);
-                const uint64_t ya = desc_advance(y_base, (uint32_t)s * kYStage);
+                const uint64_t ya = desc_advance(y_base, (uint32_t)sy * kYStage);
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
 #pragma unroll
@@ -169,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_f16(tmem, desc_advance(da, half * 16384 + kk * 32), desc_advance(ya, half * kYHalf + kk * 32),
                                 idesc, (i > 0 || half > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&dk_empty[s]);
-                mma_commit(&in_empty[s]);
+                mma_commit(&y_empty[sy]);
             }
             if (ok) mma_commit(&acc_done);
             mma_commit(&mma_done);
@@ -183,18 +236,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int i = 0; i < n_my && ok; ++i) {
             const int s = i & 1, ph = (i >> 1) & 1;
-            if (!mbar_wait(&in_full[s], ph, P.err, abort_v) || !mbar_wait(&dk_empty[s], ph ^ 1, P.err, abort_v)) {
+            const int sx = i % NX, xph = (i / NX) & 1;
+            if (!mbar_wait(&xg_full[sx], xph, P.err, abort_v) || !mbar_wait(&dk_empty[s], ph ^ 1, P.err, abort_v)) {
                 ok = false;
                 break;
             }
-            form_dk_tile(sm + kDK + s * kDKBytes, reinterpret_cast<const uint32_t*>(sm + kXS + s * kXStage),
-                         reinterpret_cast<const bf16*>(sm + kGS + s * kGStage), kPx, nrows, slot_elems, P.R, dil, 0, et,
-                         32 * kFormWarps);
+            const uint8_t* st = sm + kXG + sx * P.xg_stage;
+            form_dk_tile(sm + kDK + s * kDKBytes, reinterpret_cast<const uint32_t*>(st + kGStage),
+                         reinterpret_cast<const bf16*>(st), kPx, nrows, slot_elems, P.R, dil, 0, et, 32 * kFormWarps);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&dk_full[s]);
-                mbar_arrive(&in_empty[s]);
+                mbar_arrive(&xg_empty[sx]);
             }
         }
         // epilogue: this split's partial sums for the block of taps
@@ -239,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 bool bwd_dw_tc_eligible(const Dims& d, const void* g, const void* x, const void* y) {
-    return bwdtc::eligible(d, g, x, y);
+    return bwdtc::eligible(d, g, x, y) && xg_layout(d.R()).stages >= 2;
 }
 
 int bwd_dw_tc_splits(const Dims& d, size_t workspace_bytes) {
@@ -258,7 +312,7 @@ cudaError_t launch_bwd_dw_tc(const Dims& d, const void* g, const void* x, const 
                              cudaStream_t s) {
     static int attr_done[64] = {};
     {
-        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dw_tc_kernel, kSmemBytes, attr_done);
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dw_tc_kernel, kSmemCap, attr_done);
         if (e != cudaSuccess) return e;
     }
     DwTcParams P;
@@ -272,16 +326,21 @@ cudaError_t launch_bwd_dw_tc(const Dims& d, const void* g, const void* x, const 
     P.R = d.R();
     P.WHx = kTH + 2 * P.R;
     P.xslot_bytes = P.WHx * kWinCols * 2;
+    const XgLayout L = xg_layout(P.R);
+    if (L.stages < 2) return cudaErrorInvalidValue;
+    P.xg_stage = L.stage_bytes;
+    P.xg_stages = L.stages;
+    const int smem_bytes = kXG + L.stages * L.stage_bytes + kSlack;
     P.ws = ws;
     P.err = device_error_word();
     if (P.err == nullptr) return cudaErrorUnknown;
     CUtensorMap tmY, tmG, tmX;
     if (!encode_nchw(&tmY, y, d, d.C, kTW, 1, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_nchw(&tmG, g, d, 4 * d.C, kTW, kTH, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_nchw(&tmX, x, d, d.C, kWinCols, (uint32_t)P.WHx, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !encode_nchw(&tmG, g, d, 4 * d.C, kTW, kTH, kCB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_nchw(&tmX, x, d, d.C, kWinCols, (uint32_t)P.WHx, kCB, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     trace_begin(s, kKBwdDwTc);
-    bwd_dw_tc_kernel<<<P.n_oblk * S, kThreads, kSmemBytes, s>>>(tmY, tmG, tmX, P);
+    bwd_dw_tc_kernel<<<P.n_oblk * S, kThreads, smem_bytes, s>>>(tmY, tmG, tmX, P);
     trace_end(s);
     return cudaGetLastError();
 }
