@@ -119,45 +119,64 @@ __device__ __forceinline__ void fma2_bf16_f32(float& a0, float& a1, uint32_t t, 
 
 // ----------------------------------------------------------------------------- pack
 // Thread = (tensor, b, group, chunk, 8-pixel run): eight 16-byte channel rows in,
-// eight 16-byte pixel rows out.  HW is a multiple of 8 (W is).
-__global__ void __launch_bounds__(kPackThreads)
+// eight 16-byte pixel rows out.  HW is a multiple of 8 (W is).  Run idx (y runs
+// first, then the grad runs) lands at bytes [128 idx, 128 idx + 128) of the packed
+// buffer (gc follows yc), so the 256 runs of a block fill one contiguous 32 KiB range:
+// the block transposes through shared memory and writes that range with 512-byte
+// warp stores instead of 16-byte pieces 128 bytes apart.
+__global__ void __launch_bounds__(kPackThreads, 2)
     pack_chunks_kernel(const bf16* __restrict__ y, const bf16* __restrict__ g, bf16* __restrict__ yc,
-                       bf16* __restrict__ gc, int B, int C, long long HW, long long n_y, long long n_all) {
+                       int B, int C, long long HW, long long n_y, long long n_all) {
+    // [run][8 pixel rows of 16 B], pixel row p of run r at column p ^ (r & 7)
+    __shared__ uint4 stage[kPackThreads * 8];
     const int nch = C / 8;
     const long long runs = HW / 8;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < n_all;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const bf16* src;
-        bf16* dst;
-        if (idx < n_y) {
-            const long long o = idx % runs, bc = idx / runs;   // bc = b * nch + cb
-            const long long b = bc / nch, cb = bc % nch;
-            src = y + (b * C + cb * 8) * HW + o * 8;
-            dst = yc + (bc * HW + o * 8) * 8;
-        } else {
-            const long long j = idx - n_y;
-            const long long o = j % runs, bgc = j / runs;      // bgc = (b * 3 + grp) * nch + cb
-            const long long cb = bgc % nch, bg = bgc / nch;
-            const long long b = bg / 3, grp = bg % 3;
-            src = g + (b * 4 * C + C + grp * C + cb * 8) * HW + o * 8;
-            dst = gc + (bgc * HW + o * 8) * 8;
-        }
-        uint4 in[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) in[e] = __ldg(reinterpret_cast<const uint4*>(src + e * HW));
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            const uint32_t sel = (p & 1) ? 0x7632u : 0x5410u;
-            uint32_t w[4];
-#pragma unroll
-            for (int f = 0; f < 4; ++f) {
-                const uint4 a = in[2 * f], b = in[2 * f + 1];
-                const uint32_t aw = (p >> 1) == 0 ? a.x : (p >> 1) == 1 ? a.y : (p >> 1) == 2 ? a.z : a.w;
-                const uint32_t bw = (p >> 1) == 0 ? b.x : (p >> 1) == 1 ? b.y : (p >> 1) == 2 ? b.z : b.w;
-                w[f] = __byte_perm(aw, bw, sel);
+    const int tid = threadIdx.x;
+    uint4* out = reinterpret_cast<uint4*>(yc);
+    for (long long r0 = (long long)blockIdx.x * kPackThreads; r0 < n_all; r0 += (long long)gridDim.x * kPackThreads) {
+        const long long idx = r0 + tid;
+        if (idx < n_all) {
+            const bf16* src;
+            if (idx < n_y) {
+                const long long o = idx % runs, bc = idx / runs;   // bc = b * nch + cb
+                const long long b = bc / nch, cb = bc % nch;
+                src = y + (b * C + cb * 8) * HW + o * 8;
+            } else {
+                const long long j = idx - n_y;
+                const long long o = j % runs, bgc = j / runs;      // bgc = (b * 3 + grp) * nch + cb
+                const long long cb = bgc % nch, bg = bgc / nch;
+                const long long b = bg / 3, grp = bg % 3;
+                src = g + (b * 4 * C + C + grp * C + cb * 8) * HW + o * 8;
             }
-            *reinterpret_cast<uint4*>(dst + p * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            uint4 in[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) in[e] = __ldg(reinterpret_cast<const uint4*>(src + e * HW));
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const uint32_t sel = (p & 1) ? 0x7632u : 0x5410u;
+                uint32_t w[4];
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    const uint4 a = in[2 * f], b = in[2 * f + 1];
+                    const uint32_t aw = (p >> 1) == 0 ? a.x : (p >> 1) == 1 ? a.y : (p >> 1) == 2 ? a.z : a.w;
+                    const uint32_t bw = (p >> 1) == 0 ? b.x : (p >> 1) == 1 ? b.y : (p >> 1) == 2 ? b.z : b.w;
+                    w[f] = __byte_perm(aw, bw, sel);
+                }
+                stage[tid * 8 + (p ^ (tid & 7))] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
+        __syncthreads();
+        // copy out: 16-byte piece k of the block's range is pixel row (k & 7) of run k >> 3
+        const long long n_pieces = (n_all - r0 < kPackThreads ? n_all - r0 : kPackThreads) * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int k = i * kPackThreads + tid;
+            if (k < n_pieces) {
+                const int r = k >> 3, pr = k & 7;
+                out[r0 * 8 + k] = stage[r * 8 + (pr ^ (r & 7))];
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -477,8 +496,8 @@ cudaError_t launch_bwd_dx_packed(const Dims& d, const void* g, const void* y, co
         if (blocks > cap) blocks = cap;
         trace_begin(s, kKPackChunks);
         pack_chunks_kernel<<<(unsigned)blocks, kPackThreads, 0, s>>>(static_cast<const bf16*>(y),
-                                                                     static_cast<const bf16*>(g), yc, gc, d.B, d.C,
-                                                                     d.HW, n_y, n_all);
+                                                                     static_cast<const bf16*>(g), yc, d.B, d.C, d.HW,
+                                                                     n_y, n_all);
         trace_end(s);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -7,9 +7,11 @@
 //
 // GB300 design.  Persistent CTAs walk super tiles of 8 rows x 64 columns (four
 // 2x64 sub-tiles, 512 pixels).  For each super tile the CTA visits every block
-// of taps (14 channels of one dilation, 126 taps); per block one TMA stage
-// brings the block's W rows [128 o x 64 j], grad planes [16 x 512 px] and x
-// windows [16 x (8+2R) x 80], and serves four sub-tiles:
+// of taps (14 channels of one dilation, 126 taps); per block one producer
+// warp's TMA brings the block's W rows [128 o x 64 j] into a 3-stage ring that
+// the MMA releases, and another brings its grad planes [14 x 512 px] and x
+// windows [14 x (8+2R) x 80] into a 2-stage ring that the formers release once
+// the four sub-tiles are formed; per block:
 //   - eight warps form each sub-tile's dK^T tile (bwdtc::form_dk_tile);
 //   - one thread issues D_st[px, j] += dK[px, o] * W[o, j] (M = 128 pixels read
 //     MN-major from the dK^T tile, N = 64, K = 128 taps in eight K=16 steps).
@@ -30,20 +32,21 @@ constexpr int kSPx = kSub * kPx;  // 512 pixels
 constexpr int kDyMaxR = 5;        // halo radius the window buffers hold
 constexpr int kFormWarps = 8;
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 32 * (2 + kFormWarps + kEpiWarps);
+constexpr int kWWarp = 2 + kFormWarps + kEpiWarps;   // warp of the W producer
+constexpr int kThreads = 32 * (3 + kFormWarps + kEpiWarps);
 constexpr int kWinRowsMax = kSTH + 2 * kDyMaxR;   // 18
+constexpr int kWStages = 3, kXgStages = 2;
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr int kDK = 0;                               // 2 x dK^T tiles
-constexpr int kWS = kDK + 2 * kDKBytes;              // 2 stages x W block [128 o x 128 B] SW128
+constexpr int kWS = kDK + 2 * kDKBytes;              // W ring: stages x W block [128 o x 128 B] SW128
 constexpr int kWStage = kBlockRows * 128;            // 16384
-constexpr int kGS = kWS + 2 * kWStage;               // 2 stages x [16 slots x 512 px] bf16
-constexpr int kGStage = kSlots * kSPx * 2;           // 16384
-constexpr int kXS = kGS + 2 * kGStage;               // 2 stages x [16 slots x rows x 80] bf16
-constexpr int kXStage = kSlots * kWinRowsMax * kWinCols * 2;  // 46080
-constexpr int kSmemBytes = kXS + 2 * kXStage + 1024 + 128;   // + alignment slack + over-read margin
+constexpr int kXG = kWS + kWStages * kWStage;        // x/grad ring
+constexpr int kGStage = kCB * kSPx * 2;              // grad planes [14 x 512 px] bf16
+constexpr int kXgStage = kGStage + kCB * kWinRowsMax * kWinCols * 2;   // + x windows [14 x rows x 80] bf16
+constexpr int kSmemBytes = kXG + kXgStages * kXgStage + 1024 + 128;   // + alignment slack + over-read margin
 static_assert(kWS % 1024 == 0 && kWStage % 1024 == 0, "SW128 atoms need 1 KiB");
-static_assert(kGS % 128 == 0 && kXS % 128 == 0 && kXStage % 128 == 0, "TMA dst 128 B");
+static_assert(kXG % 128 == 0 && kGStage % 128 == 0 && kXgStage % 128 == 0, "TMA dst 128 B");
 
 struct DyTcParams {
     Dims d;
@@ -63,7 +66,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // access through it stays a shared-memory access (an integer round trip would make
     // them generic loads and stores with 64-bit addresses)
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t in_full[2], in_empty[2], dk_full[2], dk_empty[2], acc_full[2], acc_empty[2], mma_done;
+    __shared__ uint64_t w_full[kWStages], w_empty[kWStages], xg_full[kXgStages], xg_empty[kXgStages];
+    __shared__ uint64_t dk_full[2], dk_empty[2], acc_full[2], acc_empty[2], mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -75,9 +79,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&w_full[s], 1);
+            mbar_init(&w_empty[s], 1);
+        }
+        for (int s = 0; s < kXgStages; ++s) {
+            mbar_init(&xg_full[s], 1);
+            mbar_init(&xg_empty[s], kFormWarps);
+        }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&in_full[s], 1);
-            mbar_init(&in_empty[s], kFormWarps + 1);
             mbar_init(&dk_full[s], kFormWarps);
             mbar_init(&dk_empty[s], 1);
             mbar_init(&acc_full[s], 1);
@@ -98,12 +108,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------- TMA producer
+        // ------------------------------------------------------- x / grad producer
         if (lane == 0) {
-            prefetch_tmap(&tmW);
             prefetch_tmap(&tmG);
             prefetch_tmap(&tmX);
-            const uint32_t bytes = kWStage + kGStage + kSlots * P.xslot_bytes;
+            const uint32_t bytes = kGStage + kCB * P.xslot_bytes;
             int issued = 0;
             bool ok = true;
             for (int tl = 0; tl < n_my && ok; ++tl) {
@@ -111,22 +120,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
                 const int h0 = (ti / P.tiles_w) * kSTH, w0 = (ti % P.tiles_w) * kTW;
                 for (int ob = 0; ob < NB; ++ob) {
-                    const int i = tl * NB + ob, s = i & 1, ph = (i >> 1) & 1;
-                    if (!mbar_wait(&in_empty[s], ph ^ 1, P.err, abort_v)) {
+                    const int i = tl * NB + ob, s = i % kXgStages, ph = (i / kXgStages) & 1;
+                    if (!mbar_wait(&xg_empty[s], ph ^ 1, P.err, abort_v)) {
                         ok = false;
                         break;
                     }
                     const int dd = ob / P.n_cblk, c_first = (ob % P.n_cblk) * kCB;
-                    mbar_arrive_expect_tx(&in_full[s], bytes);
-                    tma_load_2d(sm + kWS + s * kWStage, &tmW, &in_full[s], 0, (dd * C + c_first) * 9);
-                    tma_load_4d(sm + kGS + s * kGStage, &tmG, &in_full[s], w0, h0, (1 + dd) * C + c_first, b);
-                    tma_load_4d(sm + kXS + s * kXStage, &tmX, &in_full[s], w0 - 8, h0 - P.R, c_first, b);
+                    uint8_t* st = sm + kXG + s * kXgStage;
+                    mbar_arrive_expect_tx(&xg_full[s], bytes);
+                    tma_load_4d(st, &tmG, &xg_full[s], w0, h0, (1 + dd) * C + c_first, b);
+                    tma_load_4d(st + kGStage, &tmX, &xg_full[s], w0 - 8, h0 - P.R, c_first, b);
+                    issued = i + 1;
+                }
+            }
+            // drain: every copy this thread started lands before its shared memory is released
+            int never = 0;
+            for (int i = issued > kXgStages ? issued - kXgStages : 0; i < issued; ++i)
+                mbar_wait(&xg_full[i % kXgStages], (i / kXgStages) & 1, P.err, &never);
+        }
+    } else if (warp == kWWarp) {
+        // ------------------------------------------------------- W producer
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            int issued = 0;
+            bool ok = true;
+            for (int tl = 0; tl < n_my && ok; ++tl) {
+                for (int ob = 0; ob < NB; ++ob) {
+                    const int i = tl * NB + ob, s = i % kWStages, ph = (i / kWStages) & 1;
+                    if (!mbar_wait(&w_empty[s], ph ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    const int dd = ob / P.n_cblk, c_first = (ob % P.n_cblk) * kCB;
+                    mbar_arrive_expect_tx(&w_full[s], kWStage);
+                    tma_load_2d(sm + kWS + s * kWStage, &tmW, &w_full[s], 0, (dd * C + c_first) * 9);
                     issued = i + 1;
                 }
             }
             int never = 0;
-            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-                mbar_wait(&in_full[i & 1], (i >> 1) & 1, P.err, &never);
+            for (int i = issued > kWStages ? issued - kWStages : 0; i < issued; ++i)
+                mbar_wait(&w_full[i % kWStages], (i / kWStages) & 1, P.err, &never);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -141,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&acc_empty[tb], tph ^ 1, P.err, abort_v)) break;
                 tc_fence_after();
                 for (int ob = 0; ob < NB && ok; ++ob) {
-                    const int i = tl * NB + ob, s = i & 1, ph = (i >> 1) & 1;
-                    if (!mbar_wait(&in_full[s], ph, P.err, abort_v)) {
+                    const int i = tl * NB + ob, s = i % kWStages, ph = (i / kWStages) & 1;
+                    if (!mbar_wait(&w_full[s], ph, P.err, abort_v)) {
                         ok = false;
                         break;
                     }
@@ -162,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (ob > 0 || kk > 0) ? 1u : 0u);
                         mma_commit(&dk_empty[db]);
                     }
-                    mma_commit(&in_empty[s]);
+                    mma_commit(&w_empty[s]);
                 }
                 if (ok) mma_commit(&acc_full[tb]);
             }
@@ -177,16 +210,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int tl = 0; tl < n_my && ok; ++tl) {
             for (int ob = 0; ob < NB && ok; ++ob) {
-                const int i = tl * NB + ob, s = i & 1, ph = (i >> 1) & 1;
-                if (!mbar_wait(&in_full[s], ph, P.err, abort_v)) {
+                const int i = tl * NB + ob, s = i % kXgStages, ph = (i / kXgStages) & 1;
+                if (!mbar_wait(&xg_full[s], ph, P.err, abort_v)) {
                     ok = false;
                     break;
                 }
                 const int dd = ob / P.n_cblk, c_first = (ob % P.n_cblk) * kCB;
                 const int nrows = min(kCB, C - c_first) * 9;
                 const int dil = dil_of(P.d, dd);
-                const uint32_t* xs32 = reinterpret_cast<const uint32_t*>(sm + kXS + s * kXStage);
-                const bf16* gs = reinterpret_cast<const bf16*>(sm + kGS + s * kGStage);
+                const bf16* gs = reinterpret_cast<const bf16*>(sm + kXG + s * kXgStage);
+                const uint32_t* xs32 = reinterpret_cast<const uint32_t*>(sm + kXG + s * kXgStage + kGStage);
                 for (int st = 0; st < kSub; ++st) {
                     const int kd = i * kSub + st, db = kd & 1;
                     if (!mbar_wait(&dk_empty[db], ((kd >> 1) & 1) ^ 1, P.err, abort_v)) {
@@ -200,10 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&dk_full[db]);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&in_empty[s]);
+                if (lane == 0) mbar_arrive(&xg_empty[s]);
             }
         }
-    } else {
+    } else if (warp < kWWarp) {
         // ------------------------------------------------------- epilogue: dy stores
         const int q = warp & 3;
         const int m = q * 32 + lane;              // pixel slot == TMEM lane
@@ -280,8 +313,8 @@ cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const 
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    if (!encode_nchw(&tmG, g, d, 4 * d.C, kTW, kSTH, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_nchw(&tmX, x, d, d.C, kWinCols, (uint32_t)P.WHx, kSlots, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_nchw(&tmG, g, d, 4 * d.C, kTW, kSTH, kCB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_nchw(&tmX, x, d, d.C, kWinCols, (uint32_t)P.WHx, kCB, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     int grid = num_sms();
     if (grid > P.n_tiles) grid = P.n_tiles;
