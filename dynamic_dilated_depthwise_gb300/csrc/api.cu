@@ -2,7 +2,9 @@
 //
 // Host-side validation, kernel selection and launch on the caller's stream.
 // The library never allocates device memory, never synchronises (except in
-// ddpm_get_device_error) and never throws across the boundary.
+// ddpm_get_device_error) and never throws across the boundary.  The backward's
+// three independent pieces (dX, dY, dW) run side by side: dY and dW on two
+// library streams forked from and joined back into the caller's stream.
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -42,6 +44,36 @@ int num_sms() {
         cache[dev] = n;
     }
     return cache[dev];
+}
+
+// Two non-blocking streams per device, and the events that fork them from and join
+// them back into a caller's stream.  The events are re-recorded by every call, so a
+// call holds `mu` from the fork to the join.
+struct SideStreams {
+    cudaStream_t s[2];
+    cudaEvent_t fork, join[2];
+};
+
+std::mutex g_side_mu;
+
+cudaError_t side_streams(SideStreams** out) {
+    static SideStreams side[64];
+    static bool ready[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!ready[dev]) {
+        SideStreams& t = side[dev];
+        for (int i = 0; i < 2; ++i)
+            if ((e = cudaStreamCreateWithFlags(&t.s[i], cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&t.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        for (int i = 0; i < 2; ++i)
+            if ((e = cudaEventCreateWithFlags(&t.join[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+        ready[dev] = true;
+    }
+    *out = &side[dev];
+    return cudaSuccess;
 }
 
 }  // namespace ddpm
@@ -178,7 +210,16 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
         const bool packed = ddpm::bwd_dx_packed_eligible(d, grad_out, y, weight) &&
                             workspace_bytes >= poff + ddpm::bwd_dx_packed_bytes(d);
         const size_t part_bytes = packed ? poff : workspace_bytes;
-        cudaError_t e;
+        // dX on the caller's stream, dY and dW (+ reduce) on the two side streams: the
+        // pieces share only inputs, and each one's last partial wave of CTAs leaves SMs
+        // that the others fill
+        std::lock_guard<std::mutex> lock(ddpm::g_side_mu);
+        ddpm::SideStreams* ss = nullptr;
+        cudaError_t e = ddpm::side_streams(&ss);
+        if (e != cudaSuccess) return from_cuda(e);
+        if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return from_cuda(e);
+        for (int i = 0; i < 2; ++i)
+            if ((e = cudaStreamWaitEvent(ss->s[i], ss->fork, 0)) != cudaSuccess) return from_cuda(e);
         if (packed)
             e = ddpm::launch_bwd_dx_packed(d, grad_out, y, weight, bias, dx, static_cast<char*>(workspace) + poff, s);
         else if (ddpm::bwd_dx_tc_eligible(d, grad_out, y, weight))
@@ -187,21 +228,28 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
             e = ddpm::launch_bwd_dx_simt(d, grad_out, y, weight, bias, dx, s);
         if (e == cudaSuccess) {
             if (ddpm::bwd_dy_tc_eligible(d, grad_out, x, weight))
-                e = ddpm::launch_bwd_dy_tc(d, grad_out, x, weight, dy, s);
+                e = ddpm::launch_bwd_dy_tc(d, grad_out, x, weight, dy, ss->s[0]);
             else
-                e = ddpm::launch_bwd_dy_simt(d, grad_out, x, weight, dy, s);
+                e = ddpm::launch_bwd_dy_simt(d, grad_out, x, weight, dy, ss->s[0]);
         }
         if (e == cudaSuccess) {
+            const cudaStream_t sw = ss->s[1];
             if (ddpm::bwd_dw_tc_eligible(d, grad_out, x, y)) {
                 const int S = ddpm::bwd_dw_tc_splits(d, part_bytes);
-                e = ddpm::launch_bwd_dw_tc(d, grad_out, x, y, (float*)workspace, S, s);
-                if (e == cudaSuccess) e = ddpm::launch_bwd_reduce(d, (const float*)workspace, S, dweight, dbias, s);
+                e = ddpm::launch_bwd_dw_tc(d, grad_out, x, y, (float*)workspace, S, sw);
+                if (e == cudaSuccess) e = ddpm::launch_bwd_reduce(d, (const float*)workspace, S, dweight, dbias, sw);
             } else {
-                e = ddpm::launch_bwd_dw_partial_simt(d, grad_out, x, y, workspace, s);
+                e = ddpm::launch_bwd_dw_partial_simt(d, grad_out, x, y, workspace, sw);
                 if (e == cudaSuccess)
                     e = ddpm::launch_bwd_reduce(d, (const float*)workspace, ddpm::backward_num_splits(d), dweight,
-                                                dbias, s);
+                                                dbias, sw);
             }
+        }
+        // join, whatever happened above, so the side streams never run ahead of `stream`
+        for (int i = 0; i < 2; ++i) {
+            const cudaError_t er = cudaEventRecord(ss->join[i], ss->s[i]);
+            const cudaError_t ew = er == cudaSuccess ? cudaStreamWaitEvent(s, ss->join[i], 0) : er;
+            if (e == cudaSuccess) e = ew;
         }
         return from_cuda(e);
     } catch (...) {

@@ -18,7 +18,8 @@
 //   - TMA brings each dilation's grad window [chunk][(16+2d) x (8+2d)][8] into a
 //     buffer of its own, reloaded for the next tile as soon as the tile's nine taps
 //     of that dilation are gathered, so the load overlaps the other dilations;
-//   - W rows of one tap for all channels stream through a ring (3-D view of W);
+//   - W rows of one tap for all channels stream through a ring (3-D view of W) fed by
+//     a producer warp of its own, so the window loads never queue behind W stages;
 //   - the bias is a last K=16 step: A is a one-hot row selecting tap k (the same
 //     eight rows for every slot group: row-group stride 0), B a resident table of
 //     bias[d, c, k];
@@ -43,7 +44,8 @@ constexpr int kPTaps = 27;
 constexpr int kPWork = 8;                  // worker warps
 constexpr int kPIssuers = 2;               // MMA-issuing threads (warp 1 and the last warp), alternate taps
 constexpr int kPIssuer2 = 2 + kPWork;      // warp of the second issuer
-constexpr int kPThreads = 32 * (3 + kPWork);
+constexpr int kPWProd = 3 + kPWork;        // warp of the W-ring producer
+constexpr int kPThreads = 32 * (4 + kPWork);
 constexpr int kPDBufs = 8;                 // TMEM accumulators of 64 columns
 constexpr int kPMaxStages = 8;             // W ring depth cap
 constexpr int kPMinStages = 2;
@@ -260,27 +262,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------- TMA producer: y window, grad windows, W ring
+        // ------------------------------------------------------- TMA producer: y window, grad windows
+        // Per tile the dilation-0 grad window goes first: its buffer is free a third of
+        // the way into the previous tile, while the y window waits for that tile's last MMA.
         if (lane == 0) {
-            prefetch_tmap(&tmW);
             prefetch_tmap(&tmY);
             prefetch_tmap(&tmG0);
             prefetch_tmap(&tmG1);
             prefetch_tmap(&tmG2);
             const CUtensorMap* tmg[3] = {&tmG0, &tmG1, &tmG2};
             const uint32_t ybytes = (uint32_t)P.nch * P.npos * 16;
-            int iw = 0, ny = 0, ng[3] = {0, 0, 0};
-            int st = 0, sph = 0;                       // W ring stage and its phase parity
+            int ny = 0, ng[3] = {0, 0, 0};
             bool ok = true;
             for (int tl = 0; tl < n_my && ok; ++tl) {
                 const int t = blockIdx.x + tl * gridDim.x;
                 const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
                 const int h0 = (ti / P.tiles_w) * kPTH, w0 = (ti % P.tiles_w) * kPTW;
-                if (!mbar_wait(&yw_empty, (tl & 1) ^ 1, P.err, abort_v)) break;
-                mbar_arrive_expect_tx(&yw_full, ybytes);
-                tma_load_4d(sm + P.oyw, &tmY, &yw_full, (w0 - R) * 8, h0 - R, 0, b);
-                ny = tl + 1;
-                for (int dd = 0; dd < 3 && ok; ++dd) {
+                for (int step = 0; step < 4 && ok; ++step) {
+                    if (step == 1) {
+                        if (!mbar_wait(&yw_empty, (tl & 1) ^ 1, P.err, abort_v)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&yw_full, ybytes);
+                        tma_load_4d(sm + P.oyw, &tmY, &yw_full, (w0 - R) * 8, h0 - R, 0, b);
+                        ny = tl + 1;
+                        continue;
+                    }
+                    const int dd = step == 0 ? 0 : step - 1;
                     const int dil = dil_of(P.d, dd);
                     if (!mbar_wait(&gw_empty[dd], (tl & 1) ^ 1, P.err, abort_v)) {
                         ok = false;
@@ -289,27 +298,38 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     mbar_arrive_expect_tx(&gw_full[dd], (uint32_t)P.nch * P.npd[dd] * 16);
                     tma_load_4d(sm + P.ogw[dd], tmg[dd], &gw_full[dd], (w0 - dil) * 8, h0 - dil, dd * P.nch, b);
                     ng[dd] = tl + 1;
-                    for (int k = 0; k < 9; ++k) {
-                        if (!mbar_wait(&wt_empty[st], sph ^ 1, P.err, abort_v)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&wt_full[st], kPWTile);
-                        tma_load_3d(sm + st * kPWTile, &tmW, &wt_full[st], 0, k, dd * C);
-                        ++iw;
-                        if (++st == S) {
-                            st = 0;
-                            sph ^= 1;
-                        }
-                    }
                 }
             }
-            // drain: every copy this CTA started lands before its shared memory is released
+            // drain: every copy this thread started lands before its shared memory is released
             int never = 0;
-            for (int i = iw > S ? iw - S : 0; i < iw; ++i) mbar_wait(&wt_full[i % S], (i / S) & 1, P.err, &never);
             if (ny > 0) mbar_wait(&yw_full, (ny - 1) & 1, P.err, &never);
             for (int dd = 0; dd < 3; ++dd)
                 if (ng[dd] > 0) mbar_wait(&gw_full[dd], (ng[dd] - 1) & 1, P.err, &never);
+        }
+    } else if (warp == kPWProd) {
+        // ------------------------------------------------------- TMA producer: W ring, one tap per stage
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            int iw = 0;
+            int st = 0, sph = 0;                       // W ring stage and its phase parity
+            bool ok = true;
+            for (int tl = 0; tl < n_my && ok; ++tl)
+                for (int u = 0; u < kPTaps; ++u) {
+                    const int dd = u / 9, k = u - dd * 9;
+                    if (!mbar_wait(&wt_empty[st], sph ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&wt_full[st], kPWTile);
+                    tma_load_3d(sm + st * kPWTile, &tmW, &wt_full[st], 0, k, dd * C);
+                    ++iw;
+                    if (++st == S) {
+                        st = 0;
+                        sph ^= 1;
+                    }
+                }
+            int never = 0;
+            for (int i = iw > S ? iw - S : 0; i < iw; ++i) mbar_wait(&wt_full[i % S], (i / S) & 1, P.err, &never);
         }
     } else if (warp == 1 || warp == kPIssuer2) {
         // ------------------------------------------------------- MMA issuers: taps of parity `par`

@@ -14,8 +14,13 @@
  *   - All tensors are dense, contiguous, NCHW (weight [O, C], bias [O]) with
  *     O = 3*C*K*K, and all share the problem's dtype.
  *   - Every pointer is a DEVICE pointer owned by the caller.  The library never
- *     allocates, frees or synchronises; it enqueues kernels on `stream` (NULL =
- *     the legacy default stream) and returns.  Inputs are read-only; outputs are
+ *     allocates device memory, frees or synchronises; it enqueues kernels on
+ *     `stream` (NULL = the legacy default stream) and returns.  The backward
+ *     also runs pieces on two streams of its own per device, forked from and
+ *     joined back into `stream` with events: its work still starts after the
+ *     work before it on `stream` and ends before the work after it.  The first
+ *     backward call on a device creates those streams; make it before any
+ *     stream capture.  Inputs are read-only; outputs are
  *     fully overwritten (no accumulation into them).  Outputs must not alias
  *     inputs.
  *   - Pointers must be aligned to the element size; 16-byte alignment enables
