@@ -388,20 +388,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int t = blockIdx.x + tl * gridDim.x;
             const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
             const int h0 = (ti / P.tiles_w) * kPTH, w0 = (ti % P.tiles_w) * kPTW;
-            // dx = grad (channel block 0) + the gathered sum.  The identity term is loaded
-            // now, as raw bf16 bits that nothing reads before the gather is done, so all 32
-            // loads are in flight at once behind it: the addresses are clamped into the
-            // tensor instead of predicating the loads (validity is applied at the store)
+            // dx = grad (channel block 0) + the gathered sum.  The identity term is only
+            // prefetched into L2 here and loaded after the gather: a load still in flight
+            // would hold up the next mbarrier wait (its acquire orders it after the load),
+            // stalling the workers at the start of every tile.  Addresses are clamped into
+            // the tensor (validity is applied at the store).
             const int h = h0 + r, w = w0 + c;
             const bool inside = h < H && w < W;
             const long long pix = inside ? (long long)h * W + w : 0;
-            unsigned short g0raw[32];
-            {
-                const unsigned short* g0p =
-                    reinterpret_cast<const unsigned short*>(P.g) + (long long)b * 4 * C * HW + pix;
+            const unsigned short* g0p = reinterpret_cast<const unsigned short*>(P.g) + (long long)b * 4 * C * HW + pix;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) g0raw[i] = __ldg(g0p + (long long)min(hc * 32 + i, C - 1) * HW);
-            }
+            for (int i = 0; i < 32; ++i)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(g0p + (long long)min(hc * 32 + i, C - 1) * HW));
             float acc[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
@@ -449,6 +447,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (lane == 0) mbar_arrive(&gw_empty[dd]);
             }
             if (!ok) break;
+            unsigned short g0raw[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) g0raw[i] = __ldg(g0p + (long long)min(hc * 32 + i, C - 1) * HW);
             if (inside) {
                 bf16* dxp = P.dx + (long long)b * C * HW + pix;
 #pragma unroll
