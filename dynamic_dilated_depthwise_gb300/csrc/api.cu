@@ -48,7 +48,7 @@ int num_sms() {
 
 // Two non-blocking streams per device, and the events that fork them from and join
 // them back into a caller's stream.  The events are re-recorded by every call, so a
-// call holds `mu` from the fork to the join.
+// call holds g_side_mu from the fork to the join.
 struct SideStreams {
     cudaStream_t s[2];
     cudaEvent_t fork, join[2];
@@ -212,14 +212,19 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
         const size_t part_bytes = packed ? poff : workspace_bytes;
         // dX on the caller's stream, dY and dW (+ reduce) on the two side streams: the
         // pieces share only inputs, and each one's last partial wave of CTAs leaves SMs
-        // that the others fill
+        // that the others fill.  While kernels are traced the pieces run one after
+        // another on the caller's stream, so each traced interval holds one kernel.
+        const bool fork = !ddpm::trace_enabled();
         std::lock_guard<std::mutex> lock(ddpm::g_side_mu);
         ddpm::SideStreams* ss = nullptr;
         cudaError_t e = ddpm::side_streams(&ss);
         if (e != cudaSuccess) return from_cuda(e);
-        if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return from_cuda(e);
-        for (int i = 0; i < 2; ++i)
-            if ((e = cudaStreamWaitEvent(ss->s[i], ss->fork, 0)) != cudaSuccess) return from_cuda(e);
+        const cudaStream_t s_dy = fork ? ss->s[0] : s, s_dw = fork ? ss->s[1] : s;
+        if (fork) {
+            if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return from_cuda(e);
+            for (int i = 0; i < 2; ++i)
+                if ((e = cudaStreamWaitEvent(ss->s[i], ss->fork, 0)) != cudaSuccess) return from_cuda(e);
+        }
         if (packed)
             e = ddpm::launch_bwd_dx_packed(d, grad_out, y, weight, bias, dx, static_cast<char*>(workspace) + poff, s);
         else if (ddpm::bwd_dx_tc_eligible(d, grad_out, y, weight))
@@ -228,12 +233,12 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
             e = ddpm::launch_bwd_dx_simt(d, grad_out, y, weight, bias, dx, s);
         if (e == cudaSuccess) {
             if (ddpm::bwd_dy_tc_eligible(d, grad_out, x, weight))
-                e = ddpm::launch_bwd_dy_tc(d, grad_out, x, weight, dy, ss->s[0]);
+                e = ddpm::launch_bwd_dy_tc(d, grad_out, x, weight, dy, s_dy);
             else
-                e = ddpm::launch_bwd_dy_simt(d, grad_out, x, weight, dy, ss->s[0]);
+                e = ddpm::launch_bwd_dy_simt(d, grad_out, x, weight, dy, s_dy);
         }
         if (e == cudaSuccess) {
-            const cudaStream_t sw = ss->s[1];
+            const cudaStream_t sw = s_dw;
             if (ddpm::bwd_dw_tc_eligible(d, grad_out, x, y)) {
                 const int S = ddpm::bwd_dw_tc_splits(d, part_bytes);
                 e = ddpm::launch_bwd_dw_tc(d, grad_out, x, y, (float*)workspace, S, sw);
@@ -246,7 +251,7 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
             }
         }
         // join, whatever happened above, so the side streams never run ahead of `stream`
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 2 && fork; ++i) {
             const cudaError_t er = cudaEventRecord(ss->join[i], ss->s[i]);
             const cudaError_t ew = er == cudaSuccess ? cudaStreamWaitEvent(s, ss->join[i], 0) : er;
             if (e == cudaSuccess) e = ew;

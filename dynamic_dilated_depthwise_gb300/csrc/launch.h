@@ -28,6 +28,7 @@ enum KernelId : int {
 
 // Tracing hooks around each launch (cheap no-ops while tracing is off).
 void trace_begin(cudaStream_t s, int kernel_id);
+bool trace_enabled();
 void trace_end(cudaStream_t s);
 
 // ddpm_problem.flags bit that forces the CUDA-core kernels (DDPM_FLAG_CUDA_CORES).

@@ -60,6 +60,8 @@ void trace_begin(cudaStream_t s, int kernel_id) {
     g_open = true;
 }
 
+bool trace_enabled() { return g_enabled.load(std::memory_order_relaxed); }
+
 void trace_end(cudaStream_t s) {
     if (!g_enabled.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lock(g_mu);

@@ -180,7 +180,9 @@ DDPM_API ddpm_status ddpm_get_device_error(ddpm_stream_t stream);
  * Kernel tracing (profiling aid; off by default).
  * While enabled, every kernel an entry point launches is bracketed by a pair of
  * CUDA events recorded on the caller's stream, so per-kernel device time can be
- * read back without a profiler.  Enabling creates CUDA events lazily (no device
+ * read back without a profiler; the backward's pieces, which otherwise overlap
+ * on the library's own streams, then run one after another on that stream so
+ * that each interval holds one kernel alone.  Enabling creates CUDA events lazily (no device
  * memory is allocated); at most 65536 records are kept, later ones are dropped.
  *   ddpm_trace_enable(1|0)      switch tracing on or off (returns DDPM_OK)
  *   ddpm_trace_read(ids, ms, n) wait for the recorded kernels, copy up to n
