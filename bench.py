@@ -333,6 +333,20 @@ def run_ours(args, world, rank, local):
     ms_per_step = total_ms / args.steps
     value = world * p.pixels / (ms_per_step * 1e-3) / 1e6
 
+    # ---- steady state: the same steps back to back, no flush (inputs stay in L2) ----
+    barrier(world)
+    torch.cuda.synchronize()
+    t_s0, t_s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_s0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_s1.record(stream)
+    torch.cuda.synchronize()
+    steady_ms = max_over_ranks(world, t_s0.elapsed_time(t_s1)) / args.steps
+    steady = {"value": round(world * p.pixels / (steady_ms * 1e-3) / 1e6, 3), "unit": UNIT,
+              "ms_per_step": round(steady_ms, 5),
+              "l2": "not flushed: steps back to back, inputs resident in L2 after the first"}
+
     # ---- traced loop: per-kernel device time on the launching stream ----
     binding.ddpm_trace_read()
     binding.ddpm_trace_enable(True)
@@ -454,7 +468,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
             "gpu_launches": int(round(launches_per_step * args.steps)),
-            "e2e": e2e, "wall_s_timed_loop": round(t_wall, 4)}
+            "e2e": e2e, "steady_state": steady, "wall_s_timed_loop": round(t_wall, 4)}
     line["clocks"] = clk.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(p, dtype, step=step_kind)
@@ -498,6 +512,34 @@ def run_reference(args, world, rank):
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def measure_fp32_peaks() -> dict:
+    """FP32 FFMA throughput (the library's FMA-chain kernel on every SM) and cuBLAS TF32
+    throughput (torch.matmul of two 8192 x 8192 FP32 matrices with TF32 allowed), each
+    the best of a few timed runs: the denominators the CUDA-core and a TF32 path would
+    be measured against."""
+    import torch
+    from dynamic_dilated_depthwise_gb300 import binding
+    ffma = binding.ddpm_measure_ffma_tflops()
+    n = 8192
+    torch.backends.cuda.matmul.allow_tf32 = True
+    a = torch.randn(n, n, device="cuda")
+    b = torch.randn(n, n, device="cuda")
+    for _ in range(3):
+        torch.matmul(a, b)
+    best = 1e30
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.matmul(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    tf32 = 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    return {"fp32_ffma_tflops": round(ffma, 2), "tf32_tflops": round(tf32, 1),
+            "method": "FFMA: 8 independent fmaf chains per thread, 8 blocks of 256 per SM, best of 3; "
+                      "TF32: torch.matmul 8192^3 FP32 with allow_tf32, best of 10"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[1])
     ap.add_argument("--gpus", type=int, default=1)
@@ -509,9 +551,14 @@ def main():
     ap.add_argument("--step", choices=("train", "forward", "filter"), default="train",
                     help="what one timed step runs (default: the fwd+bwd training step)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (faster runs)")
+    ap.add_argument("--peaks", action="store_true",
+                    help="measure the FP32 FFMA and TF32 tensor peaks of this GPU and print them (one JSON line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.peaks:
+        print(json.dumps(measure_fp32_peaks()), flush=True)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, world, rank)

@@ -30,7 +30,7 @@ STATUS = {
 }
 EXPORTED = ("ddpm_forward", "ddpm_filter_pregenerated", "ddpm_backward_workspace_size", "ddpm_backward",
             "ddpm_get_device_error", "ddpm_status_string", "ddpm_version", "ddpm_trace_enable",
-            "ddpm_trace_read", "ddpm_kernel_name", "ddpm_backward_noalloc")
+            "ddpm_trace_read", "ddpm_kernel_name", "ddpm_backward_noalloc", "ddpm_measure_ffma_tflops")
 
 
 class ddpm_problem(ctypes.Structure):
@@ -74,6 +74,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ddpm_trace_enable.restype = ctypes.c_int
         lib.ddpm_trace_read.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float), ctypes.c_int]
         lib.ddpm_trace_read.restype = ctypes.c_int
+        lib.ddpm_measure_ffma_tflops.argtypes = [ctypes.POINTER(ctypes.c_double)]
+        lib.ddpm_measure_ffma_tflops.restype = ctypes.c_int
         lib.ddpm_kernel_name.argtypes = [ctypes.c_int]
         lib.ddpm_kernel_name.restype = ctypes.c_char_p
         for f in ("ddpm_forward", "ddpm_filter_pregenerated", "ddpm_backward_workspace_size", "ddpm_backward",
@@ -173,6 +175,13 @@ def ddpm_trace_read(max_records: int = 65536):
     if n < 0:
         raise DDPMError(5, "ddpm_trace_read")
     return [(ddpm_kernel_name(ids[i]), float(ms[i])) for i in range(n)]
+
+
+def ddpm_measure_ffma_tflops() -> float:
+    """Measured FP32 FMA throughput of the current device, TFLOP/s (synchronises)."""
+    v = ctypes.c_double(0.0)
+    _check(load().ddpm_measure_ffma_tflops(ctypes.byref(v)), "ddpm_measure_ffma_tflops")
+    return float(v.value)
 
 
 def ddpm_kernel_name(kernel_id: int) -> str:

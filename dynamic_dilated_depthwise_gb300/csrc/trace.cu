@@ -70,9 +70,58 @@ void trace_end(cudaStream_t s) {
     g_open = false;
 }
 
+// Eight independent FMA chains per thread: with every SM full, the FP32 pipes
+// issue one FMA per lane per cycle once each chain's latency is covered.  a and b
+// come from the host, so nothing folds; the sum is written only if it takes a
+// value it cannot reach, which keeps the chains live.
+__device__ float g_ffma_sink;
+
+__global__ void __launch_bounds__(256) ffma_chain_kernel(int iters, float a, float b) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 1e-3f * (float)threadIdx.x + (float)i;
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = fmaf(v[i], a, b);
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += v[i];
+    if (s == -1.0f) g_ffma_sink = s;
+}
+
 }  // namespace ddpm
 
 extern "C" {
+
+ddpm_status ddpm_measure_ffma_tflops(double* tflops) {
+    using namespace ddpm;
+    if (tflops == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
+    const int blocks = num_sms() * 8, threads = 256, iters = 4096;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) return DDPM_ERR_CUDA;
+    ddpm_status st = DDPM_OK;
+    float best = 1e30f;
+    for (int rep = 0; rep < 4 && st == DDPM_OK; ++rep) {
+        cudaEventRecord(e0, nullptr);
+        ffma_chain_kernel<<<blocks, threads>>>(iters, 0.999999f, 1e-7f);
+        cudaEventRecord(e1, nullptr);
+        float ms = 0.0f;
+        if (cudaGetLastError() != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess)
+            st = DDPM_ERR_CUDA;
+        else if (rep > 0 && ms < best)
+            best = ms;   // the first launch is a warm-up
+    }
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (st != DDPM_OK) return st;
+    const double flops = 2.0 * 32.0 * (double)iters * (double)blocks * (double)threads;
+    *tflops = flops / ((double)best * 1e-3) / 1e12;
+    return DDPM_OK;
+}
 
 ddpm_status ddpm_trace_enable(int enable) {
     ddpm::g_enabled.store(enable != 0);

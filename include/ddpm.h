@@ -192,6 +192,15 @@ DDPM_API ddpm_status ddpm_get_device_error(ddpm_stream_t stream);
  *   ddpm_kernel_name(id)        name of a kernel id (never NULL)
  */
 DDPM_API ddpm_status ddpm_trace_enable(int enable);
+/*
+ * ddpm_measure_ffma_tflops -- measured FP32 FMA throughput of the current device
+ * (profiling aid for the CUDA-core kernels' roofline).  Launches a kernel of
+ * eight independent FMA chains per thread on every SM on the legacy default
+ * stream, synchronises, and writes the best of three timed launches, in
+ * TFLOP/s (2 flops per FMA), to *tflops.  Returns DDPM_OK, or
+ * DDPM_ERR_INVALID_ARGUMENT for a NULL pointer, or DDPM_ERR_CUDA.
+ */
+DDPM_API ddpm_status ddpm_measure_ffma_tflops(double* tflops);
 DDPM_API int ddpm_trace_read(int* kernel_ids, float* milliseconds, int max_records);
 DDPM_API const char* ddpm_kernel_name(int kernel_id);
 
