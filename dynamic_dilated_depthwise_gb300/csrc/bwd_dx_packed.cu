@@ -182,6 +182,129 @@ __global__ void __launch_bounds__(kPackThreads, 2)
     }
 }
 
+// ----------------------------------------------------------------------------- pack (TMA)
+// Persistent variant for H*W a multiple of 2048, on half of the SMs: the pack is
+// bound by HBM, not by SMs, and the SMs it leaves free run the dY and dW kernels
+// that start beside it.  Unit = 2048 pixels of one chunk (eight channel rows of
+// 4 KiB): eight untiled bulk copies bring it into a 4-stage ring; 256 threads each
+// transpose one 8-pixel run into a 128B-swizzled staging block (conflict-free
+// writes), and one 2-D tensor store with the same swizzle writes the unit's
+// contiguous 32 KiB of output (runs are rows of 64 bf16 in the packed buffer).
+constexpr int kPkWorkers = 256;
+constexpr int kPkThreads = kPkWorkers + 32;   // + a producer warp
+constexpr int kPkPx = 8 * kPkWorkers;         // 2048 pixels per unit
+constexpr int kPkStages = 4;
+constexpr int kPkRow = kPkPx * 2;             // 4 KiB: one channel row of a unit
+constexpr int kPkIn = 8 * kPkRow;             // 32 KiB
+constexpr int kPkOut = kPkWorkers * 128;      // 32 KiB
+constexpr int kPkSmem = kPkStages * kPkIn + 2 * kPkOut + 1024;
+
+struct PackParams {
+    const bf16* y;
+    const bf16* g;
+    int C, nch;
+    long long HW;
+    int units_per_chunk;   // HW / 2048
+    int n_ychunks;         // B * nch: y chunks come first, then the 3 * B * nch grad chunks
+    int n_units;
+    unsigned int* err;
+};
+
+__global__ void __launch_bounds__(kPkThreads, 1)
+    pack_chunks_tma_kernel(const __grid_constant__ CUtensorMap tmOut, const PackParams P) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ uint64_t full[kPkStages], empty[kPkStages];
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n_my = blockIdx.x < P.n_units ? (P.n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < kPkStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kPkWorkers / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == kPkWorkers / 32) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < n_my; ++i) {
+                const int s = i % kPkStages, ph = (i / kPkStages) & 1;
+                if (!mbar_wait(&empty[s], ph ^ 1, P.err, abort_v)) break;
+                const int u = blockIdx.x + i * gridDim.x;
+                const int chunk = u / P.units_per_chunk;
+                const long long px0 = (long long)(u % P.units_per_chunk) * kPkPx;
+                const bf16* src;
+                if (chunk < P.n_ychunks) {
+                    const int b = chunk / P.nch, cb = chunk % P.nch;
+                    src = P.y + ((long long)b * P.C + cb * 8) * P.HW + px0;
+                } else {
+                    const int j = chunk - P.n_ychunks;   // (b * 3 + grp) * nch + cb
+                    const int cb = j % P.nch, bg = j / P.nch, b = bg / 3, grp = bg % 3;
+                    src = P.g + ((long long)b * 4 * P.C + P.C + (long long)grp * P.C + cb * 8) * P.HW + px0;
+                }
+                uint8_t* dst = sm + s * kPkIn;
+                mbar_arrive_expect_tx(&full[s], kPkIn);
+                for (int e = 0; e < 8; ++e) bulk_load(dst + e * kPkRow, src + e * P.HW, kPkRow, &full[s]);
+                issued = i + 1;
+            }
+            // drain: every copy this thread started lands before its shared memory is released
+            int never = 0;
+            for (int i = issued > kPkStages ? issued - kPkStages : 0; i < issued; ++i)
+                mbar_wait(&full[i % kPkStages], (i / kPkStages) & 1, P.err, &never);
+        }
+    } else {
+        // ------------------------------------------------------- workers: run tid of each unit
+        uint8_t* const out0 = sm + kPkStages * kPkIn;
+        bool ok = true;
+        for (int i = 0; i < n_my; ++i) {
+            const int s = i % kPkStages, ph = (i / kPkStages) & 1, ob = i & 1;
+            if (ok) ok = mbar_wait(&full[s], ph, P.err, abort_v);
+            // staging block ob was last read by the store of unit i - 2
+            if (tid == 0) bulk_wait_read<1>();
+            asm volatile("bar.sync 1, %0;" ::"n"(kPkWorkers) : "memory");
+            if (ok) {
+                const uint8_t* in = sm + s * kPkIn + tid * 16;
+                uint4 q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q[e] = *reinterpret_cast<const uint4*>(in + e * kPkRow);
+                uint8_t* out = out0 + ob * kPkOut + tid * 128;
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    const uint32_t sel = (p & 1) ? 0x7632u : 0x5410u;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        const uint4 a = q[2 * f], b = q[2 * f + 1];
+                        const uint32_t aw = (p >> 1) == 0 ? a.x : (p >> 1) == 1 ? a.y : (p >> 1) == 2 ? a.z : a.w;
+                        const uint32_t bw = (p >> 1) == 0 ? b.x : (p >> 1) == 1 ? b.y : (p >> 1) == 2 ? b.z : b.w;
+                        w[f] = __byte_perm(aw, bw, sel);
+                    }
+                    *reinterpret_cast<uint4*>(out + ((p ^ (tid & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 1, %0;" ::"n"(kPkWorkers) : "memory");
+            if (tid == 0 && ok) {
+                const int u = blockIdx.x + i * gridDim.x;
+                const int chunk = u / P.units_per_chunk, blk = u % P.units_per_chunk;
+                const int row0 = (int)((long long)chunk * (P.HW / 8) + (long long)blk * kPkWorkers);
+                tma_store_2d(&tmOut, out0 + ob * kPkOut, 0, row0);
+                bulk_commit();
+            }
+        }
+        // every store has written global memory before the kernel ends
+        if (tid == 0) bulk_wait<0>();
+    }
+}
+
 // ----------------------------------------------------------------------------- dX
 __global__ void __launch_bounds__(kPThreads, 1)
     bwd_dx_tc_packed_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
@@ -508,7 +631,42 @@ cudaError_t launch_bwd_dx_packed(const Dims& d, const void* g, const void* y, co
     const int nch = d.C / 8;
 
     // 1. channel-chunked copies of y and of the three dilation blocks of grad
-    {
+    const long long n_rows = 4LL * d.B * nch * (d.HW / 8);   // 16-byte pixel rows of the copies
+    if (d.HW % kPkPx == 0 && n_rows <= INT_MAX && (uintptr_t)y % 16 == 0 && (uintptr_t)g % 16 == 0) {
+        static int attr_pk[64] = {};
+        {
+            const cudaError_t e = set_max_dynamic_smem((const void*)pack_chunks_tma_kernel, kPkSmem, attr_pk);
+            if (e != cudaSuccess) return e;
+        }
+        CUtensorMap tmOut;
+        const cuuint64_t dims[2] = {64, (cuuint64_t)n_rows};
+        const cuuint64_t str[1] = {128};
+        const cuuint32_t box[2] = {64, (cuuint32_t)kPkWorkers};
+        const cuuint32_t es[2] = {1, 1};
+        if (encode_fn()(&tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, packed, dims, str, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        PackParams Q;
+        Q.y = static_cast<const bf16*>(y);
+        Q.g = static_cast<const bf16*>(g);
+        Q.C = d.C;
+        Q.nch = nch;
+        Q.HW = d.HW;
+        Q.units_per_chunk = (int)(d.HW / kPkPx);
+        Q.n_ychunks = d.B * nch;
+        Q.n_units = 4 * d.B * nch * Q.units_per_chunk;
+        Q.err = device_error_word();
+        if (Q.err == nullptr) return cudaErrorUnknown;
+        int grid = num_sms() / 2;
+        if (grid < 1) grid = 1;
+        if (grid > Q.n_units) grid = Q.n_units;
+        trace_begin(s, kKPackChunks);
+        pack_chunks_tma_kernel<<<grid, kPkThreads, kPkSmem, s>>>(tmOut, Q);
+        trace_end(s);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    } else {
         const long long runs = d.HW / 8;
         const long long n_y = (long long)d.B * nch * runs;
         const long long n_all = n_y * 4;
