@@ -465,6 +465,9 @@ def run_ours(args, world, rank, local):
                                 "forward": "ddpm_forward (fused generator + filter)",
                                 "filter": "ddpm_filter_pregenerated (taps given)"}[step_kind],
                        "l2": "flushed: 256 MiB write before each step, outside the timed events",
+                       "flags": "DDPM_FLAG_TF32_BACKWARD" + (" (FP32: dW/dbias partials on TF32 tensor cores; dX, dY "
+                                                             "and the forward in IEEE FP32)" if dtype == "float32"
+                                                             else " (ignored for bf16)"),
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
             "gpu_launches": int(round(launches_per_step * args.steps)),

@@ -243,6 +243,10 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
                 const int S = ddpm::bwd_dw_tc_splits(d, part_bytes);
                 e = ddpm::launch_bwd_dw_tc(d, grad_out, x, y, (float*)workspace, S, sw);
                 if (e == cudaSuccess) e = ddpm::launch_bwd_reduce(d, (const float*)workspace, S, dweight, dbias, sw);
+            } else if (ddpm::bwd_dw_tf32_eligible(d, grad_out, x, y)) {
+                const int S = ddpm::bwd_dw_tf32_splits(d, part_bytes);
+                e = ddpm::launch_bwd_dw_tf32(d, grad_out, x, y, (float*)workspace, S, sw);
+                if (e == cudaSuccess) e = ddpm::launch_bwd_reduce(d, (const float*)workspace, S, dweight, dbias, sw);
             } else {
                 e = ddpm::launch_bwd_dw_partial_simt(d, grad_out, x, y, workspace, sw);
                 if (e == cudaSuccess)

@@ -23,7 +23,8 @@ enum KernelId : int {
     kKBwdDwTc = 9,
     kKPackChunks = 10,
     kKBwdDxTcPacked = 11,
-    kKNumKernels = 12
+    kKBwdDwTf32 = 12,
+    kKNumKernels = 13
 };
 
 // Tracing hooks around each launch (cheap no-ops while tracing is off).
@@ -31,8 +32,10 @@ void trace_begin(cudaStream_t s, int kernel_id);
 bool trace_enabled();
 void trace_end(cudaStream_t s);
 
-// ddpm_problem.flags bit that forces the CUDA-core kernels (DDPM_FLAG_CUDA_CORES).
+// ddpm_problem.flags bits: force the CUDA-core kernels (DDPM_FLAG_CUDA_CORES); allow
+// TF32 tensor-core contractions in an FP32 backward (DDPM_FLAG_TF32_BACKWARD).
 constexpr unsigned kFlagCudaCores = 0x2u;
+constexpr unsigned kFlagTf32Backward = 0x1u;
 
 // Multiprocessor count of the current device (cached per device).
 int num_sms();
@@ -90,6 +93,10 @@ bool bwd_dw_tc_eligible(const Dims& d, const void* g, const void* x, const void*
 int bwd_dw_tc_splits(const Dims& d, size_t workspace_bytes);
 cudaError_t launch_bwd_dw_tc(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S,
                              cudaStream_t s);
+bool bwd_dw_tf32_eligible(const Dims& d, const void* g, const void* x, const void* y);
+int bwd_dw_tf32_splits(const Dims& d, size_t workspace_bytes);
+cudaError_t launch_bwd_dw_tf32(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S,
+                               cudaStream_t s);
 
 // dX on tcgen05 tensor cores: one shifted GEMM per tap (halo radius <= 6).
 bool bwd_dx_tc_eligible(const Dims& d, const void* g, const void* y, const void* w);

@@ -67,7 +67,10 @@ typedef enum { DDPM_FLOAT32 = 0, DDPM_BFLOAT16 = 1 } ddpm_dtype;
 /* Flags for ddpm_problem.flags.
  * DDPM_FLAG_TF32_BACKWARD: FP32 problems may run the backward contractions on
  *   TF32 tensor cores (the page allows TF32 for FP32 backward reductions and
- *   recompute, never for the forward).  Ignored for BF16. */
+ *   recompute, never for the forward).  With it the dW/dbias partial sums run
+ *   on tensor cores (TF32 operands, FP32 accumulation) for K = 3, C <= 64, W a
+ *   multiple of 4, dilations <= 6 and 16-byte aligned tensors; dX and dY stay
+ *   IEEE FP32.  Ignored for BF16 and under DDPM_FLAG_CUDA_CORES. */
 #define DDPM_FLAG_TF32_BACKWARD 0x1u
 /* DDPM_FLAG_CUDA_CORES: run the CUDA-core (FFMA) kernels even where a
  *   tensor-core kernel exists for the problem (BF16 forward / backward). */

@@ -277,6 +277,51 @@ def test_tc_backward_integer_bit_exact(p):
     np.testing.assert_array_equal(to64(db), rdb)
 
 
+# --------------------------------------------- FP32 backward, TF32 dW / dbias --
+
+# Shapes the TF32 dW kernel takes (FP32, K = 3, C <= 64, W % 4 == 0, dilations <= 6):
+# ragged 64-pixel row tiles, partial blocks of 14 channels, other dilations, several images.
+TF32_SHAPES = [
+    Problem(1, 16, 9, 132, 3),               # three tiles per row, the last 4 pixels wide
+    Problem(2, 24, 10, 24, 3),               # C = 24: a partial channel block; one short tile per row
+    Problem(1, 64, 12, 64, 3),               # C = 64 as in the main workloads
+    Problem(1, 12, 7, 40, 3, (2, 2, 4)),     # other dilations
+    Problem(3, 8, 5, 68, 3, (1, 6, 2)),      # halo radius 6, several images
+]
+
+
+@pytest.mark.parametrize("p", TF32_SHAPES, ids=_id)
+def test_tf32_backward_matches_oracle(p):
+    h = make_inputs(p, 850, "float32")
+    d = _dev(h)
+    flags = binding.DDPM_FLAG_TF32_BACKWARD
+    names = _traced_kernels(lambda: run_backward(d, p, flags=flags))
+    assert "bwd_dw_tf32" in names and "bwd_dw_partial_simt" not in names, names
+    got = run_backward(d, p, flags=flags)
+    ieee = run_backward(d, p)
+    torch.cuda.synchronize()
+    ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=False)
+    for name, a, want in zip(("dx", "dy", "dW", "dbias"), got, ref):
+        assert_grad_close(a, want, "float32", name)
+    # the flag changes only the dW / dbias contraction
+    assert torch.equal(got[0], ieee[0]) and torch.equal(got[1], ieee[1])
+
+
+@pytest.mark.parametrize("p", TF32_SHAPES, ids=_id)
+def test_tf32_backward_integer_bit_exact(p):
+    """Integer inputs: every product and partial sum is exact in TF32 / FP32."""
+    h = make_integer_inputs(p, 13, "float32")
+    d = _dev(h)
+    dx, dy, dw, db = run_backward(d, p, flags=binding.DDPM_FLAG_TF32_BACKWARD)
+    torch.cuda.synchronize()
+    rdx, rdy, rdw, rdb = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations,
+                                         bf16=False)
+    np.testing.assert_array_equal(to64(dw), rdw)
+    np.testing.assert_array_equal(to64(db), rdb)
+    np.testing.assert_array_equal(to64(dx), rdx)
+    np.testing.assert_array_equal(to64(dy), rdy)
+
+
 # ----------------------------------------------------- integer, bit-exact --
 
 @pytest.mark.parametrize("dtype", DTYPES)
