@@ -71,9 +71,11 @@ def _load():
             lib.ddpmo_filter_points.argtypes = [sp, d, d, ctypes.c_int64, i64p, d]
             lib.ddpmo_backward.argtypes = [sp, d, d, d, d, d, d, d, d, d]
             lib.ddpmo_backward_points.argtypes = [sp, d, d, d, d, d, ctypes.c_int, ctypes.c_int64, i64p, d]
+            lib.ddpmo_filter_backward.argtypes = [sp, d, d, d, d, d]
             lib.ddpmo_num_threads.argtypes = []
             for f in ("ddpmo_generate_taps", "ddpmo_forward", "ddpmo_filter", "ddpmo_forward_points",
-                      "ddpmo_filter_points", "ddpmo_backward", "ddpmo_backward_points", "ddpmo_num_threads"):
+                      "ddpmo_filter_points", "ddpmo_backward", "ddpmo_backward_points", "ddpmo_filter_backward",
+                      "ddpmo_num_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -200,6 +202,20 @@ def backward(g, x, y, Wg, bias, K, dilations=(1, 3, 5), bf16=False):
     _check(_load().ddpmo_backward(ctypes.byref(s), _ptr(g), _ptr(x), _ptr(y), _ptr(Wg), _ptr(bias),
                                   _ptr(dx), _ptr(dy), _ptr(dW), _ptr(db)), "backward")
     return dx, dy, dW, db
+
+
+def filter_backward(g, x, T, K, dilations=(1, 3, 5)):
+    """Gradients of L = <g, filter_pregenerated(x, T)> (README section "CUDA 动态过滤":
+    the backward of the filter with given taps forms dX and dK without a patch
+    matrix): returns (dx [B,C,H,W], dT [B,O,H,W])."""
+    g, x, T = _f64(g), _f64(x), _f64(T)
+    B, C, H, W = x.shape
+    s = _shape(B, C, H, W, K, dilations, False)
+    dx = np.empty((B, C, H, W))
+    dT = np.empty_like(T)
+    _check(_load().ddpmo_filter_backward(ctypes.byref(s), _ptr(g), _ptr(x), _ptr(T), _ptr(dx), _ptr(dT)),
+           "filter_backward")
+    return dx, dT
 
 
 _WHICH = {"dx": 0, "dy": 1, "dW": 2, "dbias": 3}

@@ -13,7 +13,8 @@
  *     plus a 1x1 generator whose output holds the dynamic kernels,
  *     N * 3 * C * K^2 * H * W values.
  *   - "CUDA 动态过滤" (dynamic filtering): one pass covers dilations (1,3,5),
- *     accumulates and writes [x, d1, d3, d5] directly.
+ *     accumulates and writes [x, d1, d3, d5] directly; its backward forms dX
+ *     and dK (the taps' gradient) without a patch matrix.
  *   - "CUDA 融合生成器推理" (fused generator inference):
  *     y tile -> dot(weight, y) -> dynamic taps -> consume with shifted x.
  *   - "CUDA Flash 式融合训练" (flash-style fused training): dX gathers each
@@ -412,6 +413,56 @@ int ddpmo_backward(const ddpmo_shape* s, const double* g, const double* x, const
     }
     free(yt);
     return err;
+}
+
+/* ------------------------------------------------- filter-only backward -- */
+
+/* Backward of the filter with given taps (README section "CUDA 动态过滤":
+ * with the dynamic kernels already generated, the backward forms dX and dK
+ * directly, without a patch matrix).  For L = <g, out>, out = filter(x, T):
+ *   dT[b,o,h,w] = g[b,(1+di)C+c,h,w] * x~[b,c,h+(ky-r)d, w+(kx-r)d]      (dK)
+ *   dx[b,c,h,w] = g[b,c,h,w]
+ *                + sum_{di,ky,kx} T[b,o,h',w'] * g[b,(1+di)C+c,h',w'],
+ *                  (h',w') = (h-(ky-r)d, w-(kx-r)d) inside the image.
+ * The taps are used as given (no rounding in either mode). */
+static double dx_point_given(const ddpmo_shape* s, const double* g, const double* T, int b, int c, int h, int w)
+{
+    const int K = s->K, r = K / 2, C = s->C;
+    const int64_t HW = (int64_t)s->H * s->W;
+    double acc = g[((int64_t)b * 4 * C + c) * HW + (int64_t)h * s->W + w];
+    for (int di = 0; di < 3; ++di) {
+        const int d = s->dil[di];
+        for (int ky = 0; ky < K; ++ky)
+            for (int kx = 0; kx < K; ++kx) {
+                const int hs = h - (ky - r) * d, ws = w - (kx - r) * d;
+                if (hs < 0 || hs >= s->H || ws < 0 || ws >= s->W) continue;
+                const int64_t o = (int64_t)(di * C + c) * K * K + ky * K + kx;
+                const double gv = g[((int64_t)b * 4 * C + (1 + di) * C + c) * HW + (int64_t)hs * s->W + ws];
+                acc += T[((int64_t)b * n_taps(s) + o) * HW + (int64_t)hs * s->W + ws] * gv;
+            }
+    }
+    return acc;
+}
+
+int ddpmo_filter_backward(const ddpmo_shape* s, const double* g, const double* x, const double* T, double* dx,
+                          double* dT)
+{
+    if (!shape_ok(s)) return 1;
+    const int B = s->B, C = s->C, H = s->H, W = s->W;
+    const int64_t O = n_taps(s), HW = (int64_t)H * W;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int c = 0; c < C; ++c)
+            for (int h = 0; h < H; ++h)
+                for (int w = 0; w < W; ++w)
+                    dx[((int64_t)b * C + c) * HW + (int64_t)h * W + w] = dx_point_given(s, g, T, b, c, h, w);
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int64_t o = 0; o < O; ++o)
+            for (int h = 0; h < H; ++h)
+                for (int w = 0; w < W; ++w)
+                    dT[((int64_t)b * O + o) * HW + (int64_t)h * W + w] = dK_at(s, g, x, b, (int)o, h, w);
+    return 0;
 }
 
 /* Sampled gradients.  which: 0 = dx [B,C,H,W], 1 = dy [B,C,H,W],

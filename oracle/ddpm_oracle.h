@@ -38,6 +38,8 @@ int ddpmo_backward(const ddpmo_shape* s, const double* g, const double* x, const
 int ddpmo_backward_points(const ddpmo_shape* s, const double* g, const double* x, const double* y,
                           const double* Wg, const double* bias, int which, int64_t n,
                           const int64_t* idx, double* vals);
+int ddpmo_filter_backward(const ddpmo_shape* s, const double* g, const double* x, const double* T, double* dx,
+                          double* dT);
 int ddpmo_num_threads(void);
 
 #ifdef __cplusplus

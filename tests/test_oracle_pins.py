@@ -15,7 +15,10 @@ Each test ties the oracle to an independent fact about the method in the
 * adjoint identities <g,out> = <dx,x> and <g,out_d> = <dW,W> + <dbias,bias>
   = <dy,y> + <dbias,bias>;
 * the bf16 rounding against torch's float32 -> bfloat16 conversion;
-* a hand-worked example (tests/golden/handworked_k3_3x3.json).
+* a hand-worked example (tests/golden/handworked_k3_3x3.json);
+* the filter-only backward (taps given) against torch autograd through the
+  Unfold reference, the adjoint identities <g,out> = <dx,x> = <dT,T> + <g_0,x>,
+  and sum_{b,p} dT = the fused backward's dbias.
 """
 import json
 import os
@@ -343,3 +346,68 @@ def test_pins_catch_planted_mistakes():
     out_nb = oracle.forward(t["x"], t["y"], t["weight"], None, p.K, p.dilations)
     Tg = generator_reference(t["y"], t["weight"], t["bias"])
     assert np.max(np.abs(out_nb - unfold_reference(t["x"], Tg, p.K, p.dilations))) > 1e-3
+
+
+# ------------------------------------------------- filter-only backward --
+# README section "CUDA 动态过滤": with the taps given, the backward forms dX and
+# dK (the taps' gradient) without a patch matrix.  Pinned to torch autograd
+# through the Unfold reference, and to the adjoint identities of a bilinear map.
+
+def _unfold_filter_autograd(x, T, g, K, dils):
+    """(dx, dT) of L = <g, filter(x, T)> by torch autograd through F.unfold."""
+    xt = torch.tensor(x, dtype=torch.float64, requires_grad=True)
+    Tt = torch.tensor(T, dtype=torch.float64, requires_grad=True)
+    B, C, H, W = x.shape
+    K2 = K * K
+    outs = [xt]
+    for di, d in enumerate(dils):
+        U = F.unfold(xt, K, dilation=d, padding=d * (K // 2))
+        Td = Tt[:, di * C * K2:(di + 1) * C * K2].reshape(B, C * K2, H * W)
+        outs.append((U * Td).reshape(B, C, K2, H * W).sum(2).reshape(B, C, H, W))
+    L = (torch.cat(outs, 1) * torch.as_tensor(g, dtype=torch.float64)).sum()
+    L.backward()
+    return _np(xt.grad), _np(Tt.grad)
+
+
+@pytest.mark.parametrize("p", SMALL, ids=_id)
+def test_filter_backward_matches_unfold_autograd(p):
+    t = _inputs(p)
+    dx, dT = oracle.filter_backward(t["grad_out"], t["x"], t["taps"], p.K, p.dilations)
+    rdx, rdT = _unfold_filter_autograd(t["x"], t["taps"], t["grad_out"], p.K, p.dilations)
+    np.testing.assert_allclose(dx, rdx, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dT, rdT, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("p", SMALL, ids=_id)
+def test_filter_backward_adjoint_identities(p):
+    """The filter is linear in x and in T: <g,out> = <dx,x> = <dT,T> + <g_0,x>."""
+    t = _inputs(p, seed=21)
+    x, T, g = t["x"], t["taps"], t["grad_out"]
+    L = float((g * oracle.filter_pregenerated(x, T, p.K, p.dilations)).sum())
+    dx, dT = oracle.filter_backward(g, x, T, p.K, p.dilations)
+    assert abs(float((dx * x).sum()) - L) <= 1e-12 * max(1.0, abs(L))
+    assert abs(float((dT * T).sum() + (g[:, :p.C] * x).sum()) - L) <= 1e-12 * max(1.0, abs(L))
+
+
+def test_filter_backward_dT_sums_to_fused_dbias():
+    """dT is the fused path's dK: summed over batch and pixels it is dbias."""
+    p = Problem(2, 3, 6, 5, 3)
+    t = _inputs(p, seed=5)
+    _, dT = oracle.filter_backward(t["grad_out"], t["x"], t["taps"], p.K, p.dilations)
+    _, _, _, db = oracle.backward(t["grad_out"], t["x"], t["y"], t["weight"], t["bias"], p.K, p.dilations)
+    np.testing.assert_allclose(dT.sum(axis=(0, 2, 3)), db, rtol=1e-12, atol=1e-12)
+
+
+def test_filter_backward_pins_catch_planted_mistakes():
+    """A gather at +offset (flipped taps) or a dropped identity term must fail the autograd pin."""
+    p = Problem(1, 2, 7, 6, 3)
+    t = _inputs(p)
+    x, T, g = t["x"], t["taps"], t["grad_out"]
+    rdx, _ = _unfold_filter_autograd(x, T, g, p.K, p.dilations)
+    Tflip = np.ascontiguousarray(T.reshape(p.B, 3 * p.C, p.K, p.K, p.H, p.W)[:, :, ::-1, ::-1].reshape(T.shape))
+    wrong, _ = oracle.filter_backward(g, x, Tflip, p.K, p.dilations)
+    assert np.max(np.abs(wrong - rdx)) > 1e-3
+    g_no_id = g.copy()
+    g_no_id[:, :p.C] = 0.0
+    wrong, _ = oracle.filter_backward(g_no_id, x, T, p.K, p.dilations)
+    assert np.max(np.abs(wrong - rdx)) > 1e-3
