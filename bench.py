@@ -35,7 +35,8 @@ METRIC = "DDPM fused fwd+bwd Mpixel/s (C=64,K=3,256² bf16, 1 GB300); % of roofl
 # metric names of the other steps (--step forward / filter), same unit
 STEP_METRIC = {"train": METRIC,
                "forward": "DDPM fused generator+filter forward Mpixel/s (1 GB300); % of roofline",
-               "filter": "DDPM filter with pregenerated taps Mpixel/s (1 GB300); % of HBM roofline"}
+               "filter": "DDPM filter with pregenerated taps Mpixel/s (1 GB300); % of HBM roofline",
+               "filter_train": "DDPM filter with pregenerated taps fwd+bwd Mpixel/s (1 GB300); % of HBM roofline"}
 UNIT = "Mpixel/s"
 DEFAULT_WORKLOAD = "b1_c64_256x256_k3"
 FLUSH_BYTES = 256 << 20
@@ -76,6 +77,10 @@ def kernel_work(name: str, p, es: int, splits: int):
     gemm = 2.0 * O * C * P
     if name == "filter_pregenerated_simt":
         return "hbm", P * (O + C + 4 * C) * es, "bytes"
+    if name == "filter_bwd_dx":            # reads the taps and grad (4C), writes dx
+        return "hbm", P * (O + 4 * C + C) * es, "bytes"
+    if name == "filter_bwd_dtaps":         # reads grad blocks 1..3 and x, writes dtaps
+        return "hbm", P * (3 * C + C + O) * es, "bytes"
     if name in ("forward_simt", "bwd_dx_simt", "bwd_dy_simt"):
         return "alu", gemm, "flops"
     if name == "bwd_dw_partial_simt":
@@ -96,7 +101,8 @@ def step_roofline_us(p, es: int, peaks, step: str = "train") -> dict:
               generator recompute for dX, dY, dW); x, y, weight, bias and grad
               read once, out / dx / dy / dW / dbias written once;
       forward: one contraction; x, y, weight, bias read, out written;
-      filter:  no contraction; x and the taps read, out written."""
+      filter:  no contraction; x and the taps read, out written;
+      filter_train: no contraction; x, the taps and grad read, out, dx and dtaps written."""
     P = p.B * p.H * p.W
     w_bytes = (p.O * p.C + p.O) * es
     if step == "train":
@@ -105,6 +111,9 @@ def step_roofline_us(p, es: int, peaks, step: str = "train") -> dict:
     elif step == "forward":
         flops = 2.0 * p.O * p.C * P
         nbytes = P * (2 * p.C + 4 * p.C) * es + w_bytes
+    elif step == "filter_train":
+        flops = 0.0
+        nbytes = P * (p.C + p.O + 4 * p.C + 4 * p.C + p.C + p.O) * es
     else:
         flops = 0.0
         nbytes = P * (p.C + p.O + 4 * p.C) * es
@@ -236,15 +245,18 @@ def cpu_baseline(p, dtype: str, target_s: float = 10.0, step: str = "train") -> 
     import oracle
     from dynamic_dilated_depthwise_gb300.inputs import Problem, SEEDS, make_inputs
     one = Problem(1, p.C, p.H, p.W, p.K, p.dilations)
-    h = make_inputs(one, SEEDS.get(p.name, 1000), dtype, grad=step == "train", taps=step == "filter")
+    h = make_inputs(one, SEEDS.get(p.name, 1000), dtype, grad=step in ("train", "filter_train"),
+                    taps=step in ("filter", "filter_train"))
     h = {k: v.double().numpy() for k, v in h.items()}
     bf = dtype == "bfloat16"
     oracle.build()
     reps, t_total = 0, 0.0
     while reps < 5 and (reps == 0 or t_total < target_s):
         t0 = time.perf_counter()
-        if step == "filter":
+        if step in ("filter", "filter_train"):
             oracle.filter_pregenerated(h["x"], h["taps"], p.K, p.dilations)
+            if step == "filter_train":
+                oracle.filter_backward(h["grad_out"], h["x"], h["taps"], p.K, p.dilations)
         else:
             oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
         if step == "train":
@@ -252,7 +264,8 @@ def cpu_baseline(p, dtype: str, target_s: float = 10.0, step: str = "train") -> 
         t_total += time.perf_counter() - t0
         reps += 1
     px = reps * one.pixels
-    what = {"train": "fwd+bwd", "forward": "forward", "filter": "filter-only"}[step]
+    what = {"train": "fwd+bwd", "forward": "forward", "filter": "filter-only",
+            "filter_train": "filter-only fwd+bwd"}[step]
     return {"value": px / t_total / 1e6, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{reps} x {what} of one {p.H}x{p.W} image (C={p.C}, K={p.K}, {dtype}-valued inputs, FP64 math)",
             "seconds": round(t_total, 3)}
@@ -271,9 +284,12 @@ def run_ours(args, world, rank, local):
     dtype = args.dtype
     es = 2 if dtype == "bfloat16" else 4
     step_kind = args.step
-    h = make_inputs(p, SEEDS[p.name] + rank, dtype, grad=step_kind == "train", taps=step_kind == "filter")
+    h = make_inputs(p, SEEDS[p.name] + rank, dtype, grad=step_kind in ("train", "filter_train"),
+                    taps=step_kind in ("filter", "filter_train"))
     if step_kind == "filter":
         h = {k: h[k] for k in ("x", "taps")}
+    elif step_kind == "filter_train":
+        h = {k: h[k] for k in ("x", "taps", "grad_out")}
     elif step_kind == "forward":
         h = {k: h[k] for k in ("x", "y", "weight", "bias")}
     d = {k: v.to(dev) for k, v in h.items()}
@@ -284,6 +300,7 @@ def run_ours(args, world, rank, local):
     dx, dy = torch.empty_like(d["x"]), torch.empty_like(d["x"])
     dw = torch.empty((p.O, p.C), dtype=d["x"].dtype, device=dev)
     db = torch.empty((p.O,), dtype=d["x"].dtype, device=dev)
+    dtaps = torch.empty_like(d["taps"]) if step_kind == "filter_train" else None
     ws_bytes = binding.ddpm_backward_workspace_size(prob) if step_kind == "train" else 0
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -295,8 +312,11 @@ def run_ours(args, world, rank, local):
     pref = ctypes.byref(prob)
 
     def step():
-        if step_kind == "filter":
+        if step_kind in ("filter", "filter_train"):
             s1, s2 = lib.ddpm_filter_pregenerated(pref, ptr["x"], ptr["taps"], out.data_ptr(), sh), 0
+            if step_kind == "filter_train":
+                s2 = lib.ddpm_filter_pregenerated_backward(pref, ptr["grad_out"], ptr["x"], ptr["taps"],
+                                                           dx.data_ptr(), dtaps.data_ptr(), sh)
         else:
             s1 = lib.ddpm_forward(pref, ptr["x"], ptr["y"], ptr["weight"], ptr["bias"], out.data_ptr(), sh)
             s2 = 0
@@ -394,7 +414,9 @@ def run_ours(args, world, rank, local):
     e2e_steps = min(args.steps, 20)
     hin = {k: v.pin_memory() for k, v in h.items()}
     out_like = {"out": out, "dx": dx, "dy": dy, "dw": dw, "db": db}
-    if step_kind != "train":
+    if step_kind == "filter_train":
+        out_like = {"out": out, "dx": dx, "dtaps": dtaps}
+    elif step_kind != "train":
         out_like = {"out": out}
     hout = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out_like.items()} for _ in range(2)]
     din = [d] + [{k: torch.empty_like(v) for k, v in d.items()}]
@@ -407,8 +429,11 @@ def run_ours(args, world, rank, local):
     def step_on(stream_c, pi, po):
         sc = stream_c.cuda_stream
         pp = {k: v.data_ptr() for k, v in pi.items()}
-        if step_kind == "filter":
+        if step_kind in ("filter", "filter_train"):
             s1, s2 = lib.ddpm_filter_pregenerated(pref, pp["x"], pp["taps"], po["out"].data_ptr(), sc), 0
+            if step_kind == "filter_train":
+                s2 = lib.ddpm_filter_pregenerated_backward(pref, pp["grad_out"], pp["x"], pp["taps"],
+                                                           po["dx"].data_ptr(), po["dtaps"].data_ptr(), sc)
         else:
             s1 = lib.ddpm_forward(pref, pp["x"], pp["y"], pp["weight"], pp["bias"], po["out"].data_ptr(), sc)
             s2 = 0
@@ -463,7 +488,9 @@ def run_ours(args, world, rank, local):
                        "dilations": list(p.dilations), "dtype": dtype,
                        "step": {"train": "ddpm_forward + ddpm_backward (dx, dy, dweight, dbias)",
                                 "forward": "ddpm_forward (fused generator + filter)",
-                                "filter": "ddpm_filter_pregenerated (taps given)"}[step_kind],
+                                "filter": "ddpm_filter_pregenerated (taps given)",
+                                "filter_train": "ddpm_filter_pregenerated + ddpm_filter_pregenerated_backward "
+                                                "(dx, dtaps; taps given)"}[step_kind],
                        "l2": "flushed: 256 MiB write before each step, outside the timed events",
                        "flags": "DDPM_FLAG_TF32_BACKWARD" + (" (FP32: dW/dbias partials on TF32 tensor cores; dX, dY "
                                                              "and the forward in IEEE FP32)" if dtype == "float32"
@@ -551,7 +578,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--dtype", choices=("bfloat16", "float32"), default="bfloat16")
-    ap.add_argument("--step", choices=("train", "forward", "filter"), default="train",
+    ap.add_argument("--step", choices=("train", "forward", "filter", "filter_train"), default="train",
                     help="what one timed step runs (default: the fwd+bwd training step)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (faster runs)")
     ap.add_argument("--peaks", action="store_true",

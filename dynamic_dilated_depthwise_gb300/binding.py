@@ -30,7 +30,8 @@ STATUS = {
 }
 EXPORTED = ("ddpm_forward", "ddpm_filter_pregenerated", "ddpm_backward_workspace_size", "ddpm_backward",
             "ddpm_get_device_error", "ddpm_status_string", "ddpm_version", "ddpm_trace_enable",
-            "ddpm_trace_read", "ddpm_kernel_name", "ddpm_backward_noalloc", "ddpm_measure_ffma_tflops")
+            "ddpm_trace_read", "ddpm_kernel_name", "ddpm_backward_noalloc", "ddpm_measure_ffma_tflops",
+            "ddpm_filter_pregenerated_backward")
 
 
 class ddpm_problem(ctypes.Structure):
@@ -62,6 +63,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         vp, sz = ctypes.c_void_p, ctypes.c_size_t
         lib.ddpm_forward.argtypes = [P, vp, vp, vp, vp, vp, vp]
         lib.ddpm_filter_pregenerated.argtypes = [P, vp, vp, vp, vp]
+        lib.ddpm_filter_pregenerated_backward.argtypes = [P, vp, vp, vp, vp, vp, vp]
         lib.ddpm_backward_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
         lib.ddpm_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.ddpm_get_device_error.argtypes = [vp]
@@ -131,6 +133,12 @@ def ddpm_forward(problem, x, y, weight, bias, out, stream=None) -> None:
 def ddpm_filter_pregenerated(problem, x, taps, out, stream=None) -> None:
     _check(load().ddpm_filter_pregenerated(ctypes.byref(problem), _p(x), _p(taps), _p(out), _stream(stream)),
            "ddpm_filter_pregenerated")
+
+
+def ddpm_filter_pregenerated_backward(problem, grad_out, x, taps, dx, dtaps, stream=None) -> None:
+    _check(load().ddpm_filter_pregenerated_backward(ctypes.byref(problem), _p(grad_out), _p(x), _p(taps), _p(dx),
+                                                    _p(dtaps), _stream(stream)),
+           "ddpm_filter_pregenerated_backward")
 
 
 def ddpm_backward_workspace_size(problem) -> int:
@@ -228,6 +236,16 @@ def filter_pregenerated(x, taps, K, dilations=(1, 3, 5), out=None, stream=None):
         out = torch.empty((B, 4 * C, H, W), dtype=x.dtype, device=x.device)
     ddpm_filter_pregenerated(_problem_of(x, K, dilations), x, taps, out, stream)
     return out
+
+
+def filter_pregenerated_backward(grad_out, x, taps, K, dilations=(1, 3, 5), with_dtaps=True, stream=None):
+    """Gradients (dx, dtaps) of <grad_out, filter_pregenerated(x, taps)>; dtaps is
+    None when with_dtaps is False (dx alone)."""
+    _same(x, grad_out, taps)
+    dx = torch.empty_like(x)
+    dtaps = torch.empty_like(taps) if with_dtaps else None
+    ddpm_filter_pregenerated_backward(_problem_of(x, K, dilations), grad_out, x, taps, dx, dtaps, stream)
+    return dx, dtaps
 
 
 def backward_workspace_size(x, K, dilations=(1, 3, 5), flags=0) -> int:

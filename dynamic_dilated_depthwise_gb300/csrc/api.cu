@@ -175,6 +175,23 @@ ddpm_status ddpm_filter_pregenerated(const ddpm_problem* problem, const void* x,
     }
 }
 
+ddpm_status ddpm_filter_pregenerated_backward(const ddpm_problem* problem, const void* grad_out, const void* x,
+                                              const void* taps, void* dx, void* dtaps, ddpm_stream_t stream) {
+    Dims d;
+    DDPM_TRY(validate(problem, &d));
+    const size_t es = elem_size(d.dtype);
+    DDPM_TRY(check_ptr(grad_out, es, false));
+    DDPM_TRY(check_ptr(x, es, false));
+    DDPM_TRY(check_ptr(taps, es, false));
+    DDPM_TRY(check_ptr(dx, es, false));
+    DDPM_TRY(check_ptr(dtaps, es, true));
+    try {
+        return from_cuda(ddpm::launch_filter_backward_simt(d, grad_out, x, taps, dx, dtaps, (cudaStream_t)stream));
+    } catch (...) {
+        return DDPM_ERR_CUDA;
+    }
+}
+
 ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* bytes) {
     Dims d;
     DDPM_TRY(validate(problem, &d));

@@ -24,7 +24,9 @@ enum KernelId : int {
     kKPackChunks = 10,
     kKBwdDxTcPacked = 11,
     kKBwdDwTf32 = 12,
-    kKNumKernels = 13
+    kKFilterBwdDx = 13,
+    kKFilterBwdDtaps = 14,
+    kKNumKernels = 15
 };
 
 // Tracing hooks around each launch (cheap no-ops while tracing is off).
@@ -60,6 +62,9 @@ unsigned int* device_error_word();
 // Dynamic filter with pregenerated taps (README section "CUDA 动态过滤").
 cudaError_t launch_filter_simt(const Dims& d, const void* x, const void* taps, void* out,
                                cudaStream_t s);
+// Backward of the filter with given taps (dx and, when dtaps is non-null, the taps' gradient).
+cudaError_t launch_filter_backward_simt(const Dims& d, const void* g, const void* x, const void* taps, void* dx,
+                                        void* dtaps, cudaStream_t s);
 
 // Fused generator + filter on CUDA cores (IEEE FP32 FMA; also any dtype/shape).
 cudaError_t launch_forward_simt(const Dims& d, const void* x, const void* y, const void* w,

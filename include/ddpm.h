@@ -111,6 +111,23 @@ DDPM_API ddpm_status ddpm_filter_pregenerated(const ddpm_problem* problem, const
                                      void* out, ddpm_stream_t stream);
 
 /*
+ * ddpm_filter_pregenerated_backward -- gradients of L = <grad_out, out> for
+ * ddpm_filter_pregenerated.  Source: README section "CUDA 动态过滤" (with the
+ * taps given, the backward forms dX and dK directly, without a patch matrix):
+ *   dx[b,c,q]    = grad[b,c,q] + sum_{di,ky,kx} taps[b,o,q-off] * grad[b,(1+di)C+c,q-off]
+ *                  (terms whose q-off lies outside the image are dropped);
+ *   dtaps[b,o,p] = grad[b,(1+di)C+c,p] * x[b,c,p+off]  (0 where p+off lies outside),
+ *   o = (di*C + c)*K*K + ky*K + kx, off = ((ky-K/2)*d, (kx-K/2)*d), d = dilations[di].
+ * Products and sums in FP32, each output rounded once to the problem's dtype.
+ *   grad_out  [B, 4C, H, W];  x [B, C, H, W];  taps [B, O, H, W]
+ *   dx        [B, C, H, W]    output
+ *   dtaps     [B, O, H, W]    output, or NULL to compute dx alone
+ */
+DDPM_API ddpm_status ddpm_filter_pregenerated_backward(const ddpm_problem* problem, const void* grad_out,
+                                                      const void* x, const void* taps, void* dx, void* dtaps,
+                                                      ddpm_stream_t stream);
+
+/*
  * ddpm_backward_workspace_size -- bytes of device workspace ddpm_backward needs.
  * Host only; enqueues nothing.  The workspace holds at most 16 FP32 partial
  * sums of [O, C+1] (dW and dbias), per README section "CUDA Flash 式融合训练"

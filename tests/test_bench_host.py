@@ -52,6 +52,9 @@ def test_forward_and_filter_rooflines(bench):
     assert t["flops"] == 0
     assert t["bytes"] == P * (C + O + 4 * C) * 4      # x and the taps in, 4C channels out
     assert t["roofline_us"] == pytest.approx(t["bytes"] / 5000e9 * 1e6)
+    # filter fwd+bwd: x, taps and grad (4C) in; out (4C), dx (C) and dtaps (O) out
+    ft = bench.step_roofline_us(p, 2, PEAKS, "filter_train")
+    assert ft["flops"] == 0 and ft["bytes"] == P * (10 * C + 2 * O) * 2
 
 
 def test_kernel_work(bench):
@@ -63,6 +66,8 @@ def test_kernel_work(bench):
     assert bench.kernel_work("filter_pregenerated_simt", p, 2, 1) == ("hbm", P * (O + 5 * C) * 2, "bytes")
     assert bench.kernel_work("bwd_dw_reduce", p, 2, 10) == ("hbm", 10 * O * (C + 1) * 4 + O * (C + 1) * 2,
                                                             "bytes")
+    assert bench.kernel_work("filter_bwd_dx", p, 2, 1) == ("hbm", P * (O + 5 * C) * 2, "bytes")
+    assert bench.kernel_work("filter_bwd_dtaps", p, 4, 1) == ("hbm", P * (4 * C + O) * 4, "bytes")
     assert bench.kernel_work("no_such_kernel", p, 2, 1)[0] == "unknown"
 
 
@@ -83,5 +88,5 @@ def test_peaks_from_measured_file(bench):
 
 
 def test_step_metrics_share_the_unit(bench):
-    assert set(bench.STEP_METRIC) == {"train", "forward", "filter"}
+    assert set(bench.STEP_METRIC) == {"train", "forward", "filter", "filter_train"}
     assert bench.STEP_METRIC["train"] == bench.METRIC

@@ -70,6 +70,7 @@ def test_invalid_problems_rejected_on_host(lib, kw):
     assert lib.ddpm_backward_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 1
     assert lib.ddpm_forward(ctypes.byref(p), 16, 16, 16, 16, 16, None) == 1
     assert lib.ddpm_filter_pregenerated(ctypes.byref(p), 16, 16, 16, None) == 1
+    assert lib.ddpm_filter_pregenerated_backward(ctypes.byref(p), 16, 16, 16, 16, 16, None) == 1
 
 
 def test_unsupported_sizes(lib):
@@ -88,6 +89,11 @@ def test_null_and_misaligned_pointers(lib):
     assert lib.ddpm_forward(ctypes.byref(pb), 16, 16, 16, 17, 16, None) == 3           # bias odd address
     assert lib.ddpm_filter_pregenerated(ctypes.byref(p), 16, None, 16, None) == 1
     assert lib.ddpm_forward(None, 16, 16, 16, 16, 16, None) == 1
+    # filter backward: a NULL grad, x, taps or dx is rejected; dtaps may be NULL
+    assert lib.ddpm_filter_pregenerated_backward(ctypes.byref(p), 16, 16, 16, None, 16, None) == 1
+    assert lib.ddpm_filter_pregenerated_backward(ctypes.byref(p), None, 16, 16, 16, None, None) == 1
+    assert lib.ddpm_filter_pregenerated_backward(ctypes.byref(p), 16, 16, 18, 16, 16, None) == 3   # taps at 2 bytes
+    assert lib.ddpm_filter_pregenerated_backward(ctypes.byref(p), 16, 16, 16, 16, 22, None) == 3   # dtaps at 2 bytes
     # backward: NULL grad, misaligned workspace, too-small workspace
     assert lib.ddpm_backward(ctypes.byref(p), None, 16, 16, 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 1
     assert lib.ddpm_backward(ctypes.byref(p), 16, 16, 16, 16, 16, 16, 16, 16, 16, 24, 1 << 30, None) == 3

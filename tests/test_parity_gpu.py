@@ -277,6 +277,54 @@ def test_tc_backward_integer_bit_exact(p):
     np.testing.assert_array_equal(to64(db), rdb)
 
 
+# ----------------------------------------- filter-only backward (taps given) --
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", SMALL, ids=_id)
+def test_filter_backward_matches_oracle(p, dtype):
+    h = make_inputs(p, 900, dtype, grad=True, taps=True)
+    d = _dev(h)
+    names = _traced_kernels(lambda: binding.filter_pregenerated_backward(d["grad_out"], d["x"], d["taps"], p.K,
+                                                                         p.dilations))
+    assert names == ["filter_bwd_dx", "filter_bwd_dtaps"], names
+    dx, dT = binding.filter_pregenerated_backward(d["grad_out"], d["x"], d["taps"], p.K, p.dilations)
+    dx_only, none = binding.filter_pregenerated_backward(d["grad_out"], d["x"], d["taps"], p.K, p.dilations,
+                                                         with_dtaps=False)
+    torch.cuda.synchronize()
+    rdx, rdT = oracle.filter_backward(h["grad_out"], h["x"], h["taps"], p.K, p.dilations)
+    assert_grad_close(dx, rdx, dtype, "dx")
+    assert_grad_close(dT, rdT, dtype, "dtaps")
+    assert none is None and torch.equal(dx_only, dx)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", [Problem(2, 24, 15, 17, 3), Problem(1, 8, 12, 11, 5), Problem(1, 12, 20, 19, 3, (2, 2, 4)),
+                               Problem(2, 5, 6, 7, 1), Problem(1, 6, 13, 9, 7)], ids=_id)
+def test_filter_backward_integer_bit_exact(p, dtype):
+    """Integer inputs: every product and sum is a small integer, exact in bf16 and fp32."""
+    h = make_integer_inputs(p, 17, dtype, taps=True)
+    d = _dev(h)
+    dx, dT = binding.filter_pregenerated_backward(d["grad_out"], d["x"], d["taps"], p.K, p.dilations)
+    torch.cuda.synchronize()
+    rdx, rdT = oracle.filter_backward(h["grad_out"], h["x"], h["taps"], p.K, p.dilations)
+    np.testing.assert_array_equal(to64(dx), rdx)
+    np.testing.assert_array_equal(to64(dT), rdT)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_filter_backward_full_size(dtype):
+    """The 128x128, C=64, K=3 filter workload, compared over whole tensors."""
+    p = WORKLOADS["b1_c64_128x128_k3"]
+    h = make_inputs(p, SEEDS.get(p.name, 1000), dtype, grad=True, taps=True)
+    d = _dev(h)
+    dx, dT = binding.filter_pregenerated_backward(d["grad_out"], d["x"], d["taps"], p.K, p.dilations)
+    torch.cuda.synchronize()
+    rdx, rdT = oracle.filter_backward(h["grad_out"], h["x"], h["taps"], p.K, p.dilations)
+    assert_grad_close(dx, rdx, dtype, "dx")
+    assert_grad_close(dT, rdT, dtype, "dtaps")
+    assert binding.ddpm_get_device_error() == 0
+
+
 # --------------------------------------------- FP32 backward, TF32 dW / dbias --
 
 # Shapes the TF32 dW kernel takes (FP32, K = 3, C <= 64, W % 4 == 0, dilations <= 6):
