@@ -8,11 +8,13 @@
 //
 // One thread owns one pixel; a block owns 128 pixels of one image and a group
 // of CG output channels.  For each (channel c, dilation di) the block stages
-// the K*K generator rows of that (di, c) in shared memory as Ws[j][k] (k
-// padded to a multiple of 4 so a thread reads four taps' weights with one
-// 16-byte broadcast load), each thread forms its K*K taps from y at its pixel
-// (y streamed from L1: it is re-read for every (c, di) of the group), rounds
-// them for bf16, and applies them to the zero-padded shifted x.
+// the K*K generator rows of that (di, c) in shared memory, each thread forms its
+// K*K taps from y at its pixel, rounds them for bf16, and applies them to the
+// zero-padded shifted x.  With K <= 3 and C a multiple of 4 (up to 64) y stays
+// in registers and the rows are staged as they lie in memory, Ws[k][j]: a
+// 16-byte broadcast load gives four input channels of one tap, with no padded
+// taps.  Otherwise Ws[j][k], k padded to a multiple of 4 (four taps' weights of
+// one input channel per 16-byte load) and y streamed from L1.
 #include "launch.h"
 
 namespace ddpm {
@@ -22,7 +24,7 @@ constexpr int kThreads = 128;
 constexpr int kCG = 8;  // output channels per block
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kThreads) forward_simt_kernel(Dims d, const T* __restrict__ x,
+__global__ void __launch_bounds__(kThreads, K <= 3 ? 4 : 0) forward_simt_kernel(Dims d, const T* __restrict__ x,
                                                                 const T* __restrict__ y,
                                                                 const T* __restrict__ wgt,
                                                                 const T* __restrict__ bias,
@@ -44,7 +46,7 @@ __global__ void __launch_bounds__(kThreads) forward_simt_kernel(Dims d, const T*
     // C <= 64 and K <= 3 (one load per input channel instead of one per (channel,
     // dilation, input)); larger kernels need the registers for their taps
     constexpr int kYR = K <= 3 ? 64 : 1;
-    const bool y_in_regs = K <= 3 && C <= kYR;
+    const bool y_in_regs = K <= 3 && C <= kYR && C % 4 == 0;
     float yr[kYR];
 #pragma unroll
     for (int j = 0; j < kYR; ++j) yr[j] = (y_in_regs && active && j < C) ? ldg_f(yb + (long long)j * d.HW + p) : 0.0f;
@@ -52,12 +54,12 @@ __global__ void __launch_bounds__(kThreads) forward_simt_kernel(Dims d, const T*
     // the current ones are applied, so the staging latency overlaps
     constexpr int ITW = K <= 3 ? (kYR * KP + kThreads - 1) / kThreads : 1;
     float wn[ITW];
+    // Ws[k][j] = W[o0 + k][j]: K2 contiguous rows of C, one coalesced copy
     auto load_rows = [&](long long o0) {
 #pragma unroll
         for (int it = 0; it < ITW; ++it) {
             const int i = threadIdx.x + it * kThreads;
-            const int j = i / KP, k = i % KP;
-            wn[it] = (i < C * KP && k < K2) ? to_f(wgt[(o0 + k) * C + j]) : 0.0f;
+            wn[it] = i < K2 * C ? to_f(wgt[o0 * C + i]) : 0.0f;
         }
     };
     if (y_in_regs) load_rows((long long)c0 * K2);
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) forward_simt_kernel(Dims d, const T*
 #pragma unroll
                 for (int it = 0; it < ITW; ++it) {
                     const int i = threadIdx.x + it * kThreads;
-                    if (i < C * KP) Ws[i] = wn[it];
+                    if (i < K2 * C) Ws[i] = wn[it];
                 }
             } else {
                 for (int i = threadIdx.x; i < C * KP; i += kThreads) {
@@ -94,18 +96,17 @@ __global__ void __launch_bounds__(kThreads) forward_simt_kernel(Dims d, const T*
 #pragma unroll
             for (int k = 0; k < KP; ++k) t[k] = (bias != nullptr && k < K2) ? to_f(bias[o0 + k]) : 0.0f;
             if (y_in_regs) {
+                // input channels in fours, every tap per four: t[k] still sums j = 0, 1, 2, ... in order
 #pragma unroll
-                for (int j = 0; j < kYR; ++j) {
-                    if (j >= C) break;
-                    const float yv = yr[j];
-                    const float4* wr = reinterpret_cast<const float4*>(Ws + j * KP);
+                for (int q = 0; q < kYR / 4; ++q) {
+                    if (4 * q >= C) break;
 #pragma unroll
-                    for (int q = 0; q < KP / 4; ++q) {
-                        const float4 w4 = wr[q];
-                        t[4 * q + 0] = __fmaf_rn(w4.x, yv, t[4 * q + 0]);
-                        t[4 * q + 1] = __fmaf_rn(w4.y, yv, t[4 * q + 1]);
-                        t[4 * q + 2] = __fmaf_rn(w4.z, yv, t[4 * q + 2]);
-                        t[4 * q + 3] = __fmaf_rn(w4.w, yv, t[4 * q + 3]);
+                    for (int k = 0; k < K2; ++k) {
+                        const float4 w4 = *reinterpret_cast<const float4*>(Ws + k * C + 4 * q);
+                        t[k] = __fmaf_rn(w4.x, yr[4 * q + 0], t[k]);
+                        t[k] = __fmaf_rn(w4.y, yr[4 * q + 1], t[k]);
+                        t[k] = __fmaf_rn(w4.z, yr[4 * q + 2], t[k]);
+                        t[k] = __fmaf_rn(w4.w, yr[4 * q + 3], t[k]);
                     }
                 }
             } else {
