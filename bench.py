@@ -180,31 +180,41 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def kernel_source_digest() -> str:
-    """Digest of the CUDA sources (to invalidate stored ncu traffic figures)."""
+# The source file of each kernel whose ncu traffic is stored (all of them also
+# depend on every shared header, .cuh / .h).
+KERNEL_SOURCE = {"forward_tc": "forward_tc.cu", "pack_chunks": "bwd_dx_packed.cu",
+                 "bwd_dx_tc_packed": "bwd_dx_packed.cu", "bwd_dy_tc": "bwd_dy_tc.cu", "bwd_dw_tc": "bwd_dw_tc.cu",
+                 "bwd_dw_reduce": "backward_simt.cu"}
+
+
+def kernel_source_digest(kernel: str) -> str:
+    """Digest of a kernel's source file and of every shared header (to invalidate
+    its stored ncu traffic figure once any of them changes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dynamic_dilated_depthwise_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    names = sorted(n for n in os.listdir(csrc) if n.endswith((".cuh", ".h")))
+    names.append(KERNEL_SOURCE.get(kernel, ""))
+    for name in names:
+        path = os.path.join(csrc, name)
+        if not os.path.isfile(path):
+            return "missing"
+        with open(path, "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def stored_traffic(kernel: str, workload: str):
     """dram bytes per launch from the committed ncu summary, or None if the
-    kernels changed since the counters were taken."""
+    kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    if t.get("source_digest") != kernel_source_digest():
-        return None
     k = t.get("kernels", {}).get(kernel)
-    if not k or k.get("workload") != workload:
+    if not k or k.get("workload") != workload or k.get("source_digest") != kernel_source_digest(kernel):
         return None
     return k.get("dram_bytes_per_launch")
 

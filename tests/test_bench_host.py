@@ -90,3 +90,15 @@ def test_peaks_from_measured_file(bench):
 def test_step_metrics_share_the_unit(bench):
     assert set(bench.STEP_METRIC) == {"train", "forward", "filter", "filter_train"}
     assert bench.STEP_METRIC["train"] == bench.METRIC
+
+
+def test_stored_traffic_is_keyed_per_kernel(bench):
+    # kernels sharing a source file share a digest; different files give different digests
+    assert bench.kernel_source_digest("pack_chunks") == bench.kernel_source_digest("bwd_dx_tc_packed")
+    assert bench.kernel_source_digest("bwd_dy_tc") != bench.kernel_source_digest("bwd_dw_tc")
+    assert bench.kernel_source_digest("no_such_kernel") == "missing"
+    t = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    for name, k in t["kernels"].items():
+        want = k["dram_bytes_per_launch"] if k["source_digest"] == bench.kernel_source_digest(name) else None
+        assert bench.stored_traffic(name, k["workload"]) == want
+        assert bench.stored_traffic(name, "another_workload") is None
