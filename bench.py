@@ -522,16 +522,25 @@ def run_reference(args, world, rank):
     import oracle
     from dynamic_dilated_depthwise_gb300.inputs import Problem, SEEDS, WORKLOADS, make_inputs
     p = WORKLOADS[args.workload]
+    kind = args.step
     rows = 16
     sample = Problem(1, p.C, rows, p.W, p.K, p.dilations)
-    h = make_inputs(sample, SEEDS[p.name], args.dtype)
+    h = make_inputs(sample, SEEDS[p.name], args.dtype, grad=kind in ("train", "filter_train"),
+                    taps=kind in ("filter", "filter_train"))
     h = {k: v.double().numpy() for k, v in h.items()}
     bf = args.dtype == "bfloat16"
     oracle.build()
 
     def step():
+        # the same work as our arm's step, on the band
+        if kind in ("filter", "filter_train"):
+            oracle.filter_pregenerated(h["x"], h["taps"], p.K, p.dilations)
+            if kind == "filter_train":
+                oracle.filter_backward(h["grad_out"], h["x"], h["taps"], p.K, p.dilations)
+            return
         oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
-        oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
+        if kind == "train":
+            oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=bf)
 
     for _ in range(args.warmup):
         step()
@@ -541,8 +550,10 @@ def run_reference(args, world, rank):
     t = time.perf_counter() - t0
     ms = t / args.steps * 1e3
     value = sample.pixels / (ms * 1e-3) / 1e6
-    desc = f"fwd+bwd of a {rows}x{p.W} band (B=1, C={p.C}, K={p.K}) per step, FP64, {args.dtype}-valued inputs"
-    return {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "impl": "reference", "n_gpus": world,
+    what = {"train": "fwd+bwd", "forward": "forward", "filter": "filter-only",
+            "filter_train": "filter-only fwd+bwd"}[kind]
+    desc = f"{what} of a {rows}x{p.W} band (B=1, C={p.C}, K={p.K}) per step, FP64, {args.dtype}-valued inputs"
+    return {"metric": STEP_METRIC[kind], "value": round(value, 4), "unit": UNIT, "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": p.name, "B": p.B, "C": p.C, "H": p.H, "W": p.W, "K": p.K,

@@ -83,3 +83,17 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "Mpixel/s"
     assert d["value"] > 0 and d["e2e"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+
+
+@pytest.mark.parametrize("step", ["forward", "filter", "filter_train"])
+def test_reference_arm_times_each_step_kind(step):
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--step", step, "--steps", "1", "--warmup", "3",
+           "--workload", "b2_c24_15x17_k3", "--dtype", "float32"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        env.pop(k, None)
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    bench = _load_bench()
+    assert d["impl"] == "reference" and d["metric"] == bench.STEP_METRIC[step] and d["value"] > 0
