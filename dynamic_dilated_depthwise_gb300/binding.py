@@ -286,3 +286,21 @@ class DDPMCoreFunction(torch.autograd.Function):
         dx, dy, dw, db = backward(grad_out.contiguous(), x, y, weight, bias, ctx.K, ctx.dilations,
                                   with_dbias=bias is not None)
         return dx, dy, dw, db, None, None
+
+
+class DDPMFilterFunction(torch.autograd.Function):
+    """autograd wrapper of the filter with given taps: forward and backward (dx, dtaps)
+    both run in the CUDA library; dtaps is computed only when taps needs a gradient."""
+
+    @staticmethod
+    def forward(ctx, x, taps, K, dilations):
+        ctx.save_for_backward(x, taps)
+        ctx.K, ctx.dilations = K, tuple(dilations)
+        return filter_pregenerated(x, taps, K, dilations)
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        x, taps = ctx.saved_tensors
+        dx, dtaps = filter_pregenerated_backward(grad_out.contiguous(), x, taps, ctx.K, ctx.dilations,
+                                                 with_dtaps=ctx.needs_input_grad[1])
+        return dx, dtaps, None, None

@@ -448,6 +448,18 @@ def test_autograd_wrapper():
         assert_grad_close(d[t].grad, want, "float32", name)
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_filter_autograd_wrapper(dtype):
+    p = Problem(1, 8, 10, 16, 3)
+    h = make_inputs(p, 610, dtype, grad=True, taps=True)
+    d = {k: v.cuda().requires_grad_(k in ("x", "taps")) for k, v in h.items()}
+    out = binding.DDPMFilterFunction.apply(d["x"], d["taps"], p.K, p.dilations)
+    out.backward(d["grad_out"])
+    rdx, rdT = oracle.filter_backward(h["grad_out"], h["x"], h["taps"], p.K, p.dilations)
+    assert_grad_close(d["x"].grad, rdx, dtype, "dx")
+    assert_grad_close(d["taps"].grad, rdT, dtype, "dtaps")
+
+
 def test_device_error_word_is_clear():
     p = Problem(1, 16, 8, 8, 3)
     run_forward(_dev(make_inputs(p, 1, "bfloat16", grad=False)), p)
