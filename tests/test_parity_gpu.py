@@ -297,6 +297,38 @@ def test_filter_backward_matches_oracle(p, dtype):
     assert none is None and torch.equal(dx_only, dx)
 
 
+# Shapes the tiled filter-backward kernels take (W a multiple of 8): every K, ragged
+# tile rows, several tiles per row, several images, other dilations.
+FILTER_TILED_BWD = [
+    Problem(1, 3, 9, 24, 3), Problem(2, 2, 19, 16, 5), Problem(1, 2, 7, 40, 7), Problem(2, 3, 5, 8, 1),
+    Problem(1, 2, 21, 136, 3, (2, 2, 4)), Problem(1, 2, 10, 72, 3, (1, 6, 2)), Problem(2, 2, 17, 64, 5, (3, 1, 2)),
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", FILTER_TILED_BWD, ids=_id)
+def test_filter_backward_tiled_matches_oracle(p, dtype):
+    h = make_inputs(p, 905, dtype, grad=True, taps=True)
+    d = _dev(h)
+    dx, dT = binding.filter_pregenerated_backward(d["grad_out"], d["x"], d["taps"], p.K, p.dilations)
+    torch.cuda.synchronize()
+    rdx, rdT = oracle.filter_backward(h["grad_out"], h["x"], h["taps"], p.K, p.dilations)
+    assert_grad_close(dx, rdx, dtype, "dx")
+    assert_grad_close(dT, rdT, dtype, "dtaps")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("p", FILTER_TILED_BWD, ids=_id)
+def test_filter_backward_tiled_integer_bit_exact(p, dtype):
+    h = make_integer_inputs(p, 19, dtype, taps=True)
+    d = _dev(h)
+    dx, dT = binding.filter_pregenerated_backward(d["grad_out"], d["x"], d["taps"], p.K, p.dilations)
+    torch.cuda.synchronize()
+    rdx, rdT = oracle.filter_backward(h["grad_out"], h["x"], h["taps"], p.K, p.dilations)
+    np.testing.assert_array_equal(to64(dx), rdx)
+    np.testing.assert_array_equal(to64(dT), rdT)
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("p", [Problem(2, 24, 15, 17, 3), Problem(1, 8, 12, 11, 5), Problem(1, 12, 20, 19, 3, (2, 2, 4)),
                                Problem(2, 5, 6, 7, 1), Problem(1, 6, 13, 9, 7)], ids=_id)
