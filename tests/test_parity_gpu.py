@@ -233,7 +233,9 @@ def test_tc_forward_repeated_calls_identical():
 
 # ------------------------------------------------ tensor-core backward path --
 
-TC_BWD_SHAPES = list(TC_SHAPES)
+# + H*W a multiple of 2048 with several images and fewer than eight channel chunks:
+# the persistent TMA pack
+TC_BWD_SHAPES = list(TC_SHAPES) + [Problem(2, 24, 32, 64, 3)]
 
 
 @pytest.mark.parametrize("p", TC_BWD_SHAPES, ids=_id)
