@@ -44,6 +44,9 @@ FLUSH_BYTES = 256 << 20
 # Nominal GB300 unit counts used for the CUDA-core (FFMA) ceiling.
 NUM_SMS = 152
 FP32_LANES_PER_SM = 128
+# Nominal dense tensor rates (PFLOP/s): a TF32 contraction is measured against the
+# measured bf16 peak times their ratio.
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
 
 
 def load_peaks():
@@ -91,6 +94,8 @@ def kernel_work(name: str, p, es: int, splits: int):
         return "hbm", 2 * P * 4 * C * es, "bytes"
     if name in ("forward_tc", "bwd_dx_tc", "bwd_dx_tc_packed", "bwd_dy_tc", "bwd_dw_tc"):
         return "tensor", gemm, "flops"
+    if name == "bwd_dw_tf32":
+        return "tensor_tf32", 2.0 * O * (C + 1) * P, "flops"
     return "unknown", 0.0, "flops"
 
 
@@ -399,12 +404,16 @@ def run_ours(args, world, rank, local):
         achieved, peak, unit = amount / (avg_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
     elif bound == "tensor":
         achieved, peak, unit = amount / (avg_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    elif bound == "tensor_tf32":
+        achieved, peak, unit = amount / (avg_ms * 1e-3) / 1e12, peaks["bf16_tflops"] * NOMINAL_TF32_OVER_BF16, "TFLOP/s"
     else:
         achieved, peak, unit = amount / (avg_ms * 1e-3) / 1e12, fp32_alu_tflops(peaks), "TFLOP/s"
     roof = {"bound": bound, "kernel": dominant, "achieved": round(achieved, 3), "peak": round(peak, 1),
             "unit": unit, "frac": round(achieved / peak, 4),
             "traffic": stored_traffic(dominant, p.name),
-            "peak_source": peaks["source"] if bound != "alu" else "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock",
+            "peak_source": {"alu": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock",
+                            "tensor_tf32": peaks["source"] + " bf16 x nominal tf32/bf16 (1.1/2.25)"}.get(
+                                bound, peaks["source"]),
             "avg_launch_us": round(avg_ms * 1e3, 3),
             "work_per_launch": amount, "work_unit": kind}
     kernels = {k: {"launches_per_step": len(v) / args.steps, "avg_us": round(sum(v) / len(v) * 1e3, 3),

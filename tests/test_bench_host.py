@@ -67,6 +67,7 @@ def test_kernel_work(bench):
     assert bench.kernel_work("bwd_dw_reduce", p, 2, 10) == ("hbm", 10 * O * (C + 1) * 4 + O * (C + 1) * 2,
                                                             "bytes")
     assert bench.kernel_work("filter_bwd_dx", p, 2, 1) == ("hbm", P * (O + 5 * C) * 2, "bytes")
+    assert bench.kernel_work("bwd_dw_tf32", p, 4, 16) == ("tensor_tf32", 2.0 * O * (C + 1) * P, "flops")
     assert bench.kernel_work("filter_bwd_dtaps", p, 4, 1) == ("hbm", P * (4 * C + O) * 4, "bytes")
     assert bench.kernel_work("no_such_kernel", p, 2, 1)[0] == "unknown"
 
