@@ -408,7 +408,8 @@ def run_ours(args, world, rank, local):
         achieved, peak, unit = amount / (avg_ms * 1e-3) / 1e12, peaks["bf16_tflops"] * NOMINAL_TF32_OVER_BF16, "TFLOP/s"
     else:
         achieved, peak, unit = amount / (avg_ms * 1e-3) / 1e12, fp32_alu_tflops(peaks), "TFLOP/s"
-    roof = {"bound": bound, "kernel": dominant, "achieved": round(achieved, 3), "peak": round(peak, 1),
+    roof = {"bound": "tensor" if bound == "tensor_tf32" else bound, "kernel": dominant,
+            "achieved": round(achieved, 3), "peak": round(peak, 1),
             "unit": unit, "frac": round(achieved / peak, 4),
             "traffic": stored_traffic(dominant, p.name),
             "peak_source": {"alu": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock",
