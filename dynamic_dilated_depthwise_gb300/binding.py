@@ -209,6 +209,10 @@ def _problem_of(x, K, dilations, flags=0):
 
 
 def _same(x, *ts):
+    """Every tensor a contiguous CUDA tensor on x's device with x's dtype (the library
+    takes raw device pointers: a host tensor must never reach it)."""
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("tensors must be contiguous CUDA tensors")
     for t in ts:
         if t is None:
             continue

@@ -10,6 +10,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from dynamic_dilated_depthwise_gb300 import binding, build
 
@@ -136,3 +137,20 @@ def test_bf16_workspace_adds_packed_copies(lib, B, C, H, W, K, dil, packed):
         assert n == ((parts + 255) // 256) * 256 + 4 * B * C * H * W * 2
     else:
         assert n == parts
+
+
+def test_binding_rejects_host_and_mixed_tensors():
+    """The binding checks its tensors before any library call: host tensors and mixed
+    dtypes raise in Python and never reach the kernels (no GPU needed)."""
+    x = torch.zeros(1, 2, 4, 8)
+    taps = torch.zeros(1, 3 * 2 * 9, 4, 8)
+    g = torch.zeros(1, 8, 4, 8)
+    with pytest.raises(ValueError):
+        binding.filter_pregenerated(x, taps, 3)
+    with pytest.raises(ValueError):
+        binding.filter_pregenerated_backward(g, x, taps, 3)
+    w, b = torch.zeros(54, 2), torch.zeros(54)
+    with pytest.raises(ValueError):
+        binding.forward(x, x, w, b, 3)
+    with pytest.raises(ValueError):
+        binding.backward(g, x, x, w, b, 3)
