@@ -19,6 +19,7 @@ warm-up steps, barrier + synchronize on both sides, max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -296,10 +297,13 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     p = WORKLOADS[args.workload]
+    seed = SEEDS[p.name] + rank
+    if args.batch is not None and args.batch != p.B:
+        p = dataclasses.replace(p, B=args.batch, name=f"{p.name}_batch{args.batch}")
     dtype = args.dtype
     es = 2 if dtype == "bfloat16" else 4
     step_kind = args.step
-    h = make_inputs(p, SEEDS[p.name] + rank, dtype, grad=step_kind in ("train", "filter_train"),
+    h = make_inputs(p, seed, dtype, grad=step_kind in ("train", "filter_train"),
                     taps=step_kind in ("filter", "filter_train"))
     if step_kind == "filter":
         h = {k: h[k] for k in ("x", "taps")}
@@ -308,7 +312,7 @@ def run_ours(args, world, rank, local):
     elif step_kind == "forward":
         h = {k: h[k] for k in ("x", "y", "weight", "bias")}
     d = {k: v.to(dev) for k, v in h.items()}
-    flags = binding.DDPM_FLAG_TF32_BACKWARD
+    flags = binding.DDPM_FLAG_CUDA_CORES if args.cuda_cores else binding.DDPM_FLAG_TF32_BACKWARD
     prob = binding.make_problem(p.B, p.C, p.H, p.W, p.K, p.dilations,
                                 binding.DDPM_BFLOAT16 if dtype == "bfloat16" else binding.DDPM_FLOAT32, flags)
     out = torch.empty((p.B, 4 * p.C, p.H, p.W), dtype=d["x"].dtype, device=dev)
@@ -317,6 +321,8 @@ def run_ours(args, world, rank, local):
     db = torch.empty((p.O,), dtype=d["x"].dtype, device=dev)
     dtaps = torch.empty_like(d["taps"]) if step_kind == "filter_train" else None
     ws_bytes = binding.ddpm_backward_workspace_size(prob) if step_kind == "train" else 0
+    if args.min_workspace and ws_bytes:
+        ws_bytes = binding.ddpm_backward_workspace_min(prob)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -341,6 +347,16 @@ def run_ours(args, world, rank, local):
                                    ws.numel(), sh)
         if s1 or s2:
             raise RuntimeError(f"library error {binding.status_string(s1 or s2)}")
+
+    if args.once:
+        # profiling aid: W untimed steps, then one more step, and nothing else
+        for _ in range(args.warmup + 1):
+            step()
+        torch.cuda.synchronize()
+        assert binding.ddpm_get_device_error() == 0
+        print(json.dumps({"once": step_kind, "workload": p.name, "dtype": dtype, "steps": args.warmup + 1}),
+              flush=True)
+        return None
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -512,9 +528,11 @@ def run_ours(args, world, rank, local):
                                 "filter_train": "ddpm_filter_pregenerated + ddpm_filter_pregenerated_backward "
                                                 "(dx, dtaps; taps given)"}[step_kind],
                        "l2": "flushed: 256 MiB write before each step, outside the timed events",
-                       "flags": "DDPM_FLAG_TF32_BACKWARD" + (" (FP32: dW/dbias partials on TF32 tensor cores; dX, dY "
-                                                             "and the forward in IEEE FP32)" if dtype == "float32"
-                                                             else " (ignored for bf16)"),
+                       "flags": ("DDPM_FLAG_CUDA_CORES" if args.cuda_cores else
+                                 "DDPM_FLAG_TF32_BACKWARD" + (" (FP32: dW/dbias partials on TF32 tensor cores; dX, dY "
+                                                              "and the forward in IEEE FP32)" if dtype == "float32"
+                                                              else " (ignored for bf16)")),
+                       "workspace_bytes": ws_bytes,
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
             "gpu_launches": int(round(launches_per_step * args.steps)),
@@ -612,11 +630,22 @@ def main():
     ap.add_argument("--step", choices=("train", "forward", "filter", "filter_train"), default="train",
                     help="what one timed step runs (default: the fwd+bwd training step)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (faster runs)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="run the workload with this batch size instead of its own (larger inputs for profiling)")
+    ap.add_argument("--min-workspace", action="store_true",
+                    help="give the backward only the smallest workspace it accepts (the dW/dbias partials)")
+    ap.add_argument("--cuda-cores", action="store_true",
+                    help="run the CUDA-core kernels (DDPM_FLAG_CUDA_CORES) instead of the tensor-core ones")
+    ap.add_argument("--once", action="store_true",
+                    help="profiling aid: run --warmup untimed steps and one more step, print nothing else "
+                         "(any --warmup >= 0); for one-kernel ncu captures")
     ap.add_argument("--peaks", action="store_true",
                     help="measure the FP32 FFMA and TF32 tensor peaks of this GPU and print them (one JSON line)")
     args = ap.parse_args()
-    if args.warmup < 3:
+    if args.warmup < 3 and not args.once:
         ap.error("--warmup must be at least 3")
+    if args.batch is not None and args.batch < 1:
+        ap.error("--batch must be at least 1")
     if args.peaks:
         print(json.dumps(measure_fp32_peaks()), flush=True)
         return

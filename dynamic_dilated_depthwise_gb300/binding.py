@@ -31,7 +31,8 @@ STATUS = {
 EXPORTED = ("ddpm_forward", "ddpm_filter_pregenerated", "ddpm_backward_workspace_size", "ddpm_backward",
             "ddpm_get_device_error", "ddpm_status_string", "ddpm_version", "ddpm_trace_enable",
             "ddpm_trace_read", "ddpm_kernel_name", "ddpm_backward_noalloc", "ddpm_measure_ffma_tflops",
-            "ddpm_filter_pregenerated_backward")
+            "ddpm_filter_pregenerated_backward", "ddpm_debug_wait_probe",
+            "ddpm_backward_workspace_min_size")
 
 
 class ddpm_problem(ctypes.Structure):
@@ -65,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ddpm_filter_pregenerated.argtypes = [P, vp, vp, vp, vp]
         lib.ddpm_filter_pregenerated_backward.argtypes = [P, vp, vp, vp, vp, vp, vp]
         lib.ddpm_backward_workspace_size.argtypes = [P, ctypes.POINTER(sz)]
+        lib.ddpm_backward_workspace_min_size.argtypes = [P, ctypes.POINTER(sz)]
+        lib.ddpm_backward_workspace_min_size.restype = ctypes.c_int
         lib.ddpm_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.ddpm_get_device_error.argtypes = [vp]
         lib.ddpm_backward_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -78,6 +81,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.ddpm_trace_read.restype = ctypes.c_int
         lib.ddpm_measure_ffma_tflops.argtypes = [ctypes.POINTER(ctypes.c_double)]
         lib.ddpm_measure_ffma_tflops.restype = ctypes.c_int
+        lib.ddpm_debug_wait_probe.argtypes = [ctypes.c_uint, vp]
+        lib.ddpm_debug_wait_probe.restype = ctypes.c_int
         lib.ddpm_kernel_name.argtypes = [ctypes.c_int]
         lib.ddpm_kernel_name.restype = ctypes.c_char_p
         for f in ("ddpm_forward", "ddpm_filter_pregenerated", "ddpm_backward_workspace_size", "ddpm_backward",
@@ -148,6 +153,13 @@ def ddpm_backward_workspace_size(problem) -> int:
     return int(n.value)
 
 
+def ddpm_backward_workspace_min(problem) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().ddpm_backward_workspace_min_size(ctypes.byref(problem), ctypes.byref(n)),
+           "ddpm_backward_workspace_min_size")
+    return int(n.value)
+
+
 def ddpm_backward(problem, grad_out, x, y, weight, bias, dx, dy, dweight, dbias, workspace, workspace_bytes,
                   stream=None) -> None:
     _check(load().ddpm_backward(ctypes.byref(problem), _p(grad_out), _p(x), _p(y), _p(weight), _p(bias), _p(dx),
@@ -165,6 +177,11 @@ def ddpm_backward_noalloc(problem, grad_out, x, y, weight, bias, dx, dy, dweight
 
 def ddpm_get_device_error(stream=None) -> int:
     return int(load().ddpm_get_device_error(_stream(stream)))
+
+
+def ddpm_debug_wait_probe(limit_us: int, stream=None) -> None:
+    """Enqueue the bounded-wait failure probe (a wait that expires after limit_us)."""
+    _check(load().ddpm_debug_wait_probe(int(limit_us), _stream(stream)), "ddpm_debug_wait_probe")
 
 
 def ddpm_version() -> int:

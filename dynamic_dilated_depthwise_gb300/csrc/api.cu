@@ -139,6 +139,10 @@ ddpm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DDPM_OK : DDPM_
 
 }  // namespace
 
+namespace ddpm {
+ddpm_status backward_workspace_min(const ddpm_problem* problem, size_t* bytes);
+}
+
 extern "C" {
 
 ddpm_status ddpm_forward(const ddpm_problem* problem, const void* x, const void* y, const void* weight,
@@ -200,6 +204,10 @@ ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* by
                  ? packed_offset(d) + ddpm::bwd_dx_packed_bytes(d)
                  : ddpm::backward_simt_workspace(d);
     return DDPM_OK;
+}
+
+ddpm_status ddpm_backward_workspace_min_size(const ddpm_problem* problem, size_t* bytes) {
+    return ddpm::backward_workspace_min(problem, bytes);
 }
 
 ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, const void* x, const void* y,

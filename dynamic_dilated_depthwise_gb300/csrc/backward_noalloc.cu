@@ -5,16 +5,20 @@
 // device memory, a real-time loop that forbids allocation after start-up, or
 // a plain C caller with no allocator for temporaries).  For them this entry
 // point keeps the backward's scratch -- the <= 16 FP32 dW/dbias partial sums
-// -- in a fixed device array that is part of the library itself.  The array
-// holds no channel-chunked copies of y and grad, so dX runs on the kernel that
-// stages its operands itself.
+// -- in a fixed device array that is part of the library itself.  The whole
+// array is handed to ddpm_backward as its workspace: where it also has room for
+// the channel-chunked copies of y and grad (BF16 problems with small images)
+// dX takes the packed kernel, as ddpm_backward would with a workspace of that
+// size; otherwise dX runs on the kernel that stages its operands itself.
 //
 // The array is a file-scope __device__ object of DDPM_NOALLOC_SCRATCH_BYTES.
 // Every GPU that loads this library holds it until the process exits.  Host
 // code cannot use the array's name as a device address, so the first call on
 // each device looks the address up with cudaGetSymbolAddress (with that device
 // current) and caches it; that first call should therefore come before any
-// stream capture.  All calls share the one array, and it keeps whatever the
+// stream capture.  The address is kept for the life of the process: after a
+// cudaDeviceReset it would no longer be the array's, so this entry point must
+// not be called again after one.  All calls share the one array, and it keeps whatever the
 // last call left in it.  Nothing in it needs to start at zero: the partial
 // kernel overwrites every slot the reduce kernel then reads.  Two calls whose
 // work overlaps on the GPU (different streams, or different host threads on

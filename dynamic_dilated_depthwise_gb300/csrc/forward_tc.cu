@@ -4,26 +4,28 @@
 //   y tile -> dot(weight, y) -> dynamic taps -> consume with shifted x -> output,
 // with the taps living only on chip; BF16 taps are rounded to bf16 before use.
 //
-// GB300 design.  A persistent CTA owns one group of 16 output channels and
-// walks pixel tiles of 128 pixels (2 rows x 64 columns, or several whole rows
-// when W < 64).  Per tile and dilation d the generator GEMM is
-//   D[p, n] = sum_j y[j, p] * W[o_n, j] + bias[o_n],  n = c_local*9 + k  (144 columns)
-// issued as tcgen05.mma (M = 128 pixels, N = 144, K = 64 in four K=16 steps,
-// plus one K=16 step that adds the bias through a ones column) into TMEM:
+// GB300 design.  A persistent CTA owns one group of CG output channels (CG = 8
+// for K = 3, two CTAs per SM; CG = 4 for K = 5, one CTA per SM) and walks pixel
+// tiles of 128 pixels (2 rows x 64 columns, or several whole rows when W < 64).
+// Per tile and dilation d the generator GEMM is
+//   D[p, n] = sum_j y[j, p] * W[o_n, j] + bias[o_n],  n = c_local*K*K + k
+// (CG*K*K taps, padded to N = 80 for K = 3 and N = 112 for K = 5), issued as
+// tcgen05.mma (M = 128 pixels, N, K = 64 in four K=16 steps, plus one K=16 step
+// that adds the bias through a ones column) into TMEM:
 // TMEM lane = pixel, so each epilogue thread owns every tap of its pixel and
 // filters without any cross-thread reduction.
 //
 //   warp 0      TMA producer: W slice of the group (once), y tiles (2 stages)
 //   warp 1      TMEM owner + MMA issuer (one elected lane)
 //   warp 2      TMA producer: the x window of each tile, one box per channel
-//               into a slot of fixed stride (3 buffers)
+//               into a slot of fixed stride (2 buffers)
 //   warps 3..   epilogue: each thread owns one pixel and kCPT channels.  Per
-//               dilation it reads its 9*kCPT taps from TMEM, rounds each pair
+//               dilation it reads its K*K*kCPT taps from TMEM, rounds each pair
 //               of channels' taps to bf16 with one conversion, and accumulates
 //               tap * x with the mixed-precision FMA (bf16 operands, FP32
 //               accumulator, exact product), x read as bf16 straight from the
 //               window at immediate offsets.
-// Three TMEM regions (one per dilation, 144 columns each) form the MMA /
+// Three TMEM regions (one per dilation, N columns each) form the MMA /
 // epilogue pipeline: a region is released as soon as its taps are in registers.
 #include <utility>
 

@@ -77,21 +77,28 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 constexpr uint32_t kSuspendHintNs = 20000u;   // re-check abort / time limit at least this often
 
 // Wait for the phase with the given parity to complete.  Returns false (and
-// records kErrTimeout) if it has not after kWaitLimitNs, or if *abort is set
-// by another thread that gave up first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
-                                          volatile int* abort) {
+// records kErrTimeout) if it has not after limit_ns, or if *abort is set by
+// another thread that gave up first.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                              volatile int* abort, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
+    const uint32_t hint = limit_ns < kSuspendHintNs ? (uint32_t)limit_ns : kSuspendHintNs;
     while (true) {
-        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+        if (mbar_try_wait_suspend(bar, parity, hint)) return true;
         if (*abort) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort = 1;
             if (err) atomicOr(err, kErrTimeout);
             return false;
         }
     }
+}
+
+// The kernels' wait: mbar_wait_for with the library's limit (kWaitLimitNs).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                          volatile int* abort) {
+    return mbar_wait_for(bar, parity, err, abort, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- TMA --

@@ -132,9 +132,23 @@ DDPM_API ddpm_status ddpm_filter_pregenerated_backward(const ddpm_problem* probl
  * Host only; enqueues nothing.  The workspace holds at most 16 FP32 partial
  * sums of [O, C+1] (dW and dbias), per README section "CUDA Flash 式融合训练"
  * (dWeight/dbias: split tokens into at most 16 FP32 partials, reduce them in a
- * second short kernel) -- a few MiB, independent of the image size.
+ * second short kernel): 16 * O * (C+1) * 4 bytes at most, independent of the
+ * image size (7.2 MB for C = 64, K = 3).  For BF16 problems whose dX runs on the
+ * packed tensor-core kernel, the returned size also covers channel-chunked
+ * copies of y and of the three dilation blocks of grad (4 * B * C * H * W bf16
+ * elements, which does grow with the image); ddpm_backward accepts any
+ * workspace of at least the partials' size and then stages dX's operands inside
+ * the kernel instead.
  */
 DDPM_API ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* bytes);
+
+/*
+ * ddpm_backward_workspace_min_size -- the smallest workspace ddpm_backward
+ * accepts: the <= 16 FP32 partial sums of [O, C+1] alone (same section), i.e. at
+ * most 16 * O * (C+1) * 4 bytes whatever the image size.  With a workspace of
+ * this size dX stages its operands inside the kernel.  Host only.
+ */
+DDPM_API ddpm_status ddpm_backward_workspace_min_size(const ddpm_problem* problem, size_t* bytes);
 
 /*
  * ddpm_backward -- gradients of L = <grad_out, out> for ddpm_forward.
@@ -173,13 +187,18 @@ DDPM_API ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad
  *   Arguments and results are those of ddpm_backward, minus the workspace.
  *   The FP32 dW/dbias partial sums live in a fixed device array of
  *   DDPM_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library; every GPU that loads
- *   the library holds it until the process exits.  Problems whose partials
- *   need more (ddpm_backward_workspace_size() > DDPM_NOALLOC_SCRATCH_BYTES,
- *   e.g. C=64 with K=5) are rejected with DDPM_ERR_UNSUPPORTED before anything
- *   is enqueued; C=64, K=3 needs 7.2 MB at any image size.
+ *   the library holds it until the process exits.  The criterion is the
+ *   partials alone: problems whose partials need more than the array
+ *   (16 * 3*C*K*K * (C+1) * 4 bytes at most; e.g. C=64 with K=5 needs 20 MB)
+ *   are rejected with DDPM_ERR_UNSUPPORTED before anything is enqueued; C=64,
+ *   K=3 needs 7.2 MB at any image size.  ddpm_backward_workspace_size() may
+ *   report more for the same problem, because it also counts the optional
+ *   packed copies that only speed up dX.
  *   No device memory is allocated or freed.  The first call on each device looks
  *   up the array's device address (cudaGetSymbolAddress with that device
- *   current); make that first call before any stream capture.
+ *   current) and keeps it for the life of the process; make that first call
+ *   before any stream capture, and do not call this entry point again after a
+ *   cudaDeviceReset (the kept address would no longer be the array's).
  *   All calls share the one array and it keeps the last call's contents (no
  *   slot needs to start at zero: each call overwrites every slot it reads).
  *   Calls that overlap on the GPU -- on different streams or from different
@@ -195,6 +214,21 @@ DDPM_API ddpm_status ddpm_backward_noalloc(const ddpm_problem* problem, const vo
  * Returns DDPM_OK, DDPM_ERR_DEVICE_TIMEOUT or DDPM_ERR_CUDA.
  */
 DDPM_API ddpm_status ddpm_get_device_error(ddpm_stream_t stream);
+
+/*
+ * ddpm_debug_wait_probe -- run the library's bounded-wait failure path once, on
+ * purpose (a diagnostic; the pages have no counterpart).  Every tensor-core
+ * kernel here waits on shared-memory barriers with a time limit (2 s); when a
+ * limit runs out, the block records DDPM_ERR_DEVICE_TIMEOUT in the device error
+ * word, makes its other waiters leave, frees its tensor memory and returns
+ * instead of trapping, so the CUDA context stays usable.  This enqueues on
+ * `stream` a kernel with the same warp roles whose wait can never be satisfied,
+ * limited to `limit_us` microseconds (1 .. 1,000,000).  Afterwards
+ * ddpm_get_device_error(stream) reports (and clears) DDPM_ERR_DEVICE_TIMEOUT.
+ * Returns DDPM_ERR_INVALID_ARGUMENT for a limit outside the range (nothing is
+ * enqueued), DDPM_ERR_CUDA if the launch fails, else DDPM_OK.
+ */
+DDPM_API ddpm_status ddpm_debug_wait_probe(unsigned int limit_us, ddpm_stream_t stream);
 
 /*
  * Kernel tracing (profiling aid; off by default).

@@ -137,6 +137,9 @@ def test_bf16_workspace_adds_packed_copies(lib, B, C, H, W, K, dil, packed):
         assert n == ((parts + 255) // 256) * 256 + 4 * B * C * H * W * 2
     else:
         assert n == parts
+    # the smallest workspace the backward accepts is the partials alone, in every dtype
+    assert binding.ddpm_backward_workspace_min(p) == parts
+    assert binding.ddpm_backward_workspace_min(p) <= 16 * 3 * C * K * K * (C + 1) * 4
 
 
 def test_binding_rejects_host_and_mixed_tensors():
@@ -154,3 +157,9 @@ def test_binding_rejects_host_and_mixed_tensors():
         binding.forward(x, x, w, b, 3)
     with pytest.raises(ValueError):
         binding.backward(g, x, x, w, b, 3)
+
+
+def test_wait_probe_rejects_limits_out_of_range(lib):
+    """The failure probe's limit is checked on the host: nothing is enqueued."""
+    assert lib.ddpm_debug_wait_probe(0, None) == 1
+    assert lib.ddpm_debug_wait_probe(1000001, None) == 1

@@ -31,7 +31,10 @@ def lib():
     return binding.load()
 
 
+# FP32 regression shape; a small BF16 image whose packed copies also fit in the array
+# (dX takes the packed kernel); the 256x256 BF16 workload (dX stages its operands)
 CASES = [(Problem(2, 24, 15, 17, 3), "float32", 41),
+         (Problem(1, 64, 32, 32, 3), "bfloat16", 42),
          (WORKLOADS["b1_c64_256x256_k3"], "bfloat16", SEEDS["b1_c64_256x256_k3"])]
 
 
@@ -54,12 +57,22 @@ def test_noalloc_backward_matches_workspace_backward(lib):
             torch.cuda.synchronize()
             for name, got, want in zip(("dx", "dy", "dW", "dbias"), outs, ref):
                 assert torch.isfinite(got).all(), f"call {call}: {name} not fully written"
-                assert_grad_close(got, want, dtype, f"call {call} {name}")
+                assert_grad_close(got, want, dtype, f"{name} (call {call})")
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch(lib):
     p = WORKLOADS["b1_c64_128x128_k5"]          # partials need 16 x 4800 x 65 x 4 B = 20 MB > 8 MiB
     prob = binding.make_problem(p.B, p.C, p.H, p.W, p.K, p.dilations, binding.DDPM_BFLOAT16)
     assert binding.ddpm_backward_workspace_size(prob) > 8 << 20
-    status = lib.ddpm_backward_noalloc(ctypes.byref(prob), 256, 256, 256, 256, 256, 256, 256, 256, 256, None)
+    # real device buffers of the problem's shapes: were the size check ever to let the
+    # problem through, the backward would run on valid memory and the status would say so
+    h = make_inputs(p, 5, "bfloat16")
+    d = {k: v.cuda() for k, v in h.items()}
+    outs = [torch.empty_like(d["x"]), torch.empty_like(d["x"]), torch.empty_like(d["weight"]),
+            torch.empty_like(d["bias"])]
+    status = lib.ddpm_backward_noalloc(ctypes.byref(prob), d["grad_out"].data_ptr(), d["x"].data_ptr(),
+                                       d["y"].data_ptr(), d["weight"].data_ptr(), d["bias"].data_ptr(),
+                                       outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(),
+                                       outs[3].data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
     assert status == 2  # DDPM_ERR_UNSUPPORTED, rejected on the host before any launch
