@@ -97,6 +97,8 @@ def kernel_work(name: str, p, es: int, splits: int):
         return "tensor", gemm, "flops"
     if name == "bwd_dw_tf32":
         return "tensor_tf32", 2.0 * O * (C + 1) * P, "flops"
+    if name == "forward_tf32":             # the algorithm's contraction (the kernel issues it as 3 TF32 products)
+        return "tensor_tf32", gemm, "flops"
     return "unknown", 0.0, "flops"
 
 
@@ -190,7 +192,11 @@ class ClockSampler:
 # depend on every shared header, .cuh / .h).
 KERNEL_SOURCE = {"forward_tc": "forward_tc.cu", "pack_chunks": "bwd_dx_packed.cu",
                  "bwd_dx_tc_packed": "bwd_dx_packed.cu", "bwd_dy_tc": "bwd_dy_tc.cu", "bwd_dw_tc": "bwd_dw_tc.cu",
-                 "bwd_dw_reduce": "backward_simt.cu"}
+                 "bwd_dw_reduce": "backward_simt.cu", "bwd_dx_tc": "bwd_dx_tc.cu", "bwd_dw_tf32": "bwd_dw_tf32.cu",
+                 "forward_tf32": "forward_tf32.cu", "forward_simt": "forward_simt.cu",
+                 "filter_pregenerated_simt": "filter_simt.cu", "filter_bwd_dx": "filter_bwd_simt.cu",
+                 "filter_bwd_dtaps": "filter_bwd_simt.cu", "bwd_dx_simt": "backward_simt.cu",
+                 "bwd_dy_simt": "backward_simt.cu", "bwd_dw_partial_simt": "backward_simt.cu"}
 
 
 def kernel_source_digest(kernel: str) -> str:
@@ -313,6 +319,8 @@ def run_ours(args, world, rank, local):
         h = {k: h[k] for k in ("x", "y", "weight", "bias")}
     d = {k: v.to(dev) for k, v in h.items()}
     flags = binding.DDPM_FLAG_CUDA_CORES if args.cuda_cores else binding.DDPM_FLAG_TF32_BACKWARD
+    if args.tf32x3 and not args.cuda_cores:
+        flags |= binding.DDPM_FLAG_TF32X3_FORWARD
     prob = binding.make_problem(p.B, p.C, p.H, p.W, p.K, p.dilations,
                                 binding.DDPM_BFLOAT16 if dtype == "bfloat16" else binding.DDPM_FLOAT32, flags)
     out = torch.empty((p.B, 4 * p.C, p.H, p.W), dtype=d["x"].dtype, device=dev)
@@ -531,7 +539,9 @@ def run_ours(args, world, rank, local):
                        "flags": ("DDPM_FLAG_CUDA_CORES" if args.cuda_cores else
                                  "DDPM_FLAG_TF32_BACKWARD" + (" (FP32: dW/dbias partials on TF32 tensor cores; dX, dY "
                                                               "and the forward in IEEE FP32)" if dtype == "float32"
-                                                              else " (ignored for bf16)")),
+                                                              else " (ignored for bf16)")
+                                 + (" | DDPM_FLAG_TF32X3_FORWARD (FP32 generator GEMM as three TF32 products, "
+                                    "filter IEEE FP32)" if args.tf32x3 else "")),
                        "workspace_bytes": ws_bytes,
                        "parallelism": f"replicas x{world}"},
             "roofline": roof, "step_roofline": step_roof, "kernels": kernels,
@@ -636,6 +646,9 @@ def main():
                     help="give the backward only the smallest workspace it accepts (the dW/dbias partials)")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="run the CUDA-core kernels (DDPM_FLAG_CUDA_CORES) instead of the tensor-core ones")
+    ap.add_argument("--tf32x3", action="store_true",
+                    help="FP32: compute the forward's generator GEMM as three TF32 tensor-core products "
+                         "(DDPM_FLAG_TF32X3_FORWARD); the filter stays IEEE FP32")
     ap.add_argument("--once", action="store_true",
                     help="profiling aid: run --warmup untimed steps and one more step, print nothing else "
                          "(any --warmup >= 0); for one-kernel ncu captures")

@@ -23,6 +23,7 @@ DDPM_FLOAT32 = 0
 DDPM_BFLOAT16 = 1
 DDPM_FLAG_TF32_BACKWARD = 0x1
 DDPM_FLAG_CUDA_CORES = 0x2
+DDPM_FLAG_TF32X3_FORWARD = 0x4
 
 STATUS = {
     0: "DDPM_OK", 1: "DDPM_ERR_INVALID_ARGUMENT", 2: "DDPM_ERR_UNSUPPORTED", 3: "DDPM_ERR_MISALIGNED",

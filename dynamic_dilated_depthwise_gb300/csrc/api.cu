@@ -98,7 +98,8 @@ ddpm_status validate(const ddpm_problem* p, Dims* d) {
     if (p->dtype != DDPM_FLOAT32 && p->dtype != DDPM_BFLOAT16) return DDPM_ERR_INVALID_ARGUMENT;
     for (int i = 0; i < 3; ++i)
         if (p->dilations[i] < 1) return DDPM_ERR_INVALID_ARGUMENT;
-    if ((p->flags & ~(DDPM_FLAG_TF32_BACKWARD | DDPM_FLAG_CUDA_CORES)) != 0) return DDPM_ERR_INVALID_ARGUMENT;
+    if ((p->flags & ~(DDPM_FLAG_TF32_BACKWARD | DDPM_FLAG_CUDA_CORES | DDPM_FLAG_TF32X3_FORWARD)) != 0)
+        return DDPM_ERR_INVALID_ARGUMENT;
     if (p->K > 7) return DDPM_ERR_UNSUPPORTED;
     // grid-dimension and index-width limits of this build
     if (p->B > 65535 || p->C > 65535) return DDPM_ERR_UNSUPPORTED;
@@ -158,6 +159,8 @@ ddpm_status ddpm_forward(const ddpm_problem* problem, const void* x, const void*
     try {
         if (ddpm::forward_tc_eligible(d, y, weight) && (uintptr_t)x % 16 == 0)
             return from_cuda(ddpm::launch_forward_tc(d, x, y, weight, bias, out, (cudaStream_t)stream));
+        if (ddpm::forward_tf32_eligible(d, x, y, weight, out))
+            return from_cuda(ddpm::launch_forward_tf32(d, x, y, weight, bias, out, (cudaStream_t)stream));
         return from_cuda(ddpm::launch_forward_simt(d, x, y, weight, bias, out, (cudaStream_t)stream));
     } catch (...) {
         return DDPM_ERR_CUDA;

@@ -1,0 +1,503 @@
+// forward_tf32.cu -- FP32 fused generator + filter with the generator GEMM on tcgen05 tensor
+// cores in three TF32 products (opt-in: DDPM_FLAG_TF32X3_FORWARD).
+//
+// README "lartpang/DynamicConvolutionOperator", section "CUDA 融合生成器推理": y tile ->
+// dot(weight, y) -> dynamic taps -> consume with shifted x -> output, the taps living only
+// on chip.  Section "已验证但未采用的方案" lists tf32x3 for the FP32 forward as tried on
+// the page's card and not adopted there; GB300's TF32 rate (about 12x its FP32 FMA rate)
+// is the reason to offer it here.  The filter itself stays IEEE FP32 FMA.
+//
+// Each FP32 operand a is split as hi = tf32(a) (round to nearest) and lo = a - hi (exact),
+// and the GEMM is accumulated in FP32 as hi_y*hi_W + hi_y*lo_W + lo_y*hi_W: the neglected
+// lo*lo term and the TF32 reading of lo leave a relative error of about 2^-21 per product.
+// The bias enters as one more K step (a ones column against bias_hi and bias_lo).
+//
+// GB300 design (the FP32 counterpart of forward_tc.cu).  A persistent CTA (one per SM)
+// owns CG output channels (CG = 4, N = 48 taps per dilation, 36 of them real) and walks
+// 128-pixel tiles (2 rows x 64 columns, or whole rows when W < 64).  TMEM lane = pixel, so
+// each epilogue thread owns every tap of its pixel.
+//   warp 0      TMA: the group's W rows (once, 128B-swizzled K-major) and each tile's raw
+//               y [64 j][128 px] (one stage)
+//   warp 1      TMEM owner + MMA issuer: per dilation 8 K-steps x 3 products + the bias
+//               step, kind::tf32, M = 128, N = 48, into one of three TMEM regions
+//   warp 2      TMA: the x window of each tile, one box per channel (2 buffers)
+//   warps 3-6   splitters: W and bias hi/lo once; per tile y hi/lo, transposed into
+//               128B-swizzled K-major tiles (the MMA reads both operands K-major)
+//   warps 7-14  epilogue: each thread owns one pixel and 2 channels; per dilation it
+//               reads its 18 taps from TMEM and accumulates tap * x in IEEE FP32 FMA,
+//               x read from the window at the tap's offset; results leave by TMA store
+#include "bwd_tc_common.cuh"
+#include "tc.cuh"
+
+namespace ddpm {
+namespace {
+
+constexpr int kTile = 128;               // pixels per tile (MMA M)
+constexpr int kKPad = 64;                // generator K (channels of y), zero padded
+constexpr int kCG = 4;                   // output channels per CTA group
+constexpr int kTaps = 9;                 // K = 3
+constexpr int kN = 48;                   // MMA N per dilation: 36 taps padded to a multiple of 16
+constexpr int kHalo = 8;                 // x window columns left / right of the tile
+constexpr int kWinMax = 960;             // x window positions (TH + 2R) x (TW + 16)
+constexpr int kSplit0 = 3, kSplitWarps = 4;
+constexpr int kEpi0 = kSplit0 + kSplitWarps, kEpiWarps = 8;
+constexpr int kCPT = kCG / (kEpiWarps / 4);   // channels per epilogue thread (2)
+constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
+constexpr int kTmemCols = 256;
+constexpr int kRawBufs = 2;
+
+// shared memory (bytes from a 1024-aligned base)
+constexpr int kWAtom = kN * 128;                     // one K-atom (32 fp32 of K) of N rows, SW128
+constexpr int kSW = 0;                               // W hi [3 dil][2 K-atoms][N rows x 128 B]
+constexpr int kSWlo = kSW + 6 * kWAtom;              // W lo, same layout
+constexpr int kSYr = kSWlo + 6 * kWAtom;             // raw y [2 halves][64 j][64 px] fp32
+constexpr int kSYhi = kSYr + 2 * 64 * 64 * 4;        // y hi [2 K-atoms][128 rows x 128 B], SW128 K-major
+constexpr int kSYlo = kSYhi + 2 * kTile * 128;       // y lo, same layout
+constexpr int kSOnes = kSYlo + 2 * kTile * 128;      // ones A operand [128 x 8] fp32, no swizzle
+constexpr int kSBias = kSOnes + (kTile / 8) * 256;   // bias B operand 3 x [N x 8] fp32, no swizzle
+constexpr int kBiasTile = (kN / 8) * 256;
+constexpr int kSX = kSBias + 3 * kBiasTile;          // x windows 2 x [CG slots][kWinMax] fp32
+constexpr int kSlot = kWinMax * 4;
+constexpr int kRawBuf = kCG * kSlot;
+constexpr int kSStage = kSX + kRawBufs * kRawBuf;    // output staging 4 blocks x [CG][TH][TW] fp32
+constexpr int kStageBlk = kCG * kTile * 4;
+constexpr int kSmemBytes = kSStage + 4 * kStageBlk + 1024;
+static_assert(kWAtom % 1024 == 0 && kSWlo % 1024 == 0 && kSYhi % 1024 == 0 && kSYlo % 1024 == 0,
+              "SW128 atoms need 1 KiB alignment");
+static_assert(kSOnes % 128 == 0 && kSBias % 128 == 0 && kSX % 128 == 0 && kSlot % 128 == 0 && kSStage % 128 == 0,
+              "operand / TMA alignment");
+static_assert(3 * kN <= kTmemCols && kCG * kTaps <= kN && kN % 16 == 0, "MMA N and TMEM columns");
+static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory");
+
+struct Tf32Params {
+    Dims d;
+    int TH, TW, tiles_per_row, tiles_per_img, n_tiles, n_groups, ctas_per_group;
+    int R, WH, WC;
+    const float* bias;     // may be null
+    unsigned int* err;
+};
+
+struct TileCoord {
+    int b, h0, w0;
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const Tf32Params& P, int t) {
+    TileCoord c;
+    c.b = t / P.tiles_per_img;
+    const int ti = t % P.tiles_per_img;
+    c.h0 = (ti / P.tiles_per_row) * P.TH;
+    c.w0 = (ti % P.tiles_per_row) * P.TW;
+    return c;
+}
+
+// tf32 (nearest, ties away from zero) of an fp32 value, as fp32 with the low 13 bits clear
+__device__ __forceinline__ float tf32_hi(float a) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(a));
+    return __uint_as_float(r);
+}
+
+template <int NTHREADS>
+__device__ __forceinline__ void named_bar(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(NTHREADS) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    forward_tf32_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
+                        const Tf32Params P) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    // 1 KiB-aligned base by pointer arithmetic on the shared array (accesses stay shared-space)
+    uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ uint64_t bar_w, bar_wsplit, bar_yraw_full, bar_yraw_empty, bar_ysplit_full, bar_ysplit_empty,
+        bar_acc_full[3], bar_acc_empty[3], bar_raw_full[kRawBufs], bar_raw_empty[kRawBufs], bar_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = blockIdx.x % P.n_groups;
+    const int cta_in_group = blockIdx.x / P.n_groups;
+    const int c0 = group * kCG;
+    const int C = P.d.C;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar_w, 1);
+        mbar_init(&bar_wsplit, kSplitWarps);
+        mbar_init(&bar_yraw_full, 1);
+        mbar_init(&bar_yraw_empty, kSplitWarps);
+        mbar_init(&bar_ysplit_full, kSplitWarps);
+        mbar_init(&bar_ysplit_empty, 1);
+        for (int dd = 0; dd < 3; ++dd) {
+            mbar_init(&bar_acc_full[dd], 1);
+            mbar_init(&bar_acc_empty[dd], kEpiWarps);
+        }
+        for (int s = 0; s < kRawBufs; ++s) {
+            mbar_init(&bar_raw_full[s], 1);
+            mbar_init(&bar_raw_empty[s], kEpiWarps);
+        }
+        mbar_init(&bar_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
+    if (warp >= kEpi0) {
+        // constant operands (no swizzle, 8x16-byte core matrices, element (m, k) at
+        // (m/8)*256 + (k/4)*128 + (m%8)*16 + (k%4)*4): a ones pair (A, columns 0 and 1) and
+        // the bias split into hi and lo (B, columns 0 and 1), so one K step adds hi + lo
+        const int et = threadIdx.x - 32 * kEpi0;
+        for (int i = et; i < kTile * 8; i += 32 * kEpiWarps) {
+            const int m = i / 8, k = i % 8;
+            *reinterpret_cast<float*>(sm + kSOnes + (m / 8) * 256 + (k / 4) * 128 + (m % 8) * 16 + (k % 4) * 4) =
+                k < 2 ? 1.0f : 0.0f;
+        }
+        for (int i = et; i < 3 * kN * 8; i += 32 * kEpiWarps) {
+            const int dd = i / (kN * 8), rem = i % (kN * 8), n = rem / 8, k = rem % 8;
+            const long long o = (long long)(dd * C + c0) * kTaps + n;
+            float v = 0.0f;
+            if (k < 2 && P.bias != nullptr && n < kCG * kTaps && o < P.d.O) {
+                const float b = P.bias[o];
+                const float hi = tf32_hi(b);
+                v = k == 0 ? hi : b - hi;
+            }
+            *reinterpret_cast<float*>(sm + kSBias + dd * kBiasTile + (n / 8) * 256 + (k / 4) * 128 + (n % 8) * 16 +
+                                      (k % 4) * 4) = v;
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const int n_my = cta_in_group < P.n_tiles ? (P.n_tiles - 1 - cta_in_group) / P.ctas_per_group + 1 : 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer: W, raw y
+        if (lane == 0) {
+            prefetch_tmap(&tmY);
+            prefetch_tmap(&tmW);
+            mbar_arrive_expect_tx(&bar_w, 6 * kWAtom);
+            for (int dd = 0; dd < 3; ++dd)
+                for (int kh = 0; kh < 2; ++kh)
+                    tma_load_2d(sm + kSW + (dd * 2 + kh) * kWAtom, &tmW, &bar_w, kh * 32, (dd * C + c0) * kTaps);
+            const int half_step = P.TW == 64 ? P.d.W : 64;
+            int issued = 0;
+            for (int i = 0; i < n_my; ++i) {
+                const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
+                if (!mbar_wait(&bar_yraw_empty, (i & 1) ^ 1, P.err, abort_v)) break;
+                const int pb = tcd.h0 * P.d.W + tcd.w0;
+                mbar_arrive_expect_tx(&bar_yraw_full, 2 * 64 * 64 * 4);
+                tma_load_3d(sm + kSYr, &tmY, &bar_yraw_full, pb, 0, tcd.b);
+                tma_load_3d(sm + kSYr + 64 * 64 * 4, &tmY, &bar_yraw_full, pb + half_step, 0, tcd.b);
+                issued = i + 1;
+            }
+            // drain: every copy this thread started lands before shared memory is released
+            int never = 0;
+            mbar_wait(&bar_w, 0, P.err, &never);
+            if (issued > 0) mbar_wait(&bar_yraw_full, (issued - 1) & 1, P.err, &never);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------- TMA producer: x windows
+        if (lane == 0) {
+            prefetch_tmap(&tmX);
+            const int nch = min(kCG, C - c0);
+            const uint32_t raw_bytes = (uint32_t)(nch * P.WH * P.WC * 4);
+            int issued = 0;
+            for (int i = 0; i < n_my; ++i) {
+                const int s = i % kRawBufs, ph = (i / kRawBufs) & 1;
+                const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
+                if (!mbar_wait(&bar_raw_empty[s], ph ^ 1, P.err, abort_v)) break;
+                mbar_arrive_expect_tx(&bar_raw_full[s], raw_bytes);
+                uint8_t* rb = sm + kSX + s * kRawBuf;
+                for (int c = 0; c < nch; ++c)
+                    tma_load_4d(rb + c * kSlot, &tmX, &bar_raw_full[s], tcd.w0 - kHalo, tcd.h0 - P.R, c0 + c, tcd.b);
+                issued = i + 1;
+            }
+            int never = 0;
+            for (int i = issued > kRawBufs ? issued - kRawBufs : 0; i < issued; ++i)
+                mbar_wait(&bar_raw_full[i % kRawBufs], (i / kRawBufs) & 1, P.err, &never);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(&bar_wsplit, 0, P.err, abort_v);
+            const uint32_t idesc = instr_desc(2, 0, 0, kTile, kN);   // TF32, both operands K-major
+            const uint64_t yhi = smem_desc(smem_u32(sm + kSYhi), 16, 1024, kSwizzle128B);
+            const uint64_t ylo = smem_desc(smem_u32(sm + kSYlo), 16, 1024, kSwizzle128B);
+            const uint64_t whi = smem_desc(smem_u32(sm + kSW), 16, 1024, kSwizzle128B);
+            const uint64_t wlo = smem_desc(smem_u32(sm + kSWlo), 16, 1024, kSwizzle128B);
+            const uint64_t ones = smem_desc(smem_u32(sm + kSOnes), 128, 256, kSwizzleNone);
+            const uint64_t bias = smem_desc(smem_u32(sm + kSBias), 128, 256, kSwizzleNone);
+            for (int i = 0; ok && i < n_my; ++i) {
+                if (!mbar_wait(&bar_ysplit_full, i & 1, P.err, abort_v)) break;
+                tc_fence_after();
+                for (int dd = 0; dd < 3 && ok; ++dd) {
+                    if (!mbar_wait(&bar_acc_empty[dd], (i & 1) ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t dt = tmem + dd * kN;
+#pragma unroll
+                    for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t ya = (uint32_t)(kh * kTile * 128 + kk * 32);
+                            const uint32_t wa = (uint32_t)((dd * 2 + kh) * kWAtom + kk * 32);
+                            mma_tf32(dt, desc_advance(yhi, ya), desc_advance(whi, wa), idesc, (kh | kk) ? 1u : 0u);
+                            mma_tf32(dt, desc_advance(yhi, ya), desc_advance(wlo, wa), idesc, 1u);
+                            mma_tf32(dt, desc_advance(ylo, ya), desc_advance(whi, wa), idesc, 1u);
+                        }
+                    mma_tf32(dt, ones, desc_advance(bias, (uint32_t)(dd * kBiasTile)), idesc, 1u);
+                    mma_commit(&bar_acc_full[dd]);
+                }
+                if (!ok) break;
+                mma_commit(&bar_ysplit_empty);
+            }
+            // all issued MMAs retire before TMEM is released
+            mma_commit(&bar_done);
+            int never = 0;
+            mbar_wait(&bar_done, 0, P.err, &never);
+        }
+    } else if (warp < kEpi0) {
+        // ------------------------------------------------------- splitters
+        const int st = threadIdx.x - 32 * kSplit0, nst = 32 * kSplitWarps;
+        bool ok = mbar_wait(&bar_w, 0, P.err, abort_v);
+        if (ok) {
+            // W hi in place, W lo beside it (same swizzled offsets: the split is elementwise)
+            for (int i = st; i < 6 * kWAtom / 16; i += nst) {
+                float4* ph = reinterpret_cast<float4*>(sm + kSW) + i;
+                float4* pl = reinterpret_cast<float4*>(sm + kSWlo) + i;
+                const float4 v = *ph;
+                float4 h, l;
+                h.x = tf32_hi(v.x); l.x = v.x - h.x;
+                h.y = tf32_hi(v.y); l.y = v.y - h.y;
+                h.z = tf32_hi(v.z); l.z = v.z - h.z;
+                h.w = tf32_hi(v.w); l.w = v.w - h.w;
+                *ph = h;
+                *pl = l;
+            }
+            fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_wsplit);
+        for (int i = 0; ok && i < n_my; ++i) {
+            if (!mbar_wait(&bar_yraw_full, i & 1, P.err, abort_v) ||
+                !mbar_wait(&bar_ysplit_empty, (i & 1) ^ 1, P.err, abort_v)) {
+                ok = false;
+                break;
+            }
+            // unit = (pixel px, group of 4 input channels jc): a warp covers 32 consecutive
+            // pixels of one jc, so its raw reads are 128 contiguous bytes per channel and its
+            // 16-byte stores touch each bank once per 8 rows
+            for (int u = st; u < kTile * 16; u += nst) {
+                const int px = u % kTile, jc = u / kTile;
+                const float* raw = reinterpret_cast<const float*>(sm + kSYr + (px / 64) * 64 * 64 * 4) + (px % 64);
+                float4 h, l;
+                const float y0 = raw[(4 * jc + 0) * 64], y1 = raw[(4 * jc + 1) * 64];
+                const float y2 = raw[(4 * jc + 2) * 64], y3 = raw[(4 * jc + 3) * 64];
+                h.x = tf32_hi(y0); l.x = y0 - h.x;
+                h.y = tf32_hi(y1); l.y = y1 - h.y;
+                h.z = tf32_hi(y2); l.z = y2 - h.z;
+                h.w = tf32_hi(y3); l.w = y3 - h.w;
+                const int off = (jc / 8) * kTile * 128 + (px / 8) * 1024 + (px % 8) * 128 + (((jc % 8) ^ (px % 8)) << 4);
+                *reinterpret_cast<float4*>(sm + kSYhi + off) = h;
+                *reinterpret_cast<float4*>(sm + kSYlo + off) = l;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bar_yraw_empty);
+                mbar_arrive(&bar_ysplit_full);
+            }
+        }
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int ew = warp - kEpi0;
+        const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+        const int cl0 = (ew >> 2) * kCPT;        // first local channel of this thread
+        const int s = q * 32 + lane;             // pixel slot == TMEM lane
+        const bool leader = ew == 0 && lane == 0;
+        const int tpix = P.TH * P.TW;
+        const bool in_tile = s < tpix;
+        const int rr = in_tile ? s / P.TW : 0, cc = in_tile ? s % P.TW : 0;
+        const int WC = P.WC;
+        const int center = (rr + P.R) * WC + cc + kHalo;
+        float* stage0 = reinterpret_cast<float*>(sm + kSStage) + cl0 * tpix + (in_tile ? s : 0);
+        int buf = 0, bph = 0;
+        bool ok = true;
+        auto flush_block = [&](int blk, const TileCoord& tcd) {
+            fence_proxy_async_smem();
+            if (leader) bulk_wait_read<2>();
+            named_bar<32 * kEpiWarps>(1);
+            if (leader && ok) {
+                const int cbase = (blk == 0 ? 0 : blk * C) + c0;
+                tma_store_4d(&tmO, sm + kSStage + blk * kStageBlk, tcd.w0, tcd.h0, cbase, tcd.b);
+                bulk_commit();
+            }
+        };
+        for (int i = 0; i < n_my; ++i) {
+            const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
+            const float* xw = reinterpret_cast<const float*>(sm + kSX + buf * kRawBuf + cl0 * kSlot) + center;
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw_full[buf], bph, P.err, abort_v));
+            // channels c0 .. c0+CG-1 of the output are x itself
+            if (ok && in_tile) {
+#pragma unroll
+                for (int c = 0; c < kCPT; ++c) stage0[c * tpix] = xw[c * (kSlot / 4)];
+            }
+            flush_block(0, tcd);
+            for (int dd = 0; dd < 3; ++dd) {
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[dd], i & 1, P.err, abort_v));
+                if (!ok) {
+                    flush_block(1 + dd, tcd);
+                    continue;
+                }
+                tc_fence_after();
+                uint32_t t[kCPT * kTaps];
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + dd * kN + cl0 * kTaps;
+                DDPM_TMEM_LD_X16(ta, t);
+                DDPM_TMEM_LD_X2(ta + 16, (t + 16));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar_acc_empty[dd]);
+                const int dil = dil_of(P.d, dd);
+                float acc[kCPT];
+#pragma unroll
+                for (int c = 0; c < kCPT; ++c) acc[c] = 0.0f;
+#pragma unroll
+                for (int k = 0; k < kTaps; ++k) {
+                    const int off = ((k / 3 - 1) * WC + (k % 3 - 1)) * dil;
+#pragma unroll
+                    for (int c = 0; c < kCPT; ++c)
+                        acc[c] = fmaf(__uint_as_float(t[c * kTaps + k]), xw[c * (kSlot / 4) + off], acc[c]);
+                }
+                if (in_tile) {
+                    float* sa = stage0 + (1 + dd) * (kStageBlk / 4);
+#pragma unroll
+                    for (int c = 0; c < kCPT; ++c) sa[c * tpix] = acc[c];
+                }
+                if (dd == 2) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar_raw_empty[buf]);
+                }
+                flush_block(1 + dd, tcd);
+            }
+            if (++buf == kRawBufs) {
+                buf = 0;
+                bph ^= 1;
+            }
+        }
+        if (leader) bulk_wait<0>();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// fp32 NCHW tensor map, dims (W, H, ch, B)
+bool encode_nchw_f32(CUtensorMap* m, const void* base, const Dims& d, int ch, uint32_t bw, uint32_t bh, uint32_t bc) {
+    const cuuint64_t dims[4] = {(cuuint64_t)d.W, (cuuint64_t)d.H, (cuuint64_t)ch, (cuuint64_t)d.B};
+    const cuuint64_t str[3] = {(cuuint64_t)d.W * 4, (cuuint64_t)d.HW * 4, (cuuint64_t)d.HW * ch * 4};
+    const cuuint32_t box[4] = {bw, bh, bc, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return bwdtc::encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, str, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Tiling {
+    int TH, TW, tiles_per_row, tiles_per_img;
+};
+
+Tiling tiling_of(const Dims& d) {
+    Tiling t;
+    if (d.W >= 64) {
+        t.TW = 64;
+        t.TH = 2;
+        t.tiles_per_row = (d.W + 63) / 64;
+    } else {
+        t.TW = d.W;
+        t.TH = kTile / d.W < d.H ? kTile / d.W : d.H;
+        t.tiles_per_row = 1;
+    }
+    t.tiles_per_img = ((d.H + t.TH - 1) / t.TH) * t.tiles_per_row;
+    return t;
+}
+
+}  // namespace
+
+bool forward_tf32_eligible(const Dims& d, const void* x, const void* y, const void* w, const void* out) {
+    if (d.dtype != 0 || !(d.flags & kFlagTf32x3Forward) || (d.flags & kFlagCudaCores) || d.K != 3) return false;
+    if (d.C % kCG != 0 || d.C > kKPad || d.W % 4 != 0) return false;   // 16-byte TMA strides and coordinates
+    if (d.R() > kHalo) return false;
+    const Tiling t = tiling_of(d);
+    if ((long long)(t.TH + 2 * d.R()) * (t.TW + 2 * kHalo) > kWinMax) return false;
+    if ((uintptr_t)x % 16 || (uintptr_t)y % 16 || (uintptr_t)w % 16 || (uintptr_t)out % 16) return false;
+    const long long tiles = (long long)d.B * t.tiles_per_img;
+    return tiles <= (1LL << 30) && d.O <= (1LL << 30) && d.HW <= (1LL << 31) - 1024 && bwdtc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_forward_tf32(const Dims& d, const void* x, const void* y, const void* w, const void* bias,
+                                void* out, cudaStream_t s) {
+    static int attr_done[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)forward_tf32_kernel, kSmemBytes, attr_done, true);
+        if (e != cudaSuccess) return e;
+    }
+    auto enc = bwdtc::encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const Tiling t = tiling_of(d);
+    const int R = d.R();
+    CUtensorMap tmY, tmW, tmX, tmO;
+    const cuuint64_t dimY[3] = {(cuuint64_t)d.HW, (cuuint64_t)d.C, (cuuint64_t)d.B};
+    const cuuint64_t strY[2] = {(cuuint64_t)d.HW * 4, (cuuint64_t)d.HW * d.C * 4};
+    const cuuint32_t boxY[3] = {64, (cuuint32_t)kKPad, 1};
+    const cuuint32_t one3[3] = {1, 1, 1};
+    if (enc(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(y), dimY, strY, boxY, one3,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    // W [O, C] fp32: boxes of 32 input channels (one 128-byte swizzle row) x N rows
+    const cuuint64_t dimW[2] = {(cuuint64_t)d.C, (cuuint64_t)d.O};
+    const cuuint64_t strW[1] = {(cuuint64_t)d.C * 4};
+    const cuuint32_t boxW[2] = {32, (cuuint32_t)kN};
+    const cuuint32_t one2[2] = {1, 1};
+    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(w), dimW, strW, boxW, one2,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int WH = t.TH + 2 * R, WC = t.TW + 2 * kHalo;
+    if (!encode_nchw_f32(&tmX, x, d, d.C, (uint32_t)WC, (uint32_t)WH, 1) ||
+        !encode_nchw_f32(&tmO, out, d, 4 * d.C, (uint32_t)t.TW, (uint32_t)t.TH, (uint32_t)kCG))
+        return cudaErrorInvalidValue;
+
+    Tf32Params P;
+    P.d = d;
+    P.TH = t.TH;
+    P.TW = t.TW;
+    P.tiles_per_row = t.tiles_per_row;
+    P.tiles_per_img = t.tiles_per_img;
+    P.n_tiles = d.B * t.tiles_per_img;
+    P.n_groups = d.C / kCG;
+    int cpg = num_sms() / P.n_groups;
+    if (cpg < 1) cpg = 1;
+    if (cpg > P.n_tiles) cpg = P.n_tiles;
+    P.ctas_per_group = cpg;
+    P.R = R;
+    P.WH = WH;
+    P.WC = WC;
+    P.bias = static_cast<const float*>(bias);
+    P.err = device_error_word();
+    if (P.err == nullptr) return cudaErrorUnknown;
+    trace_begin(s, kKForwardTf32);
+    forward_tf32_kernel<<<P.n_groups * cpg, kThreads, kSmemBytes, s>>>(tmY, tmW, tmX, tmO, P);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace ddpm

@@ -26,7 +26,8 @@ enum KernelId : int {
     kKBwdDwTf32 = 12,
     kKFilterBwdDx = 13,
     kKFilterBwdDtaps = 14,
-    kKNumKernels = 15
+    kKForwardTf32 = 15,
+    kKNumKernels = 16
 };
 
 // Tracing hooks around each launch (cheap no-ops while tracing is off).
@@ -38,6 +39,8 @@ void trace_end(cudaStream_t s);
 // TF32 tensor-core contractions in an FP32 backward (DDPM_FLAG_TF32_BACKWARD).
 constexpr unsigned kFlagCudaCores = 0x2u;
 constexpr unsigned kFlagTf32Backward = 0x1u;
+// FP32 forward with the generator GEMM as three TF32 tensor-core products (DDPM_FLAG_TF32X3_FORWARD).
+constexpr unsigned kFlagTf32x3Forward = 0x4u;
 
 // Multiprocessor count of the current device (cached per device).
 int num_sms();
@@ -74,6 +77,12 @@ cudaError_t launch_forward_simt(const Dims& d, const void* x, const void* y, con
 bool forward_tc_eligible(const Dims& d, const void* y, const void* w);
 cudaError_t launch_forward_tc(const Dims& d, const void* x, const void* y, const void* w,
                               const void* bias, void* out, cudaStream_t s);
+
+// FP32 fused generator + filter, generator GEMM as hi*hi + hi*lo + lo*hi TF32 products
+// on tcgen05 tensor cores, filter in IEEE FP32 FMA (K = 3, C a multiple of 4 up to 64).
+bool forward_tf32_eligible(const Dims& d, const void* x, const void* y, const void* w, const void* out);
+cudaError_t launch_forward_tf32(const Dims& d, const void* x, const void* y, const void* w,
+                                const void* bias, void* out, cudaStream_t s);
 
 // Backward on CUDA cores: dX gather, dY, dW/dbias split partials + reduce.
 size_t backward_simt_workspace(const Dims& d);

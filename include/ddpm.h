@@ -75,6 +75,18 @@ typedef enum { DDPM_FLOAT32 = 0, DDPM_BFLOAT16 = 1 } ddpm_dtype;
 /* DDPM_FLAG_CUDA_CORES: run the CUDA-core (FFMA) kernels even where a
  *   tensor-core kernel exists for the problem (BF16 forward / backward). */
 #define DDPM_FLAG_CUDA_CORES 0x2u
+/* DDPM_FLAG_TF32X3_FORWARD: FP32 problems compute the forward's generator GEMM on
+ *   TF32 tensor cores as three products of split operands, a = hi + lo with
+ *   hi = tf32(a): hi_y*hi_W + hi_y*lo_W + lo_y*hi_W, accumulated in FP32 (about
+ *   2^-21 relative error per product, within the FP32 forward tolerance); the
+ *   dynamic filter stays IEEE FP32 FMA.  The page lists tf32x3 among the
+ *   variants it tried for the FP32 forward and did not adopt on its card
+ *   (section "已验证但未采用的方案"); without the flag the FP32 forward is the
+ *   page's IEEE FP32 dot.  Applies for K = 3, C a multiple of 4 up to 64, W a
+ *   multiple of 4, halo radius <= 5 and 16-byte aligned tensors; other FP32
+ *   problems run the IEEE kernel.  Ignored for BF16 and under
+ *   DDPM_FLAG_CUDA_CORES. */
+#define DDPM_FLAG_TF32X3_FORWARD 0x4u
 
 typedef struct {
     int B, C, H, W;    /* batch, channels, height, width: all >= 1 */

@@ -232,6 +232,64 @@ def test_tc_forward_repeated_calls_identical():
     assert binding.ddpm_get_device_error() == 0
 
 
+# ------------------------------------- FP32 forward on TF32 tensor cores (3xTF32) --
+
+# Shapes the 3xTF32 forward takes (FP32, K = 3, C % 4 == 0, C <= 64, W % 4 == 0, halo
+# radius <= 5): ragged 64-column tiles, whole-row tiles (W < 64), several images, a
+# single-row image, other dilations, C below one K block.
+TF32X3_SHAPES = [
+    Problem(1, 16, 5, 136, 3),               # two full tiles and an 8-pixel one per row
+    Problem(2, 24, 10, 24, 3),               # whole-row tiles of 5 rows, C = 24
+    Problem(1, 64, 12, 256, 3),              # C = 64, four tiles per row
+    Problem(1, 8, 3, 40, 3, (2, 2, 4)),      # other dilations, image shorter than a tile
+    Problem(2, 64, 7, 200, 3),               # last tile of each row 8 pixels wide
+    Problem(1, 4, 1, 12, 3),                 # one row, C = 4
+    Problem(3, 64, 40, 40, 3),               # several images
+]
+TF32X3 = binding.DDPM_FLAG_TF32X3_FORWARD
+
+
+@pytest.mark.parametrize("p", TF32X3_SHAPES, ids=_id)
+def test_tf32x3_forward_matches_oracle(p):
+    h = make_inputs(p, 720, "float32", grad=False)
+    d = _dev(h)
+    run = lambda: binding.forward(d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations, flags=TF32X3)
+    names = _traced_kernels(run)
+    assert names == ["forward_tf32"], f"expected the 3xTF32 forward, got {names}"
+    out = run()
+    torch.cuda.synchronize()
+    ref = oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations)
+    assert_forward_close(out, ref, "float32", "out (3xTF32)")
+    assert torch.equal(out[:, :p.C].cpu(), h["x"])
+
+
+@pytest.mark.parametrize("p", TF32X3_SHAPES[:5], ids=_id)
+def test_tf32x3_forward_integer_bit_exact(p):
+    """Integer inputs: every operand is exact in TF32 (the lo parts are zero), so the
+    split GEMM and the FP32 filter must match the oracle bit for bit."""
+    h = make_integer_inputs(p, 21, "float32", grad=False)
+    d = _dev(h)
+    out = binding.forward(d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations, flags=TF32X3)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to64(out), oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations))
+
+
+def test_tf32x3_forward_without_bias_and_ineligible_shapes():
+    p = Problem(1, 24, 6, 64, 3)
+    h = make_inputs(p, 721, "float32", grad=False)
+    d = _dev(h)
+    out = binding.forward(d["x"], d["y"], d["weight"], None, p.K, p.dilations, flags=TF32X3)
+    torch.cuda.synchronize()
+    assert_forward_close(out, oracle.forward(h["x"], h["y"], h["weight"], None, p.K, p.dilations), "float32",
+                         "out (3xTF32, no bias)")
+    # K = 5 and W % 4 != 0 keep the IEEE kernel under the flag
+    for q in (Problem(1, 8, 12, 16, 5), Problem(1, 8, 9, 10, 3)):
+        hq = _dev(make_inputs(q, 722, "float32", grad=False))
+        names = _traced_kernels(lambda: binding.forward(hq["x"], hq["y"], hq["weight"], hq["bias"], q.K, q.dilations,
+                                                        flags=TF32X3))
+        assert names == ["forward_simt"], names
+
+
 # ------------------------------------------------ tensor-core backward path --
 
 # + H*W a multiple of 2048 with several images and fewer than eight channel chunks:
@@ -547,6 +605,21 @@ def test_full_size_forward_and_filter(name, dtype):
                              f"{name} {dtype} out (filter)")
     assert torch.equal(out[:, :p.C].cpu(), h["x"])
     assert torch.equal(filt[:, :p.C].cpu(), h["x"])
+    assert binding.ddpm_get_device_error() == 0
+
+
+@pytest.mark.parametrize("name", ["b1_c64_128x128_k3", "b1_c64_256x256_k3"])
+def test_full_size_tf32x3_forward(name):
+    """The FP32 forward with the 3xTF32 generator GEMM, whole tensors, FP32 bar."""
+    p = WORKLOADS[name]
+    h = make_inputs(p, SEEDS[name], "float32", grad=False)
+    d = _dev(h)
+    out = binding.forward(d["x"], d["y"], d["weight"], d["bias"], p.K, p.dilations, flags=TF32X3)
+    torch.cuda.synchronize()
+    with full_size_section():
+        assert_forward_close(out, oracle.forward(h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations),
+                             "float32", f"{name} float32 out (3xTF32)")
+    assert torch.equal(out[:, :p.C].cpu(), h["x"])
     assert binding.ddpm_get_device_error() == 0
 
 
