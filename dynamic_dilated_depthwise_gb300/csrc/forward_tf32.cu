@@ -17,15 +17,19 @@
 // 128-pixel tiles (2 rows x 64 columns, or whole rows when W < 64).  TMEM lane = pixel, so
 // each epilogue thread owns every tap of its pixel.
 //   warp 0      TMA: the group's W rows (once, 128B-swizzled K-major) and each tile's raw
-//               y [64 j][128 px] (one stage)
-//   warp 1      TMEM owner + MMA issuer: per dilation 8 K-steps x 3 products + the bias
-//               step, kind::tf32, M = 128, N = 48, into one of three TMEM regions
+//               y [64 j][128 px], one K-atom of 32 input channels at a time
+//   warp 1      TMEM owner + MMA issuer: per tile 8 K-steps x 3 products + the bias step,
+//               kind::tf32, M = 128, N = 144 (the three dilations' 48 columns side by
+//               side), into one of two TMEM accumulators; the y operand is released one
+//               K-atom (32 input channels) at a time
 //   warp 2      TMA: the x window of each tile, one box per channel (2 buffers)
 //   warps 3-6   splitters: W and bias hi/lo once; per tile y hi/lo, transposed into
 //               128B-swizzled K-major tiles (the MMA reads both operands K-major)
-//   warps 7-14  epilogue: each thread owns one pixel and 2 channels; per dilation it
-//               reads its 18 taps from TMEM and accumulates tap * x in IEEE FP32 FMA,
-//               x read from the window at the tap's offset; results leave by TMA store
+//   warps 7-14  epilogue: each thread owns one pixel and 2 channels; it reads its 54 taps
+//               from TMEM and, per dilation, accumulates tap * x in IEEE FP32 FMA,
+//               x read from the window at the tap's offset; each tile's four output
+//               blocks are staged (two staging buffers) and leave by TMA store after one
+//               epilogue-wide barrier
 #include "bwd_tc_common.cuh"
 #include "tc.cuh"
 
@@ -36,37 +40,39 @@ constexpr int kTile = 128;               // pixels per tile (MMA M)
 constexpr int kKPad = 64;                // generator K (channels of y), zero padded
 constexpr int kCG = 4;                   // output channels per CTA group
 constexpr int kTaps = 9;                 // K = 3
-constexpr int kN = 48;                   // MMA N per dilation: 36 taps padded to a multiple of 16
+constexpr int kN = 48;                   // taps per dilation: 36 padded to a multiple of 16
+constexpr int kNAll = 3 * kN;            // MMA N: the three dilations side by side (144)
 constexpr int kHalo = 8;                 // x window columns left / right of the tile
 constexpr int kWinMax = 960;             // x window positions (TH + 2R) x (TW + 16)
 constexpr int kSplit0 = 3, kSplitWarps = 4;
 constexpr int kEpi0 = kSplit0 + kSplitWarps, kEpiWarps = 8;
 constexpr int kCPT = kCG / (kEpiWarps / 4);   // channels per epilogue thread (2)
 constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;          // two accumulators of kNAll columns
 constexpr int kRawBufs = 2;
 
 // shared memory (bytes from a 1024-aligned base)
-constexpr int kWAtom = kN * 128;                     // one K-atom (32 fp32 of K) of N rows, SW128
-constexpr int kSW = 0;                               // W hi [3 dil][2 K-atoms][N rows x 128 B]
-constexpr int kSWlo = kSW + 6 * kWAtom;              // W lo, same layout
-constexpr int kSYr = kSWlo + 6 * kWAtom;             // raw y [2 halves][64 j][64 px] fp32
+constexpr int kWAtom = kNAll * 128;                  // one K-atom (32 fp32 of K) of the 144 rows, SW128
+constexpr int kSW = 0;                               // W hi [2 K-atoms][dilation][N rows x 128 B]
+constexpr int kSWlo = kSW + 2 * kWAtom;              // W lo, same layout
+constexpr int kSYr = kSWlo + 2 * kWAtom;             // raw y [2 K-atoms][2 pixel halves][32 j][64 px] fp32
 constexpr int kSYhi = kSYr + 2 * 64 * 64 * 4;        // y hi [2 K-atoms][128 rows x 128 B], SW128 K-major
 constexpr int kSYlo = kSYhi + 2 * kTile * 128;       // y lo, same layout
 constexpr int kSOnes = kSYlo + 2 * kTile * 128;      // ones A operand [128 x 8] fp32, no swizzle
-constexpr int kSBias = kSOnes + (kTile / 8) * 256;   // bias B operand 3 x [N x 8] fp32, no swizzle
-constexpr int kBiasTile = (kN / 8) * 256;
-constexpr int kSX = kSBias + 3 * kBiasTile;          // x windows 2 x [CG slots][kWinMax] fp32
+constexpr int kSBias = kSOnes + (kTile / 8) * 256;   // bias B operand [kNAll x 8] fp32, no swizzle
+constexpr int kBiasTile = (kNAll / 8) * 256;
+constexpr int kSX = kSBias + kBiasTile;              // x windows 2 x [CG slots][kWinMax] fp32
 constexpr int kSlot = kWinMax * 4;
 constexpr int kRawBuf = kCG * kSlot;
-constexpr int kSStage = kSX + kRawBufs * kRawBuf;    // output staging 4 blocks x [CG][TH][TW] fp32
+constexpr int kSStage = kSX + kRawBufs * kRawBuf;    // output staging 2 x 4 blocks x [CG][TH][TW] fp32
 constexpr int kStageBlk = kCG * kTile * 4;
-constexpr int kSmemBytes = kSStage + 4 * kStageBlk + 1024;
+constexpr int kStageBuf = 4 * kStageBlk;
+constexpr int kSmemBytes = kSStage + 2 * kStageBuf + 1024;
 static_assert(kWAtom % 1024 == 0 && kSWlo % 1024 == 0 && kSYhi % 1024 == 0 && kSYlo % 1024 == 0,
               "SW128 atoms need 1 KiB alignment");
 static_assert(kSOnes % 128 == 0 && kSBias % 128 == 0 && kSX % 128 == 0 && kSlot % 128 == 0 && kSStage % 128 == 0,
               "operand / TMA alignment");
-static_assert(3 * kN <= kTmemCols && kCG * kTaps <= kN && kN % 16 == 0, "MMA N and TMEM columns");
+static_assert(2 * kNAll <= kTmemCols && kCG * kTaps <= kN && kNAll % 16 == 0 && kNAll <= 256, "MMA N, TMEM columns");
 static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory");
 
 struct Tf32Params {
@@ -110,8 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB-aligned base by pointer arithmetic on the shared array (accesses stay shared-space)
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t bar_w, bar_wsplit, bar_yraw_full, bar_yraw_empty, bar_ysplit_full, bar_ysplit_empty,
-        bar_acc_full[3], bar_acc_empty[3], bar_raw_full[kRawBufs], bar_raw_empty[kRawBufs], bar_done;
+    __shared__ uint64_t bar_w, bar_wsplit, bar_yraw_full[2], bar_yraw_empty[2], bar_ysplit_full[2], bar_ysplit_empty[2],
+        bar_acc_full[2], bar_acc_empty[2], bar_raw_full[kRawBufs], bar_raw_empty[kRawBufs], bar_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -126,13 +132,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         abort_flag = 0;
         mbar_init(&bar_w, 1);
         mbar_init(&bar_wsplit, kSplitWarps);
-        mbar_init(&bar_yraw_full, 1);
-        mbar_init(&bar_yraw_empty, kSplitWarps);
-        mbar_init(&bar_ysplit_full, kSplitWarps);
-        mbar_init(&bar_ysplit_empty, 1);
-        for (int dd = 0; dd < 3; ++dd) {
-            mbar_init(&bar_acc_full[dd], 1);
-            mbar_init(&bar_acc_empty[dd], kEpiWarps);
+        for (int kh = 0; kh < 2; ++kh) {
+            mbar_init(&bar_yraw_full[kh], 1);
+            mbar_init(&bar_yraw_empty[kh], kSplitWarps);
+            mbar_init(&bar_ysplit_full[kh], kSplitWarps);
+            mbar_init(&bar_ysplit_empty[kh], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar_acc_full[b], 1);
+            mbar_init(&bar_acc_empty[b], kEpiWarps);
         }
         for (int s = 0; s < kRawBufs; ++s) {
             mbar_init(&bar_raw_full[s], 1);
@@ -152,17 +160,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float*>(sm + kSOnes + (m / 8) * 256 + (k / 4) * 128 + (m % 8) * 16 + (k % 4) * 4) =
                 k < 2 ? 1.0f : 0.0f;
         }
-        for (int i = et; i < 3 * kN * 8; i += 32 * kEpiWarps) {
-            const int dd = i / (kN * 8), rem = i % (kN * 8), n = rem / 8, k = rem % 8;
-            const long long o = (long long)(dd * C + c0) * kTaps + n;
+        for (int i = et; i < kNAll * 8; i += 32 * kEpiWarps) {
+            const int n = i / 8, k = i % 8, dd = n / kN, nl = n % kN;
+            const long long o = (long long)(dd * C + c0) * kTaps + nl;
             float v = 0.0f;
-            if (k < 2 && P.bias != nullptr && n < kCG * kTaps && o < P.d.O) {
+            if (k < 2 && P.bias != nullptr && nl < kCG * kTaps && o < P.d.O) {
                 const float b = P.bias[o];
                 const float hi = tf32_hi(b);
                 v = k == 0 ? hi : b - hi;
             }
-            *reinterpret_cast<float*>(sm + kSBias + dd * kBiasTile + (n / 8) * 256 + (k / 4) * 128 + (n % 8) * 16 +
-                                      (k % 4) * 4) = v;
+            *reinterpret_cast<float*>(sm + kSBias + (n / 8) * 256 + (k / 4) * 128 + (n % 8) * 16 + (k % 4) * 4) = v;
         }
         fence_proxy_async_smem();
     }
@@ -177,25 +184,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tmY);
             prefetch_tmap(&tmW);
-            mbar_arrive_expect_tx(&bar_w, 6 * kWAtom);
+            mbar_arrive_expect_tx(&bar_w, 2 * kWAtom);
             for (int dd = 0; dd < 3; ++dd)
                 for (int kh = 0; kh < 2; ++kh)
-                    tma_load_2d(sm + kSW + (dd * 2 + kh) * kWAtom, &tmW, &bar_w, kh * 32, (dd * C + c0) * kTaps);
+                    tma_load_2d(sm + kSW + kh * kWAtom + dd * kN * 128, &tmW, &bar_w, kh * 32, (dd * C + c0) * kTaps);
+            // raw y arrives one K-atom (32 input channels) at a time, so the next tile's first
+            // atom is on its way while the splitters still work on this tile's second
             const int half_step = P.TW == 64 ? P.d.W : 64;
             int issued = 0;
-            for (int i = 0; i < n_my; ++i) {
+            bool ok = true;
+            for (int i = 0; i < n_my && ok; ++i) {
                 const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
-                if (!mbar_wait(&bar_yraw_empty, (i & 1) ^ 1, P.err, abort_v)) break;
                 const int pb = tcd.h0 * P.d.W + tcd.w0;
-                mbar_arrive_expect_tx(&bar_yraw_full, 2 * 64 * 64 * 4);
-                tma_load_3d(sm + kSYr, &tmY, &bar_yraw_full, pb, 0, tcd.b);
-                tma_load_3d(sm + kSYr + 64 * 64 * 4, &tmY, &bar_yraw_full, pb + half_step, 0, tcd.b);
-                issued = i + 1;
+                for (int kh = 0; kh < 2; ++kh) {
+                    if (!mbar_wait(&bar_yraw_empty[kh], (i & 1) ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = sm + kSYr + kh * 2 * 32 * 64 * 4;
+                    mbar_arrive_expect_tx(&bar_yraw_full[kh], 2 * 32 * 64 * 4);
+                    tma_load_3d(dst, &tmY, &bar_yraw_full[kh], pb, 32 * kh, tcd.b);
+                    tma_load_3d(dst + 32 * 64 * 4, &tmY, &bar_yraw_full[kh], pb + half_step, 32 * kh, tcd.b);
+                    issued = 2 * i + kh + 1;
+                }
             }
             // drain: every copy this thread started lands before shared memory is released
             int never = 0;
             mbar_wait(&bar_w, 0, P.err, &never);
-            if (issued > 0) mbar_wait(&bar_yraw_full, (issued - 1) & 1, P.err, &never);
+            for (int n = issued > 2 ? issued - 2 : 0; n < issued; ++n)
+                mbar_wait(&bar_yraw_full[n & 1], (n >> 1) & 1, P.err, &never);
         }
     } else if (warp == 2) {
         // ------------------------------------------------------- TMA producer: x windows
@@ -222,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             bool ok = mbar_wait(&bar_wsplit, 0, P.err, abort_v);
-            const uint32_t idesc = instr_desc(2, 0, 0, kTile, kN);   // TF32, both operands K-major
+            const uint32_t idesc = instr_desc(2, 0, 0, kTile, kNAll);   // TF32, both operands K-major
             const uint64_t yhi = smem_desc(smem_u32(sm + kSYhi), 16, 1024, kSwizzle128B);
             const uint64_t ylo = smem_desc(smem_u32(sm + kSYlo), 16, 1024, kSwizzle128B);
             const uint64_t whi = smem_desc(smem_u32(sm + kSW), 16, 1024, kSwizzle128B);
@@ -230,30 +247,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ones = smem_desc(smem_u32(sm + kSOnes), 128, 256, kSwizzleNone);
             const uint64_t bias = smem_desc(smem_u32(sm + kSBias), 128, 256, kSwizzleNone);
             for (int i = 0; ok && i < n_my; ++i) {
-                if (!mbar_wait(&bar_ysplit_full, i & 1, P.err, abort_v)) break;
+                const int tb = i & 1;                  // TMEM accumulator of this tile
+                if (!mbar_wait(&bar_acc_empty[tb], ((i >> 1) & 1) ^ 1, P.err, abort_v)) break;
                 tc_fence_after();
-                for (int dd = 0; dd < 3 && ok; ++dd) {
-                    if (!mbar_wait(&bar_acc_empty[dd], (i & 1) ^ 1, P.err, abort_v)) {
+                const uint32_t dt = tmem + tb * kNAll;
+                // K-atom by K-atom, so that the splitters refill the first atom for the next
+                // tile while the MMAs read the second
+                for (int kh = 0; kh < 2 && ok; ++kh) {
+                    if (!mbar_wait(&bar_ysplit_full[kh], i & 1, P.err, abort_v)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t dt = tmem + dd * kN;
 #pragma unroll
-                    for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t ya = (uint32_t)(kh * kTile * 128 + kk * 32);
-                            const uint32_t wa = (uint32_t)((dd * 2 + kh) * kWAtom + kk * 32);
-                            mma_tf32(dt, desc_advance(yhi, ya), desc_advance(whi, wa), idesc, (kh | kk) ? 1u : 0u);
-                            mma_tf32(dt, desc_advance(yhi, ya), desc_advance(wlo, wa), idesc, 1u);
-                            mma_tf32(dt, desc_advance(ylo, ya), desc_advance(whi, wa), idesc, 1u);
-                        }
-                    mma_tf32(dt, ones, desc_advance(bias, (uint32_t)(dd * kBiasTile)), idesc, 1u);
-                    mma_commit(&bar_acc_full[dd]);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t ya = (uint32_t)(kh * kTile * 128 + kk * 32);
+                        const uint32_t wa = (uint32_t)(kh * kWAtom + kk * 32);
+                        mma_tf32(dt, desc_advance(yhi, ya), desc_advance(whi, wa), idesc, (kh | kk) ? 1u : 0u);
+                        mma_tf32(dt, desc_advance(yhi, ya), desc_advance(wlo, wa), idesc, 1u);
+                        mma_tf32(dt, desc_advance(ylo, ya), desc_advance(whi, wa), idesc, 1u);
+                    }
+                    mma_commit(&bar_ysplit_empty[kh]);
                 }
                 if (!ok) break;
-                mma_commit(&bar_ysplit_empty);
+                mma_tf32(dt, ones, bias, idesc, 1u);
+                mma_commit(&bar_acc_full[tb]);
             }
             // all issued MMAs retire before TMEM is released
             mma_commit(&bar_done);
@@ -266,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = mbar_wait(&bar_w, 0, P.err, abort_v);
         if (ok) {
             // W hi in place, W lo beside it (same swizzled offsets: the split is elementwise)
-            for (int i = st; i < 6 * kWAtom / 16; i += nst) {
+            for (int i = st; i < 2 * kWAtom / 16; i += nst) {
                 float4* ph = reinterpret_cast<float4*>(sm + kSW) + i;
                 float4* pl = reinterpret_cast<float4*>(sm + kSWlo) + i;
                 const float4 v = *ph;
@@ -283,33 +301,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_wsplit);
         for (int i = 0; ok && i < n_my; ++i) {
-            if (!mbar_wait(&bar_yraw_full, i & 1, P.err, abort_v) ||
-                !mbar_wait(&bar_ysplit_empty, (i & 1) ^ 1, P.err, abort_v)) {
-                ok = false;
-                break;
-            }
             // unit = (pixel px, group of 4 input channels jc): a warp covers 32 consecutive
             // pixels of one jc, so its raw reads are 128 contiguous bytes per channel and its
-            // 16-byte stores touch each bank once per 8 rows
-            for (int u = st; u < kTile * 16; u += nst) {
-                const int px = u % kTile, jc = u / kTile;
-                const float* raw = reinterpret_cast<const float*>(sm + kSYr + (px / 64) * 64 * 64 * 4) + (px % 64);
-                float4 h, l;
-                const float y0 = raw[(4 * jc + 0) * 64], y1 = raw[(4 * jc + 1) * 64];
-                const float y2 = raw[(4 * jc + 2) * 64], y3 = raw[(4 * jc + 3) * 64];
-                h.x = tf32_hi(y0); l.x = y0 - h.x;
-                h.y = tf32_hi(y1); l.y = y1 - h.y;
-                h.z = tf32_hi(y2); l.z = y2 - h.z;
-                h.w = tf32_hi(y3); l.w = y3 - h.w;
-                const int off = (jc / 8) * kTile * 128 + (px / 8) * 1024 + (px % 8) * 128 + (((jc % 8) ^ (px % 8)) << 4);
-                *reinterpret_cast<float4*>(sm + kSYhi + off) = h;
-                *reinterpret_cast<float4*>(sm + kSYlo + off) = l;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bar_yraw_empty);
-                mbar_arrive(&bar_ysplit_full);
+            // 16-byte stores touch each bank once per 8 rows.  K-atom kh holds jc 8kh .. 8kh+7.
+            for (int kh = 0; kh < 2 && ok; ++kh) {
+                if (!mbar_wait(&bar_yraw_full[kh], i & 1, P.err, abort_v) ||
+                    !mbar_wait(&bar_ysplit_empty[kh], (i & 1) ^ 1, P.err, abort_v)) {
+                    ok = false;
+                    break;
+                }
+                for (int u = st; u < kTile * 8; u += nst) {
+                    const int px = u % kTile, jc = kh * 8 + u / kTile;
+                    // raw atom kh: [pixel half][32 j][64 px]; local channel jl = 4 * (jc % 8)
+                    const float* raw = reinterpret_cast<const float*>(sm + kSYr + kh * 2 * 32 * 64 * 4 +
+                                                                      (px / 64) * 32 * 64 * 4) + (px % 64);
+                    const int jl = 4 * (jc % 8);
+                    float4 h, l;
+                    const float y0 = raw[(jl + 0) * 64], y1 = raw[(jl + 1) * 64];
+                    const float y2 = raw[(jl + 2) * 64], y3 = raw[(jl + 3) * 64];
+                    h.x = tf32_hi(y0); l.x = y0 - h.x;
+                    h.y = tf32_hi(y1); l.y = y1 - h.y;
+                    h.z = tf32_hi(y2); l.z = y2 - h.z;
+                    h.w = tf32_hi(y3); l.w = y3 - h.w;
+                    const int off = kh * kTile * 128 + (px / 8) * 1024 + (px % 8) * 128 + (((jc % 8) ^ (px % 8)) << 4);
+                    *reinterpret_cast<float4*>(sm + kSYhi + off) = h;
+                    *reinterpret_cast<float4*>(sm + kSYlo + off) = l;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bar_ysplit_full[kh]);
+                    mbar_arrive(&bar_yraw_empty[kh]);
+                }
             }
         }
     } else {
@@ -324,65 +347,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rr = in_tile ? s / P.TW : 0, cc = in_tile ? s % P.TW : 0;
         const int WC = P.WC;
         const int center = (rr + P.R) * WC + cc + kHalo;
-        float* stage0 = reinterpret_cast<float*>(sm + kSStage) + cl0 * tpix + (in_tile ? s : 0);
+        // this thread's element of staging buffer 0, block 0 (buffer sb at + sb * kStageBuf)
+        const int st_off = cl0 * tpix + (in_tile ? s : 0);
         int buf = 0, bph = 0;
         bool ok = true;
-        auto flush_block = [&](int blk, const TileCoord& tcd) {
-            fence_proxy_async_smem();
-            if (leader) bulk_wait_read<2>();
-            named_bar<32 * kEpiWarps>(1);
-            if (leader && ok) {
-                const int cbase = (blk == 0 ? 0 : blk * C) + c0;
-                tma_store_4d(&tmO, sm + kSStage + blk * kStageBlk, tcd.w0, tcd.h0, cbase, tcd.b);
-                bulk_commit();
-            }
-        };
         for (int i = 0; i < n_my; ++i) {
             const TileCoord tcd = tile_coord(P, cta_in_group + i * P.ctas_per_group);
+            const int sb = i & 1;                // staging buffer: the stores of tile i - 1 may still read the other
+            float* stage0 = reinterpret_cast<float*>(sm + kSStage + sb * kStageBuf) + st_off;
             const float* xw = reinterpret_cast<const float*>(sm + kSX + buf * kRawBuf + cl0 * kSlot) + center;
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_raw_full[buf], bph, P.err, abort_v));
-            // channels c0 .. c0+CG-1 of the output are x itself
-            if (ok && in_tile) {
-#pragma unroll
-                for (int c = 0; c < kCPT; ++c) stage0[c * tpix] = xw[c * (kSlot / 4)];
-            }
-            flush_block(0, tcd);
-            for (int dd = 0; dd < 3; ++dd) {
-                if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[dd], i & 1, P.err, abort_v));
-                if (!ok) {
-                    flush_block(1 + dd, tcd);
-                    continue;
-                }
+            // all three dilations' taps of this thread, then the accumulator goes back to the MMA
+            const int tb = i & 1;
+            uint32_t t[3][kCPT * kTaps];
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[tb], (i >> 1) & 1, P.err, abort_v));
+            if (ok) {
                 tc_fence_after();
-                uint32_t t[kCPT * kTaps];
-                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + dd * kN + cl0 * kTaps;
-                DDPM_TMEM_LD_X16(ta, t);
-                DDPM_TMEM_LD_X2(ta + 16, (t + 16));
+#pragma unroll
+                for (int dd = 0; dd < 3; ++dd) {
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * kNAll + dd * kN + cl0 * kTaps;
+                    DDPM_TMEM_LD_X16(ta, t[dd]);
+                    DDPM_TMEM_LD_X2(ta + 16, (t[dd] + 16));
+                }
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar_acc_empty[dd]);
-                const int dil = dil_of(P.d, dd);
-                float acc[kCPT];
+                if (lane == 0) mbar_arrive(&bar_acc_empty[tb]);
+            }
+            if (ok && in_tile) {
+                // block 0: channels c0 .. c0+CG-1 of the output are x itself
 #pragma unroll
-                for (int c = 0; c < kCPT; ++c) acc[c] = 0.0f;
+                for (int c = 0; c < kCPT; ++c) stage0[c * tpix] = xw[c * (kSlot / 4)];
 #pragma unroll
-                for (int k = 0; k < kTaps; ++k) {
-                    const int off = ((k / 3 - 1) * WC + (k % 3 - 1)) * dil;
+                for (int dd = 0; dd < 3; ++dd) {
+                    const int dil = dil_of(P.d, dd);
+                    float acc[kCPT];
 #pragma unroll
-                    for (int c = 0; c < kCPT; ++c)
-                        acc[c] = fmaf(__uint_as_float(t[c * kTaps + k]), xw[c * (kSlot / 4) + off], acc[c]);
-                }
-                if (in_tile) {
+                    for (int c = 0; c < kCPT; ++c) acc[c] = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < kTaps; ++k) {
+                        const int off = ((k / 3 - 1) * WC + (k % 3 - 1)) * dil;
+#pragma unroll
+                        for (int c = 0; c < kCPT; ++c)
+                            acc[c] = fmaf(__uint_as_float(t[dd][c * kTaps + k]), xw[c * (kSlot / 4) + off], acc[c]);
+                    }
                     float* sa = stage0 + (1 + dd) * (kStageBlk / 4);
 #pragma unroll
                     for (int c = 0; c < kCPT; ++c) sa[c * tpix] = acc[c];
                 }
-                if (dd == 2) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar_raw_empty[buf]);
+            }
+            // the window has been read for the last time
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_raw_empty[buf]);
+            // one hand-off per tile: the leader first makes sure the stores of tile i - 1 have
+            // read their staging buffer (the one tile i + 1 writes next), then every epilogue
+            // thread's values are in place and the four blocks leave by TMA
+            fence_proxy_async_smem();
+            if (leader) bulk_wait_read<0>();
+            named_bar<32 * kEpiWarps>(1);
+            if (leader && ok) {
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk) {
+                    const int cbase = (blk == 0 ? 0 : blk * C) + c0;
+                    tma_store_4d(&tmO, sm + kSStage + sb * kStageBuf + blk * kStageBlk, tcd.w0, tcd.h0, cbase, tcd.b);
                 }
-                flush_block(1 + dd, tcd);
+                bulk_commit();
             }
             if (++buf == kRawBufs) {
                 buf = 0;
@@ -456,7 +485,7 @@ cudaError_t launch_forward_tf32(const Dims& d, const void* x, const void* y, con
     CUtensorMap tmY, tmW, tmX, tmO;
     const cuuint64_t dimY[3] = {(cuuint64_t)d.HW, (cuuint64_t)d.C, (cuuint64_t)d.B};
     const cuuint64_t strY[2] = {(cuuint64_t)d.HW * 4, (cuuint64_t)d.HW * d.C * 4};
-    const cuuint32_t boxY[3] = {64, (cuuint32_t)kKPad, 1};
+    const cuuint32_t boxY[3] = {64, 32, 1};   // 64 pixels x one K-atom of input channels
     const cuuint32_t one3[3] = {1, 1, 1};
     if (enc(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(y), dimY, strY, boxY, one3,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -465,7 +494,7 @@ cudaError_t launch_forward_tf32(const Dims& d, const void* x, const void* y, con
     // W [O, C] fp32: boxes of 32 input channels (one 128-byte swizzle row) x N rows
     const cuuint64_t dimW[2] = {(cuuint64_t)d.C, (cuuint64_t)d.O};
     const cuuint64_t strW[1] = {(cuuint64_t)d.C * 4};
-    const cuuint32_t boxW[2] = {32, (cuuint32_t)kN};
+    const cuuint32_t boxW[2] = {32, (cuuint32_t)kN};   // one dilation's rows of one K-atom
     const cuuint32_t one2[2] = {1, 1};
     if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(w), dimW, strW, boxW, one2,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
