@@ -87,8 +87,10 @@ constexpr size_t kMaxSmem = 227 * 1024;
 size_t elem_size(int dtype) { return dtype == DDPM_BFLOAT16 ? 2 : 4; }
 
 // Workspace layout of ddpm_backward: the FP32 dW/dbias partial sums (the minimum
-// a caller must supply), then -- when the workspace is large enough -- the
-// channel-chunked copies of y and grad that the packed dX kernel reads.
+// a caller must supply), then -- when the workspace is large enough -- for BF16
+// problems the channel-chunked copies of y and grad that the packed dX kernel
+// reads, for FP32 problems with TF32 contractions the rearranged weight that the
+// TF32 dY kernel reads.
 size_t packed_offset(const Dims& d) { return (ddpm::backward_simt_workspace(d) + 255) & ~size_t(255); }
 
 ddpm_status validate(const ddpm_problem* p, Dims* d) {
@@ -203,9 +205,12 @@ ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* by
     Dims d;
     DDPM_TRY(validate(problem, &d));
     if (bytes == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
-    *bytes = ddpm::bwd_dx_packed_shape_ok(d)
-                 ? packed_offset(d) + ddpm::bwd_dx_packed_bytes(d)
-                 : ddpm::backward_simt_workspace(d);
+    if (ddpm::bwd_dx_packed_shape_ok(d))
+        *bytes = packed_offset(d) + ddpm::bwd_dx_packed_bytes(d);
+    else if (ddpm::bwd_dy_tf32_shape_ok(d))
+        *bytes = packed_offset(d) + ddpm::bwd_dy_tf32_wt_bytes(d);
+    else
+        *bytes = ddpm::backward_simt_workspace(d);
     return DDPM_OK;
 }
 
@@ -237,7 +242,9 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
         const size_t poff = packed_offset(d);
         const bool packed = ddpm::bwd_dx_packed_eligible(d, grad_out, y, weight) &&
                             workspace_bytes >= poff + ddpm::bwd_dx_packed_bytes(d);
-        const size_t part_bytes = packed ? poff : workspace_bytes;
+        const bool dy_tf32 = ddpm::bwd_dy_tf32_eligible(d, grad_out, x, weight, dy) &&
+                             workspace_bytes >= poff + ddpm::bwd_dy_tf32_wt_bytes(d);
+        const size_t part_bytes = (packed || dy_tf32) ? poff : workspace_bytes;
         // dX on the caller's stream, dY and dW (+ reduce) on the two side streams: the
         // pieces share only inputs, and each one's last partial wave of CTAs leaves SMs
         // that the others fill.  While kernels are traced the pieces run one after
@@ -262,6 +269,8 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
         if (e == cudaSuccess) {
             if (ddpm::bwd_dy_tc_eligible(d, grad_out, x, weight))
                 e = ddpm::launch_bwd_dy_tc(d, grad_out, x, weight, dy, s_dy);
+            else if (dy_tf32)
+                e = ddpm::launch_bwd_dy_tf32(d, grad_out, x, weight, dy, static_cast<char*>(workspace) + poff, s_dy);
             else
                 e = ddpm::launch_bwd_dy_simt(d, grad_out, x, weight, dy, s_dy);
         }

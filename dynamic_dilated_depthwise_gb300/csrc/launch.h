@@ -27,7 +27,8 @@ enum KernelId : int {
     kKFilterBwdDx = 13,
     kKFilterBwdDtaps = 14,
     kKForwardTf32 = 15,
-    kKNumKernels = 16
+    kKBwdDyTf32 = 16,
+    kKNumKernels = 17
 };
 
 // Tracing hooks around each launch (cheap no-ops while tracing is off).
@@ -125,6 +126,15 @@ bool bwd_dx_packed_eligible(const Dims& d, const void* g, const void* y, const v
 size_t bwd_dx_packed_bytes(const Dims& d);
 cudaError_t launch_bwd_dx_packed(const Dims& d, const void* g, const void* y, const void* w, const void* bias,
                                  void* dx, void* packed, cudaStream_t s);
+
+// dY of FP32 problems on TF32 tensor cores (DDPM_FLAG_TF32_BACKWARD): K = 3, C a multiple
+// of 16 up to 64.  Needs bwd_dy_tf32_wt_bytes(d) bytes of workspace (16-byte aligned) for
+// the rearranged weight, which the launch writes first.
+bool bwd_dy_tf32_shape_ok(const Dims& d);   // the problem alone (sizes the workspace)
+bool bwd_dy_tf32_eligible(const Dims& d, const void* g, const void* x, const void* w, const void* dy);
+size_t bwd_dy_tf32_wt_bytes(const Dims& d);
+cudaError_t launch_bwd_dy_tf32(const Dims& d, const void* g, const void* x, const void* w, void* dy, void* wt,
+                               cudaStream_t s);
 
 // dY on tcgen05 tensor cores (same shapes as the dW kernel).
 bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w);

@@ -69,8 +69,10 @@ typedef enum { DDPM_FLOAT32 = 0, DDPM_BFLOAT16 = 1 } ddpm_dtype;
  *   TF32 tensor cores (the page allows TF32 for FP32 backward reductions and
  *   recompute, never for the forward).  With it the dW/dbias partial sums run
  *   on tensor cores (TF32 operands, FP32 accumulation) for K = 3, C <= 64, W a
- *   multiple of 4, dilations <= 6 and 16-byte aligned tensors; dX and dY stay
- *   IEEE FP32.  Ignored for BF16 and under DDPM_FLAG_CUDA_CORES. */
+ *   multiple of 4, dilations <= 6 and 16-byte aligned tensors, and so does dY
+ *   where C is also a multiple of 16 and the workspace holds the rearranged
+ *   weight (ddpm_backward_workspace_size counts it); dX stays IEEE FP32.
+ *   Ignored for BF16 and under DDPM_FLAG_CUDA_CORES. */
 #define DDPM_FLAG_TF32_BACKWARD 0x1u
 /* DDPM_FLAG_CUDA_CORES: run the CUDA-core (FFMA) kernels even where a
  *   tensor-core kernel exists for the problem (BF16 forward / backward). */
@@ -148,9 +150,10 @@ DDPM_API ddpm_status ddpm_filter_pregenerated_backward(const ddpm_problem* probl
  * image size (7.2 MB for C = 64, K = 3).  For BF16 problems whose dX runs on the
  * packed tensor-core kernel, the returned size also covers channel-chunked
  * copies of y and of the three dilation blocks of grad (4 * B * C * H * W bf16
- * elements, which does grow with the image); ddpm_backward accepts any
- * workspace of at least the partials' size and then stages dX's operands inside
- * the kernel instead.
+ * elements, which does grow with the image); for FP32 problems whose dY runs on
+ * TF32 tensor cores, a rearranged copy of the weight (27 * C * C FP32 values).
+ * ddpm_backward accepts any workspace of at least the partials' size and then
+ * stages dX's operands inside the kernel and runs an FP32 dY on CUDA cores.
  */
 DDPM_API ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* bytes);
 

@@ -430,6 +430,8 @@ TF32_SHAPES = [
     Problem(1, 64, 12, 64, 3),               # C = 64 as in the main workloads
     Problem(1, 12, 7, 40, 3, (2, 2, 4)),     # other dilations
     Problem(3, 8, 5, 68, 3, (1, 6, 2)),      # halo radius 6, several images
+    Problem(2, 32, 9, 36, 3, (1, 6, 2)),     # TF32 dY: ragged 4 x 32 tiles, halo radius 6, two images
+    Problem(1, 48, 6, 64, 3),                # TF32 dY with N = 48
 ]
 
 
@@ -440,14 +442,19 @@ def test_tf32_backward_matches_oracle(p):
     flags = binding.DDPM_FLAG_TF32_BACKWARD
     names = _traced_kernels(lambda: run_backward(d, p, flags=flags))
     assert "bwd_dw_tf32" in names and "bwd_dw_partial_simt" not in names, names
+    tf32_dy = p.C % 16 == 0
+    assert ("bwd_dy_tf32" in names) == tf32_dy and ("bwd_dy_simt" in names) != tf32_dy, names
     got = run_backward(d, p, flags=flags)
     ieee = run_backward(d, p)
     torch.cuda.synchronize()
     ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=False)
     for name, a, want in zip(("dx", "dy", "dW", "dbias"), got, ref):
         assert_grad_close(a, want, "float32", name)
-    # the flag changes only the dW / dbias contraction
-    assert torch.equal(got[0], ieee[0]) and torch.equal(got[1], ieee[1])
+        assert_grad_close(ieee[("dx", "dy", "dW", "dbias").index(name)], want, "float32", name + " (IEEE)")
+    # the flag leaves dX in IEEE FP32, and dY too where the TF32 dY kernel does not apply
+    assert torch.equal(got[0], ieee[0])
+    if not tf32_dy:
+        assert torch.equal(got[1], ieee[1])
 
 
 @pytest.mark.parametrize("p", TF32_SHAPES, ids=_id)
