@@ -148,22 +148,6 @@ __device__ __forceinline__ void lds_slots(uint32_t addr, unsigned short* v, std:
     ((v[I] = tc::lds_u16<I * SLOT>(addr)), ...);
 }
 
-// n consecutive TMEM columns of this warp's lane quadrant into r[0..n)
-template <int NCOL>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
-#pragma unroll
-    for (int c = 0; c + 16 <= NCOL; c += 16) DDPM_TMEM_LD_X16(taddr + c, (r + c));
-    constexpr int rem = NCOL % 16;
-    constexpr int b8 = NCOL - rem;
-    if constexpr ((rem & 8) != 0) DDPM_TMEM_LD_X8(taddr + b8, (r + b8));
-    constexpr int b4 = b8 + (rem & 8);
-    if constexpr ((rem & 4) != 0) DDPM_TMEM_LD_X4(taddr + b4, (r + b4));
-    constexpr int b2 = b4 + (rem & 4);
-    if constexpr ((rem & 2) != 0) DDPM_TMEM_LD_X2(taddr + b2, (r + b2));
-    constexpr int b1 = b2 + (rem & 2);
-    if constexpr ((rem & 1) != 0) DDPM_TMEM_LD_X1(taddr + b1, (r + b1));
-}
-
 template <int K>
 __global__ void __launch_bounds__(FwdLayout<K>::kThreads, FwdLayout<K>::kCtasPerSm)
     forward_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmW,

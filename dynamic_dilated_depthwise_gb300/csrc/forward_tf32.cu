@@ -10,23 +10,24 @@
 // Each FP32 operand a is split as hi = tf32(a) (round to nearest) and lo = a - hi (exact),
 // and the GEMM is accumulated in FP32 as hi_y*hi_W + hi_y*lo_W + lo_y*hi_W: the neglected
 // lo*lo term and the TF32 reading of lo leave a relative error of about 2^-21 per product.
-// The bias enters as one more K step (a ones column against bias_hi and bias_lo).
+// The epilogue adds the bias to each tap in FP32.
 //
 // GB300 design (the FP32 counterpart of forward_tc.cu).  A persistent CTA (one per SM)
-// owns CG output channels (CG = 4, N = 48 taps per dilation, 36 of them real) and walks
-// 128-pixel tiles (2 rows x 64 columns, or whole rows when W < 64).  TMEM lane = pixel, so
-// each epilogue thread owns every tap of its pixel.
+// owns CG output channels (K = 3: CG = 4, 36 taps per dilation in 48 rows; K = 5: CG = 2,
+// 50 taps in 56 rows) and walks 128-pixel tiles (2 rows x 64 columns, or whole rows when
+// W < 64).  TMEM lane = pixel, so each epilogue thread owns every tap of its pixel.
 //   warp 0      TMA: the group's W rows (once, 128B-swizzled K-major) and each tile's raw
 //               y [64 j][128 px], one K-atom of 32 input channels at a time
-//   warp 1      TMEM owner + MMA issuer: per tile 8 K-steps x 3 products + the bias step,
-//               kind::tf32, M = 128, N = 144 (the three dilations' 48 columns side by
-//               side), into one of two TMEM accumulators; the y operand is released one
-//               K-atom (32 input channels) at a time
+//   warp 1      TMEM owner + MMA issuer: per tile 8 K-steps x 3 products, kind::tf32,
+//               M = 128, N = the three dilations' rows side by side (144 for K = 3, 176
+//               for K = 5), into one of two TMEM accumulators; the y operand is released
+//               one K-atom (32 input channels) at a time
 //   warp 2      TMA: the x window of each tile, one box per channel (2 buffers)
-//   warps 3-6   splitters: W and bias hi/lo once; per tile y hi/lo, transposed into
+//   warps 3-6   splitters: W hi/lo once; per tile y hi/lo, transposed into
 //               128B-swizzled K-major tiles (the MMA reads both operands K-major)
-//   warps 7-14  epilogue: each thread owns one pixel and 2 channels; it reads its 54 taps
-//               from TMEM and, per dilation, accumulates tap * x in IEEE FP32 FMA,
+//   warps 7-14  epilogue: each thread owns one pixel and CG/2 channels; it reads their
+//               taps of the three dilations from TMEM, adds the bias and, per dilation,
+//               accumulates tap * x in IEEE FP32 FMA,
 //               x read from the window at the tap's offset; each tile's four output
 //               blocks are staged (two staging buffers) and leave by TMA store after one
 //               epilogue-wide barrier
@@ -38,42 +39,49 @@ namespace {
 
 constexpr int kTile = 128;               // pixels per tile (MMA M)
 constexpr int kKPad = 64;                // generator K (channels of y), zero padded
-constexpr int kCG = 4;                   // output channels per CTA group
-constexpr int kTaps = 9;                 // K = 3
-constexpr int kN = 48;                   // taps per dilation: 36 padded to a multiple of 16
-constexpr int kNAll = 3 * kN;            // MMA N: the three dilations side by side (144)
-constexpr int kHalo = 8;                 // x window columns left / right of the tile
-constexpr int kWinMax = 960;             // x window positions (TH + 2R) x (TW + 16)
 constexpr int kSplit0 = 3, kSplitWarps = 4;
 constexpr int kEpi0 = kSplit0 + kSplitWarps, kEpiWarps = 8;
-constexpr int kCPT = kCG / (kEpiWarps / 4);   // channels per epilogue thread (2)
 constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
-constexpr int kTmemCols = 512;          // two accumulators of kNAll columns
+constexpr int kTmemCols = 512;           // two accumulators of NALL columns
 constexpr int kRawBufs = 2;
 
-// shared memory (bytes from a 1024-aligned base)
-constexpr int kWAtom = kNAll * 128;                  // one K-atom (32 fp32 of K) of the 144 rows, SW128
-constexpr int kSW = 0;                               // W hi [2 K-atoms][dilation][N rows x 128 B]
-constexpr int kSWlo = kSW + 2 * kWAtom;              // W lo, same layout
-constexpr int kSYr = kSWlo + 2 * kWAtom;             // raw y [2 K-atoms][2 pixel halves][32 j][64 px] fp32
-constexpr int kSYhi = kSYr + 2 * 64 * 64 * 4;        // y hi [2 K-atoms][128 rows x 128 B], SW128 K-major
-constexpr int kSYlo = kSYhi + 2 * kTile * 128;       // y lo, same layout
-constexpr int kSOnes = kSYlo + 2 * kTile * 128;      // ones A operand [128 x 8] fp32, no swizzle
-constexpr int kSBias = kSOnes + (kTile / 8) * 256;   // bias B operand [kNAll x 8] fp32, no swizzle
-constexpr int kBiasTile = (kNAll / 8) * 256;
-constexpr int kSX = kSBias + kBiasTile;              // x windows 2 x [CG slots][kWinMax] fp32
-constexpr int kSlot = kWinMax * 4;
-constexpr int kRawBuf = kCG * kSlot;
-constexpr int kSStage = kSX + kRawBufs * kRawBuf;    // output staging 2 x 4 blocks x [CG][TH][TW] fp32
-constexpr int kStageBlk = kCG * kTile * 4;
-constexpr int kStageBuf = 4 * kStageBlk;
-constexpr int kSmemBytes = kSStage + 2 * kStageBuf + 1024;
-static_assert(kWAtom % 1024 == 0 && kSWlo % 1024 == 0 && kSYhi % 1024 == 0 && kSYlo % 1024 == 0,
-              "SW128 atoms need 1 KiB alignment");
-static_assert(kSOnes % 128 == 0 && kSBias % 128 == 0 && kSX % 128 == 0 && kSlot % 128 == 0 && kSStage % 128 == 0,
-              "operand / TMA alignment");
-static_assert(2 * kNAll <= kTmemCols && kCG * kTaps <= kN && kNAll % 16 == 0 && kNAll <= 256, "MMA N, TMEM columns");
-static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory");
+// Per-kernel-size configuration: CG output channels per CTA group; ND rows of W per
+// dilation (CG*K*K taps padded to a multiple of 8, so each dilation's rows start on a
+// swizzle atom); NALL = the MMA N (3 * ND, padded to a multiple of 16); HALO x-window
+// columns left and right of the tile (a 16-byte TMA coordinate, >= the halo radius);
+// WINMAX x-window positions (TH + 2R) x (TW + 2 HALO).
+template <int K> struct Tf32Cfg;
+template <> struct Tf32Cfg<3> { static constexpr int CG = 4, ND = 48, NALL = 144, HALO = 8, WINMAX = 960; };
+template <> struct Tf32Cfg<5> { static constexpr int CG = 2, ND = 56, NALL = 176, HALO = 12, WINMAX = 1936; };
+
+template <int K>
+struct Tf32Layout {
+    using F = Tf32Cfg<K>;
+    static constexpr int kCG = F::CG, kTaps = K * K, kN = F::ND, kNAll = F::NALL, kHalo = F::HALO;
+    static constexpr int kWinMax = F::WINMAX;
+    static constexpr int kCPT = kCG / (kEpiWarps / 4);   // channels per epilogue thread
+    // shared memory (bytes from a 1024-aligned base)
+    static constexpr int kWAtom = kNAll * 128;                  // one K-atom (32 fp32 of K) of NALL rows, SW128
+    static constexpr int kSW = 0;                               // W hi [2 K-atoms][dilation][ND rows x 128 B]
+    static constexpr int kSWlo = kSW + 2 * kWAtom;              // W lo, same layout
+    static constexpr int kSYr = kSWlo + 2 * kWAtom;             // raw y [2 K-atoms][2 pixel halves][32 j][64 px] fp32
+    static constexpr int kSYhi = kSYr + 2 * 64 * 64 * 4;        // y hi [2 K-atoms][128 rows x 128 B], SW128 K-major
+    static constexpr int kSYlo = kSYhi + 2 * kTile * 128;       // y lo, same layout
+    static constexpr int kSBias = kSYlo + 2 * kTile * 128;      // bias of the group's taps [3][CG*K*K] fp32
+    static constexpr int kSX = kSBias + (3 * kCG * kTaps * 4 + 127) / 128 * 128;   // x windows 2 x [CG][kWinMax] fp32
+    static constexpr int kSlot = (kWinMax * 4 + 127) / 128 * 128;
+    static constexpr int kRawBuf = kCG * kSlot;
+    static constexpr int kSStage = kSX + kRawBufs * kRawBuf;    // output staging 2 x 4 blocks x [CG][TH][TW] fp32
+    static constexpr int kStageBlk = kCG * kTile * 4;
+    static constexpr int kStageBuf = 4 * kStageBlk;
+    static constexpr int kSmemBytes = kSStage + 2 * kStageBuf + 1024;
+    static_assert(kWAtom % 1024 == 0 && kSWlo % 1024 == 0 && kSYhi % 1024 == 0 && kSYlo % 1024 == 0 &&
+                      (kN * 128) % 1024 == 0, "SW128 atoms need 1 KiB alignment");
+    static_assert(kSX % 128 == 0 && kSlot % 128 == 0 && kSStage % 128 == 0, "TMA alignment");
+    static_assert(2 * kNAll <= kTmemCols && kCG * kTaps <= kN && 3 * kN <= kNAll && kNAll % 16 == 0 && kNAll <= 256,
+                  "MMA N, TMEM columns");
+    static_assert(kSmemBytes <= 227 * 1024 - 512, "shared memory");
+};
 
 struct Tf32Params {
     Dims d;
@@ -108,11 +116,18 @@ __device__ __forceinline__ void named_bar(int id) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(NTHREADS) : "memory");
 }
 
+template <int K>
 __global__ void __launch_bounds__(kThreads, 1)
     forward_tf32_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
                         const Tf32Params P) {
     using namespace tc;
+    using L = Tf32Layout<K>;
+    constexpr int kCG = L::kCG, kTaps = L::kTaps, kN = L::kN, kNAll = L::kNAll, kHalo = L::kHalo, kCPT = L::kCPT;
+    constexpr int kWAtom = L::kWAtom, kSW = L::kSW, kSWlo = L::kSWlo, kSYr = L::kSYr, kSYhi = L::kSYhi,
+                  kSYlo = L::kSYlo, kSBias = L::kSBias, kSX = L::kSX, kSlot = L::kSlot, kRawBuf = L::kRawBuf,
+                  kSStage = L::kSStage, kStageBlk = L::kStageBlk, kStageBuf = L::kStageBuf;
+    constexpr int r0 = K / 2;
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB-aligned base by pointer arithmetic on the shared array (accesses stay shared-space)
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -151,25 +166,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
     if (warp >= kEpi0) {
-        // constant operands (no swizzle, 8x16-byte core matrices, element (m, k) at
-        // (m/8)*256 + (k/4)*128 + (m%8)*16 + (k%4)*4): a ones pair (A, columns 0 and 1) and
-        // the bias split into hi and lo (B, columns 0 and 1), so one K step adds hi + lo
+        // the bias of the group's taps, [dilation][local channel * K*K + k], added by the epilogue
         const int et = threadIdx.x - 32 * kEpi0;
-        for (int i = et; i < kTile * 8; i += 32 * kEpiWarps) {
-            const int m = i / 8, k = i % 8;
-            *reinterpret_cast<float*>(sm + kSOnes + (m / 8) * 256 + (k / 4) * 128 + (m % 8) * 16 + (k % 4) * 4) =
-                k < 2 ? 1.0f : 0.0f;
+        float* bt = reinterpret_cast<float*>(sm + kSBias);
+        for (int i = et; i < 3 * kCG * kTaps; i += 32 * kEpiWarps) {
+            const int dd = i / (kCG * kTaps), n = i % (kCG * kTaps);
+            const long long o = (long long)(dd * C + c0) * kTaps + n;
+            bt[i] = (P.bias != nullptr && o < P.d.O) ? P.bias[o] : 0.0f;
         }
-        for (int i = et; i < kNAll * 8; i += 32 * kEpiWarps) {
-            const int n = i / 8, k = i % 8, dd = n / kN, nl = n % kN;
-            const long long o = (long long)(dd * C + c0) * kTaps + nl;
-            float v = 0.0f;
-            if (k < 2 && P.bias != nullptr && nl < kCG * kTaps && o < P.d.O) {
-                const float b = P.bias[o];
-                const float hi = tf32_hi(b);
-                v = k == 0 ? hi : b - hi;
+        // rows 3*ND .. NALL-1 of the W operand (no TMA box writes them) are zero
+        constexpr int kPadF = (kNAll - 3 * kN) * 32;   // floats per K-atom
+        if constexpr (kPadF > 0) {
+            for (int i = et; i < 2 * kPadF; i += 32 * kEpiWarps) {
+                const int kh = i / kPadF, e = i % kPadF;
+                reinterpret_cast<float*>(sm + kSW + kh * kWAtom + 3 * kN * 128)[e] = 0.0f;
             }
-            *reinterpret_cast<float*>(sm + kSBias + (n / 8) * 256 + (k / 4) * 128 + (n % 8) * 16 + (k % 4) * 4) = v;
         }
         fence_proxy_async_smem();
     }
@@ -184,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tmY);
             prefetch_tmap(&tmW);
-            mbar_arrive_expect_tx(&bar_w, 2 * kWAtom);
+            mbar_arrive_expect_tx(&bar_w, 2 * 3 * kN * 128);
             for (int dd = 0; dd < 3; ++dd)
                 for (int kh = 0; kh < 2; ++kh)
                     tma_load_2d(sm + kSW + kh * kWAtom + dd * kN * 128, &tmW, &bar_w, kh * 32, (dd * C + c0) * kTaps);
@@ -244,8 +255,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ylo = smem_desc(smem_u32(sm + kSYlo), 16, 1024, kSwizzle128B);
             const uint64_t whi = smem_desc(smem_u32(sm + kSW), 16, 1024, kSwizzle128B);
             const uint64_t wlo = smem_desc(smem_u32(sm + kSWlo), 16, 1024, kSwizzle128B);
-            const uint64_t ones = smem_desc(smem_u32(sm + kSOnes), 128, 256, kSwizzleNone);
-            const uint64_t bias = smem_desc(smem_u32(sm + kSBias), 128, 256, kSwizzleNone);
             for (int i = 0; ok && i < n_my; ++i) {
                 const int tb = i & 1;                  // TMEM accumulator of this tile
                 if (!mbar_wait(&bar_acc_empty[tb], ((i >> 1) & 1) ^ 1, P.err, abort_v)) break;
@@ -270,7 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(&bar_ysplit_empty[kh]);
                 }
                 if (!ok) break;
-                mma_tf32(dt, ones, bias, idesc, 1u);
                 mma_commit(&bar_acc_full[tb]);
             }
             // all issued MMAs retire before TMEM is released
@@ -364,11 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 tc_fence_after();
 #pragma unroll
-                for (int dd = 0; dd < 3; ++dd) {
-                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * kNAll + dd * kN + cl0 * kTaps;
-                    DDPM_TMEM_LD_X16(ta, t[dd]);
-                    DDPM_TMEM_LD_X2(ta + 16, (t[dd] + 16));
-                }
+                for (int dd = 0; dd < 3; ++dd)
+                    tmem_load_cols<kCPT * kTaps>(tmem + ((uint32_t)(q * 32) << 16) + tb * kNAll + dd * kN + cl0 * kTaps,
+                                                 t[dd]);
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -378,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // block 0: channels c0 .. c0+CG-1 of the output are x itself
 #pragma unroll
                 for (int c = 0; c < kCPT; ++c) stage0[c * tpix] = xw[c * (kSlot / 4)];
+                const float* bt = reinterpret_cast<const float*>(sm + kSBias) + cl0 * kTaps;
 #pragma unroll
                 for (int dd = 0; dd < 3; ++dd) {
                     const int dil = dil_of(P.d, dd);
@@ -386,10 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < kCPT; ++c) acc[c] = 0.0f;
 #pragma unroll
                     for (int k = 0; k < kTaps; ++k) {
-                        const int off = ((k / 3 - 1) * WC + (k % 3 - 1)) * dil;
+                        const int off = ((k / K - r0) * WC + (k % K - r0)) * dil;
 #pragma unroll
-                        for (int c = 0; c < kCPT; ++c)
-                            acc[c] = fmaf(__uint_as_float(t[dd][c * kTaps + k]), xw[c * (kSlot / 4) + off], acc[c]);
+                        for (int c = 0; c < kCPT; ++c) {
+                            const float tap = __uint_as_float(t[dd][c * kTaps + k]) + bt[dd * kCG * kTaps + c * kTaps + k];
+                            acc[c] = fmaf(tap, xw[c * (kSlot / 4) + off], acc[c]);
+                        }
                     }
                     float* sa = stage0 + (1 + dd) * (kStageBlk / 4);
 #pragma unroll
@@ -458,24 +467,23 @@ Tiling tiling_of(const Dims& d) {
     return t;
 }
 
-}  // namespace
-
-bool forward_tf32_eligible(const Dims& d, const void* x, const void* y, const void* w, const void* out) {
-    if (d.dtype != 0 || !(d.flags & kFlagTf32x3Forward) || (d.flags & kFlagCudaCores) || d.K != 3) return false;
-    if (d.C % kCG != 0 || d.C > kKPad || d.W % 4 != 0) return false;   // 16-byte TMA strides and coordinates
-    if (d.R() > kHalo) return false;
+template <int K>
+bool eligible_k(const Dims& d) {
+    using L = Tf32Layout<K>;
+    // 16-byte TMA strides (W rows: C % 4; images: W % 4) and whole channel groups
+    if (d.C % 4 != 0 || d.C % L::kCG != 0 || d.C > kKPad || d.W % 4 != 0) return false;
+    if (d.R() > L::kHalo) return false;
     const Tiling t = tiling_of(d);
-    if ((long long)(t.TH + 2 * d.R()) * (t.TW + 2 * kHalo) > kWinMax) return false;
-    if ((uintptr_t)x % 16 || (uintptr_t)y % 16 || (uintptr_t)w % 16 || (uintptr_t)out % 16) return false;
-    const long long tiles = (long long)d.B * t.tiles_per_img;
-    return tiles <= (1LL << 30) && d.O <= (1LL << 30) && d.HW <= (1LL << 31) - 1024 && bwdtc::encode_fn() != nullptr;
+    return (long long)(t.TH + 2 * d.R()) * (t.TW + 2 * L::kHalo) <= L::kWinMax;
 }
 
-cudaError_t launch_forward_tf32(const Dims& d, const void* x, const void* y, const void* w, const void* bias,
-                                void* out, cudaStream_t s) {
+template <int K>
+cudaError_t launch_k(const Dims& d, const void* x, const void* y, const void* w, const void* bias, void* out,
+                     cudaStream_t s) {
+    using L = Tf32Layout<K>;
     static int attr_done[64] = {};
     {
-        const cudaError_t e = set_max_dynamic_smem((const void*)forward_tf32_kernel, kSmemBytes, attr_done, true);
+        const cudaError_t e = set_max_dynamic_smem((const void*)forward_tf32_kernel<K>, L::kSmemBytes, attr_done, true);
         if (e != cudaSuccess) return e;
     }
     auto enc = bwdtc::encode_fn();
@@ -491,18 +499,18 @@ cudaError_t launch_forward_tf32(const Dims& d, const void* x, const void* y, con
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    // W [O, C] fp32: boxes of 32 input channels (one 128-byte swizzle row) x N rows
+    // W [O, C] fp32: boxes of 32 input channels (one 128-byte swizzle row) x ND rows
     const cuuint64_t dimW[2] = {(cuuint64_t)d.C, (cuuint64_t)d.O};
     const cuuint64_t strW[1] = {(cuuint64_t)d.C * 4};
-    const cuuint32_t boxW[2] = {32, (cuuint32_t)kN};   // one dilation's rows of one K-atom
+    const cuuint32_t boxW[2] = {32, (cuuint32_t)L::kN};   // one dilation's rows of one K-atom
     const cuuint32_t one2[2] = {1, 1};
     if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(w), dimW, strW, boxW, one2,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    const int WH = t.TH + 2 * R, WC = t.TW + 2 * kHalo;
+    const int WH = t.TH + 2 * R, WC = t.TW + 2 * L::kHalo;
     if (!encode_nchw_f32(&tmX, x, d, d.C, (uint32_t)WC, (uint32_t)WH, 1) ||
-        !encode_nchw_f32(&tmO, out, d, 4 * d.C, (uint32_t)t.TW, (uint32_t)t.TH, (uint32_t)kCG))
+        !encode_nchw_f32(&tmO, out, d, 4 * d.C, (uint32_t)t.TW, (uint32_t)t.TH, (uint32_t)L::kCG))
         return cudaErrorInvalidValue;
 
     Tf32Params P;
@@ -512,7 +520,7 @@ cudaError_t launch_forward_tf32(const Dims& d, const void* x, const void* y, con
     P.tiles_per_row = t.tiles_per_row;
     P.tiles_per_img = t.tiles_per_img;
     P.n_tiles = d.B * t.tiles_per_img;
-    P.n_groups = d.C / kCG;
+    P.n_groups = d.C / L::kCG;
     int cpg = num_sms() / P.n_groups;
     if (cpg < 1) cpg = 1;
     if (cpg > P.n_tiles) cpg = P.n_tiles;
@@ -524,9 +532,24 @@ cudaError_t launch_forward_tf32(const Dims& d, const void* x, const void* y, con
     P.err = device_error_word();
     if (P.err == nullptr) return cudaErrorUnknown;
     trace_begin(s, kKForwardTf32);
-    forward_tf32_kernel<<<P.n_groups * cpg, kThreads, kSmemBytes, s>>>(tmY, tmW, tmX, tmO, P);
+    forward_tf32_kernel<K><<<P.n_groups * cpg, kThreads, L::kSmemBytes, s>>>(tmY, tmW, tmX, tmO, P);
     trace_end(s);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+bool forward_tf32_eligible(const Dims& d, const void* x, const void* y, const void* w, const void* out) {
+    if (d.dtype != 0 || !(d.flags & kFlagTf32x3Forward) || (d.flags & kFlagCudaCores)) return false;
+    if (!(d.K == 3 ? eligible_k<3>(d) : d.K == 5 ? eligible_k<5>(d) : false)) return false;
+    if ((uintptr_t)x % 16 || (uintptr_t)y % 16 || (uintptr_t)w % 16 || (uintptr_t)out % 16) return false;
+    const long long tiles = (long long)d.B * tiling_of(d).tiles_per_img;
+    return tiles <= (1LL << 30) && d.O <= (1LL << 30) && d.HW <= (1LL << 31) - 1024 && bwdtc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_forward_tf32(const Dims& d, const void* x, const void* y, const void* w, const void* bias,
+                                void* out, cudaStream_t s) {
+    return d.K == 3 ? launch_k<3>(d, x, y, w, bias, out, s) : launch_k<5>(d, x, y, w, bias, out, s);
 }
 
 }  // namespace ddpm

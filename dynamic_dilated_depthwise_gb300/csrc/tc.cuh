@@ -309,5 +309,21 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_format, uint32_t a
            | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// n consecutive TMEM columns of this warp's lane quadrant into r[0..n)
+template <int NCOL>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
+#pragma unroll
+    for (int c = 0; c + 16 <= NCOL; c += 16) DDPM_TMEM_LD_X16(taddr + c, (r + c));
+    constexpr int rem = NCOL % 16;
+    constexpr int b8 = NCOL - rem;
+    if constexpr ((rem & 8) != 0) DDPM_TMEM_LD_X8(taddr + b8, (r + b8));
+    constexpr int b4 = b8 + (rem & 8);
+    if constexpr ((rem & 4) != 0) DDPM_TMEM_LD_X4(taddr + b4, (r + b4));
+    constexpr int b2 = b4 + (rem & 4);
+    if constexpr ((rem & 2) != 0) DDPM_TMEM_LD_X2(taddr + b2, (r + b2));
+    constexpr int b1 = b2 + (rem & 2);
+    if constexpr ((rem & 1) != 0) DDPM_TMEM_LD_X1(taddr + b1, (r + b1));
+}
+
 }  // namespace tc
 }  // namespace ddpm

@@ -84,9 +84,10 @@ typedef enum { DDPM_FLOAT32 = 0, DDPM_BFLOAT16 = 1 } ddpm_dtype;
  *   dynamic filter stays IEEE FP32 FMA.  The page lists tf32x3 among the
  *   variants it tried for the FP32 forward and did not adopt on its card
  *   (section "已验证但未采用的方案"); without the flag the FP32 forward is the
- *   page's IEEE FP32 dot.  Applies for K = 3, C a multiple of 4 up to 64, W a
- *   multiple of 4, halo radius <= 5 and 16-byte aligned tensors; other FP32
- *   problems run the IEEE kernel.  Ignored for BF16 and under
+ *   page's IEEE FP32 dot.  Applies for K = 3 with halo radius <= 5 or K = 5 with
+ *   halo radius <= 10 (up to 8 and 12 on images narrower than 64 pixels), C a
+ *   multiple of 4 up to 64, W a multiple of 4 and 16-byte aligned tensors; other
+ *   FP32 problems run the IEEE kernel.  Ignored for BF16 and under
  *   DDPM_FLAG_CUDA_CORES. */
 #define DDPM_FLAG_TF32X3_FORWARD 0x4u
 

@@ -234,9 +234,10 @@ def test_tc_forward_repeated_calls_identical():
 
 # ------------------------------------- FP32 forward on TF32 tensor cores (3xTF32) --
 
-# Shapes the 3xTF32 forward takes (FP32, K = 3, C % 4 == 0, C <= 64, W % 4 == 0, halo
-# radius <= 5): ragged 64-column tiles, whole-row tiles (W < 64), several images, a
-# single-row image, other dilations, C below one K block.
+# Shapes the 3xTF32 forward takes (FP32, K = 3 with halo radius <= 8 or K = 5 with halo
+# radius <= 12; C % 4 == 0, C <= 64, W % 4 == 0): ragged 64-column
+# tiles, whole-row tiles (W < 64), several images, a single-row image, other dilations,
+# C below one K block, and for K = 5 the radius-10 halo of dilation 5.
 TF32X3_SHAPES = [
     Problem(1, 16, 5, 136, 3),               # two full tiles and an 8-pixel one per row
     Problem(2, 24, 10, 24, 3),               # whole-row tiles of 5 rows, C = 24
@@ -246,10 +247,17 @@ TF32X3_SHAPES = [
     Problem(1, 4, 1, 12, 3),                 # one row, C = 4
     Problem(3, 64, 40, 40, 3),               # several images
 ]
+TF32X3_K5_SHAPES = [
+    Problem(1, 64, 12, 256, 5),              # C = 64, four tiles per row, halo radius 10
+    Problem(2, 16, 10, 24, 5),               # whole-row tiles of 5 rows
+    Problem(1, 4, 7, 200, 5),                # C = 4 (two channel groups), 8-pixel last tile
+    Problem(1, 8, 3, 40, 5, (1, 2, 2)),      # other dilations, image shorter than a tile
+    Problem(3, 24, 33, 36, 5, (2, 4, 6)),    # radius 12, several images, ragged rows
+]
 TF32X3 = binding.DDPM_FLAG_TF32X3_FORWARD
 
 
-@pytest.mark.parametrize("p", TF32X3_SHAPES, ids=_id)
+@pytest.mark.parametrize("p", TF32X3_SHAPES + TF32X3_K5_SHAPES, ids=_id)
 def test_tf32x3_forward_matches_oracle(p):
     h = make_inputs(p, 720, "float32", grad=False)
     d = _dev(h)
@@ -263,7 +271,7 @@ def test_tf32x3_forward_matches_oracle(p):
     assert torch.equal(out[:, :p.C].cpu(), h["x"])
 
 
-@pytest.mark.parametrize("p", TF32X3_SHAPES[:5], ids=_id)
+@pytest.mark.parametrize("p", TF32X3_SHAPES[:5] + TF32X3_K5_SHAPES[:3], ids=_id)
 def test_tf32x3_forward_integer_bit_exact(p):
     """Integer inputs: every operand is exact in TF32 (the lo parts are zero), so the
     split GEMM and the FP32 filter must match the oracle bit for bit."""
@@ -282,8 +290,9 @@ def test_tf32x3_forward_without_bias_and_ineligible_shapes():
     torch.cuda.synchronize()
     assert_forward_close(out, oracle.forward(h["x"], h["y"], h["weight"], None, p.K, p.dilations), "float32",
                          "out (3xTF32, no bias)")
-    # K = 5 and W % 4 != 0 keep the IEEE kernel under the flag
-    for q in (Problem(1, 8, 12, 16, 5), Problem(1, 8, 9, 10, 3)):
+    # a K = 5 halo radius above 12, C % 4 != 0 and W % 4 != 0 keep the IEEE kernel under
+    # the flag
+    for q in (Problem(1, 8, 12, 16, 5, (1, 3, 7)), Problem(1, 6, 6, 16, 5), Problem(1, 8, 9, 10, 3)):
         hq = _dev(make_inputs(q, 722, "float32", grad=False))
         names = _traced_kernels(lambda: binding.forward(hq["x"], hq["y"], hq["weight"], hq["bias"], q.K, q.dilations,
                                                         flags=TF32X3))
@@ -615,7 +624,7 @@ def test_full_size_forward_and_filter(name, dtype):
     assert binding.ddpm_get_device_error() == 0
 
 
-@pytest.mark.parametrize("name", ["b1_c64_128x128_k3", "b1_c64_256x256_k3"])
+@pytest.mark.parametrize("name", ["b1_c64_128x128_k3", "b1_c64_256x256_k3", "b1_c64_128x128_k5"])
 def test_full_size_tf32x3_forward(name):
     """The FP32 forward with the 3xTF32 generator GEMM, whole tensors, FP32 bar."""
     p = WORKLOADS[name]
