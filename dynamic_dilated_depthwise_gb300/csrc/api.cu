@@ -93,6 +93,14 @@ size_t elem_size(int dtype) { return dtype == DDPM_BFLOAT16 ? 2 : 4; }
 // TF32 dY kernel reads.
 size_t packed_offset(const Dims& d) { return (ddpm::backward_simt_workspace(d) + 255) & ~size_t(255); }
 
+// FP32 workspace after the partials: the TF32 dY's rearranged weight, then (256-byte
+// aligned) the TF32 dX's channel-chunked copy of y.  The offsets depend on the problem
+// alone, so a workspace sized for both serves either.
+size_t dx_tf32_offset(const Dims& d) {
+    const size_t wt = ddpm::bwd_dy_tf32_shape_ok(d) ? ddpm::bwd_dy_tf32_wt_bytes(d) : 0;
+    return (packed_offset(d) + wt + 255) & ~size_t(255);
+}
+
 ddpm_status validate(const ddpm_problem* p, Dims* d) {
     if (p == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
     if (p->B < 1 || p->C < 1 || p->H < 1 || p->W < 1) return DDPM_ERR_INVALID_ARGUMENT;
@@ -207,6 +215,8 @@ ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* by
     if (bytes == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
     if (ddpm::bwd_dx_packed_shape_ok(d))
         *bytes = packed_offset(d) + ddpm::bwd_dx_packed_bytes(d);
+    else if (ddpm::bwd_dx_tf32_shape_ok(d))
+        *bytes = dx_tf32_offset(d) + ddpm::bwd_dx_tf32_bytes(d);
     else if (ddpm::bwd_dy_tf32_shape_ok(d))
         *bytes = packed_offset(d) + ddpm::bwd_dy_tf32_wt_bytes(d);
     else
@@ -244,7 +254,10 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
                             workspace_bytes >= poff + ddpm::bwd_dx_packed_bytes(d);
         const bool dy_tf32 = ddpm::bwd_dy_tf32_eligible(d, grad_out, x, weight, dy) &&
                              workspace_bytes >= poff + ddpm::bwd_dy_tf32_wt_bytes(d);
-        const size_t part_bytes = (packed || dy_tf32) ? poff : workspace_bytes;
+        const size_t xoff = dx_tf32_offset(d);
+        const bool dx_tf32 = ddpm::bwd_dx_tf32_eligible(d, grad_out, y, weight, dx) &&
+                             workspace_bytes >= xoff + ddpm::bwd_dx_tf32_bytes(d);
+        const size_t part_bytes = (packed || dy_tf32 || dx_tf32) ? poff : workspace_bytes;
         // dX on the caller's stream, dY and dW (+ reduce) on the two side streams: the
         // pieces share only inputs, and each one's last partial wave of CTAs leaves SMs
         // that the others fill.  While kernels are traced the pieces run one after
@@ -264,6 +277,8 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
             e = ddpm::launch_bwd_dx_packed(d, grad_out, y, weight, bias, dx, static_cast<char*>(workspace) + poff, s);
         else if (ddpm::bwd_dx_tc_eligible(d, grad_out, y, weight))
             e = ddpm::launch_bwd_dx_tc(d, grad_out, y, weight, bias, dx, s);
+        else if (dx_tf32)
+            e = ddpm::launch_bwd_dx_tf32(d, grad_out, y, weight, bias, dx, static_cast<char*>(workspace) + xoff, s);
         else
             e = ddpm::launch_bwd_dx_simt(d, grad_out, y, weight, bias, dx, s);
         if (e == cudaSuccess) {

@@ -1,0 +1,461 @@
+// bwd_dx_tf32.cu -- dX of FP32 problems on TF32 tensor cores (DDPM_FLAG_TF32_BACKWARD).
+//
+// README "lartpang/DynamicConvolutionOperator", section "CUDA Flash 式融合训练":
+// dX recomputes the dynamic taps and gathers each dilation's contribution,
+//   dx[b,c,q] = grad[b,c,q] + sum_{d,ky,kx} T[b,o,q-off] * grad[b,(1+d)C+c,q-off],
+//   T = bias[o] + sum_j W[o,j] y[b,j,q-off],  o = (d*C + c)*9 + ky*3 + kx,
+// and the section's precision policy lets an FP32 backward run its recompute on TF32
+// tensor cores (FP32 accumulation).
+//
+// Two launches.
+// pack_y_f32: y is copied once into a channel-chunked layout [B][C/4][H][W][4] -- the
+//   four channels of a chunk at one pixel in 16 contiguous bytes (HBM-bound).
+// bwd_dx_tf32: one shifted TF32 GEMM per tap.  A persistent CTA walks 16x8 pixel tiles
+//   (MMA M = 128, slot s = r*8 + c) with all channels (N = 64):
+//   - TMA brings the tile's y window [chunk][(16+2R) x (8+2R) positions][4] from the
+//     packed copy (one contiguous run per window row and chunk); eight consecutive
+//     slots are eight consecutive positions of one window row, so the A operand of tap
+//     (ky, kx) is the window at a start offset (K-major, no swizzle, core matrices of
+//     8 positions x 4 channels, row-group stride WW*16 bytes);
+//   - the W rows of one tap for all channels ([64 c][64 j] fp32, two 128B-swizzled
+//     K-atoms) stream through a ring fed by a producer warp of its own;
+//   - the bias is two last K=8 steps: A a one-hot row selecting tap k (every row group
+//     the same: stride 0), B a resident table of bias[d, c, k];
+//   - two threads in different warps issue the MMAs of even and odd taps (an issuing
+//     thread waits for the tensor pipe to accept each MMA; the other one fills the gaps);
+//   - D of each tap lands in one of eight TMEM buffers [128 x 64]; eight worker warps
+//     accumulate tap * grad in IEEE FP32.  Four-byte grad windows of all 64 channels do
+//     not fit in shared memory beside the y window, so each worker gathers its grad
+//     values from global memory (L2), one tap ahead of their use: a warp's 32 pixels of
+//     one channel are four 32-byte sectors.
+#include "bwd_tc_common.cuh"
+#include "tc.cuh"
+
+namespace ddpm {
+namespace {
+
+constexpr int kTH = 16, kTW = 8;          // pixel tile
+constexpr int kN = 64;                    // MMA N: channels (rows of W beyond C are never read back)
+constexpr int kTaps = 27;
+constexpr int kWork = 8;                  // worker warps
+constexpr int kIssuers = 2;               // MMA-issuing threads (warp 1 and warp kIssuer2), alternate taps
+constexpr int kIssuer2 = 2 + kWork;
+constexpr int kWProd = 3 + kWork;         // W-ring producer warp
+constexpr int kThreads = 32 * (4 + kWork);
+constexpr int kDBufs = 8;                 // TMEM accumulators of 64 columns
+constexpr int kMaxStages = 8;
+constexpr int kMinStages = 2;
+constexpr int kMaxR = 6;
+constexpr int kWAtom = 64 * 128;          // [64 c][32 j] fp32, SW128
+constexpr int kWTile = 2 * kWAtom;        // one tap: j 0..31 and 32..63
+constexpr int kOneHot = 9 * 512;          // [tap k][4 K-groups][8 rows][4] fp32
+constexpr int kBiasTab = 3 * 4096;        // [d][c/8][k/4][c%8][k%4] fp32
+constexpr int kSmemCap = 227 * 1024 - 1024;
+constexpr int kPackThreads = 256;
+
+struct DxTf32Params {
+    Dims d;
+    int tiles_w, tiles_per_img, n_tiles;
+    int R, WW, WH, npos, nch4, nks, stages;
+    int oyw, ooh, obt;                     // shared-memory offsets from the aligned base
+    const float* g;                        // grad, NCHW [B][4C][H][W]
+    const float* bias;                     // may be null
+    float* dx;
+    unsigned int* err;
+};
+
+// Shared-memory plan for a problem; stages == 0 when it does not fit.
+struct DxTf32Layout {
+    int stages, oyw, ooh, obt, bytes;
+};
+
+DxTf32Layout dx_tf32_layout(const Dims& d) {
+    DxTf32Layout L{};
+    const int R = d.R();
+    if (R > kMaxR) return L;
+    const int npos = (kTH + 2 * R) * (kTW + 2 * R);
+    const int nks = (d.C + 7) / 8;
+    const int ybytes = 2 * nks * npos * 16;
+    const int rest = ybytes + kOneHot + kBiasTab;
+    int stages = (kSmemCap - 1024 - rest) / kWTile;
+    if (stages > kMaxStages) stages = kMaxStages;
+    // an even number of stages: tap i uses stage i % stages and the taps alternate between
+    // the two issuers, so every use of a stage falls to the same issuer
+    stages &= ~1;
+    if (stages < kMinStages) return L;
+    L.stages = stages;
+    L.oyw = stages * kWTile;
+    L.ooh = L.oyw + ybytes;
+    L.obt = L.ooh + kOneHot;
+    L.bytes = L.obt + kBiasTab + 1024;
+    return L;
+}
+
+// ----------------------------------------------------------------------------- pack
+// Thread = (b, chunk, 4-pixel group): four 16-byte channel rows in, four 16-byte
+// pixel rows out.  HW is a multiple of 4 (W is).
+__global__ void __launch_bounds__(kPackThreads)
+    pack_y_f32_kernel(const float* __restrict__ y, float* __restrict__ yc, int C, long long HW, long long n_units) {
+    const int nch4 = C / 4;
+    const long long groups = HW / 4;
+    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < n_units;
+         u += (long long)gridDim.x * blockDim.x) {
+        const long long p4 = u % groups, bc = u / groups;   // bc = b * nch4 + cb
+        const long long b = bc / nch4, cb = bc % nch4;
+        const float* src = y + (b * C + cb * 4) * HW + p4 * 4;
+        float4 in[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) in[e] = __ldg(reinterpret_cast<const float4*>(src + e * HW));
+        float4* dst = reinterpret_cast<float4*>(yc + (bc * HW + p4 * 4) * 4);
+        dst[0] = make_float4(in[0].x, in[1].x, in[2].x, in[3].x);
+        dst[1] = make_float4(in[0].y, in[1].y, in[2].y, in[3].y);
+        dst[2] = make_float4(in[0].z, in[1].z, in[2].z, in[3].z);
+        dst[3] = make_float4(in[0].w, in[1].w, in[2].w, in[3].w);
+    }
+}
+
+// ----------------------------------------------------------------------------- dX
+// The grad values of one tap for this thread's pixel and 32 channels (zero where the
+// source pixel lies outside the image or the channel beyond C).
+__device__ __forceinline__ void gather_tap(float (&g)[32], const float* gb, int u, const DxTf32Params& P, int h, int w,
+                                           bool inside, int c0) {
+    const int dd = u / 9, k = u - dd * 9;
+    const int dil = dil_of(P.d, dd);
+    const int sh = h - (k / 3 - 1) * dil, sw = w - (k % 3 - 1) * dil;
+    const bool valid = inside && sh >= 0 && sh < P.d.H && sw >= 0 && sw < P.d.W;
+    if (valid) {
+        const float* p = gb + (long long)((1 + dd) * P.d.C + c0) * P.d.HW + (long long)sh * P.d.W + sw;
+        const int nc = P.d.C - c0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[i] = i < nc ? __ldg(p + (long long)i * P.d.HW) : 0.0f;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[i] = 0.0f;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dx_tf32_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
+                       const DxTf32Params P) {
+    using namespace tc;
+    extern __shared__ uint8_t smem_raw[];
+    // 1 KiB-aligned base by pointer arithmetic on the shared array (accesses stay shared-space)
+    uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ uint64_t wt_full[kMaxStages], wt_empty[kMaxStages], d_full[kDBufs], d_empty[kDBufs];
+    __shared__ uint64_t yw_full, yw_empty, mma_done[kIssuers];
+    __shared__ uint32_t tmem_slot;
+    __shared__ uint32_t a_shift[kTaps];   // per-tap start offset of the A operand in the y window, bytes
+    __shared__ int abort_flag;
+    volatile int* abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = P.d.C, H = P.d.H, W = P.d.W;
+    const long long HW = P.d.HW;
+    const int n_my = blockIdx.x < P.n_tiles ? (P.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int S = P.stages, R = P.R;
+
+    if (threadIdx.x < kTaps) {
+        // tap (ky, kx) of dilation d reads y at q - ((ky-1) d, (kx-1) d): window position (r + R - (ky-1) d, c + R - (kx-1) d)
+        const int u = threadIdx.x, dil = dil_of(P.d, u / 9), ky = (u % 9) / 3, kx = u % 3;
+        a_shift[u] = (uint32_t)((R - (ky - 1) * dil) * P.WW + (R - (kx - 1) * dil)) * 16;
+    }
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&wt_full[i], 1);
+            mbar_init(&wt_empty[i], 1);
+        }
+        for (int i = 0; i < kDBufs; ++i) {
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], kWork);
+        }
+        mbar_init(&yw_full, 1);
+        mbar_init(&yw_empty, kIssuers);   // each issuer commits once per tile
+        for (int i = 0; i < kIssuers; ++i) mbar_init(&mma_done[i], 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_slot, 512);
+    if (warp >= 2 && warp < 2 + kWork) {
+        // constant operands: one-hot tap selectors, bias tables, the zero chunk of the y window
+        const int et = threadIdx.x - 64, nt = 32 * kWork;
+        float* oh = reinterpret_cast<float*>(sm + P.ooh);
+        for (int i = et; i < kOneHot / 4; i += nt) {        // [tap k][K-group g][row][e], column g*4 + e
+            const int k = i >> 7, g = (i >> 5) & 3, e = i & 3;
+            oh[i] = (g * 4 + e == k) ? 1.0f : 0.0f;
+        }
+        float* bt = reinterpret_cast<float*>(sm + P.obt);
+        for (int i = et; i < kBiasTab / 4; i += nt) {       // [d][c/8][k/4][c%8][k%4]
+            const int dd = i >> 10, r = i & 1023;
+            const int c = (r >> 7) * 8 + ((r >> 2) & 7), k = ((r >> 5) & 3) * 4 + (r & 3);
+            bt[i] = (P.bias != nullptr && c < C && k < 9) ? P.bias[((long long)dd * C + c) * 9 + k] : 0.0f;
+        }
+        const int nzero = (2 * P.nks - P.nch4) * P.npos;    // chunk nch4 when C/4 is odd
+        for (int i = et; i < nzero; i += nt)
+            *reinterpret_cast<uint4*>(sm + P.oyw + ((long long)P.nch4 * P.npos + i) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer: y window
+        if (lane == 0) {
+            prefetch_tmap(&tmY);
+            const uint32_t ybytes = (uint32_t)P.nch4 * P.npos * 16;
+            int ny = 0;
+            for (int tl = 0; tl < n_my; ++tl) {
+                const int t = blockIdx.x + tl * gridDim.x;
+                const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
+                const int h0 = (ti / P.tiles_w) * kTH, w0 = (ti % P.tiles_w) * kTW;
+                if (!mbar_wait(&yw_empty, (tl & 1) ^ 1, P.err, abort_v)) break;
+                mbar_arrive_expect_tx(&yw_full, ybytes);
+                tma_load_4d(sm + P.oyw, &tmY, &yw_full, (w0 - R) * 4, h0 - R, 0, b);
+                ny = tl + 1;
+            }
+            // drain: every copy this thread started lands before its shared memory is released
+            int never = 0;
+            if (ny > 0) mbar_wait(&yw_full, (ny - 1) & 1, P.err, &never);
+        }
+    } else if (warp == kWProd) {
+        // ------------------------------------------------------- TMA producer: W ring, one tap per stage
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            int iw = 0, st = 0, sph = 0;               // taps issued, ring stage and its phase parity
+            const bool two_atoms = C > 32;             // j 32..63 exist
+            bool ok = true;
+            for (int tl = 0; tl < n_my && ok; ++tl)
+                for (int u = 0; u < kTaps; ++u) {
+                    const int dd = u / 9, k = u - dd * 9;
+                    if (!mbar_wait(&wt_empty[st], sph ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&wt_full[st], two_atoms ? kWTile : kWAtom);
+                    tma_load_3d(sm + st * kWTile, &tmW, &wt_full[st], 0, k, dd * C);
+                    if (two_atoms) tma_load_3d(sm + st * kWTile + kWAtom, &tmW, &wt_full[st], 32, k, dd * C);
+                    ++iw;
+                    if (++st == S) {
+                        st = 0;
+                        sph ^= 1;
+                    }
+                }
+            int never = 0;
+            for (int i = iw > S ? iw - S : 0; i < iw; ++i) mbar_wait(&wt_full[i % S], (i / S) & 1, P.err, &never);
+        }
+    } else if (warp == 1 || warp == kIssuer2) {
+        // ------------------------------------------------------- MMA issuers: taps of parity `par`
+        const int par = warp == 1 ? 0 : 1;
+        if (lane == 0 && n_my > 0) {
+            const uint32_t idesc = instr_desc(2, 0, 0, 128, kN);   // TF32, both operands K-major
+            const uint32_t lbo_y = (uint32_t)P.npos * 16, sbo_y = (uint32_t)P.WW * 16;
+            const uint64_t a_base = smem_desc(smem_u32(sm + P.oyw), lbo_y, sbo_y, kSwizzleNone);
+            const uint64_t w_base = smem_desc(smem_u32(sm), 16, 1024, kSwizzle128B);
+            const uint64_t oh_base = smem_desc(smem_u32(sm + P.ooh), 128, 0, kSwizzleNone);
+            const uint64_t bt_base = smem_desc(smem_u32(sm + P.obt), 128, 512, kSwizzleNone);
+            const int nks = P.nks;
+            bool ok = true;
+            for (int tl = 0; tl < n_my && ok; ++tl) {
+                if (!mbar_wait(&yw_full, tl & 1, P.err, abort_v)) break;
+                tc_fence_after();
+                for (int u = 0; u < kTaps; ++u) {
+                    const int i = tl * kTaps + u;             // tap counter of this CTA
+                    if ((i & 1) != par) continue;
+                    const int dd = u / 9, k = u - dd * 9;
+                    const int st = i % S, sph = (i / S) & 1;
+                    const int buf = i % kDBufs, bph = (i / kDBufs) & 1;
+                    if (!mbar_wait(&wt_full[st], sph, P.err, abort_v) ||
+                        !mbar_wait(&d_empty[buf], bph ^ 1, P.err, abort_v)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a = desc_advance(a_base, a_shift[u]);
+                    const uint64_t b = desc_advance(w_base, (uint32_t)st * kWTile);
+                    const uint32_t dt = tmem + buf * kN;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        if (kk < nks)
+                            mma_tf32(dt, desc_advance(a, 2 * kk * lbo_y),
+                                     desc_advance(b, (uint32_t)((kk >> 2) * kWAtom + (kk & 3) * 32)), idesc,
+                                     kk > 0 ? 1u : 0u);
+                    mma_tf32(dt, desc_advance(oh_base, k * 512), desc_advance(bt_base, dd * 4096), idesc, 1u);
+                    mma_tf32(dt, desc_advance(oh_base, k * 512 + 256), desc_advance(bt_base, dd * 4096 + 256), idesc,
+                             1u);
+                    mma_commit(&d_full[buf]);
+                    mma_commit(&wt_empty[st]);
+                }
+                if (ok) mma_commit(&yw_empty);
+            }
+            // every MMA this thread issued retires before TMEM is released
+            mma_commit(&mma_done[par]);
+            int never = 0;
+            mbar_wait(&mma_done[par], 0, P.err, &never);
+        }
+    } else {
+        // ------------------------------------------------------- workers: gather, accumulate
+        const int q = warp & 3, hc = (warp - 2) >> 2;   // lane quadrant, channel half [32 hc, 32 hc + 32)
+        const int s = q * 32 + lane;                    // slot == TMEM lane
+        const int r = s >> 3, c = s & 7;
+        const int c0 = hc * 32;
+        bool ok = true;
+        for (int tl = 0; tl < n_my && ok; ++tl) {
+            const int t = blockIdx.x + tl * gridDim.x;
+            const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
+            const int h = (ti / P.tiles_w) * kTH + r, w = (ti % P.tiles_w) * kTW + c;
+            const bool inside = h < H && w < W;
+            const long long pix = inside ? (long long)h * W + w : 0;
+            const float* gb = P.g + (long long)b * 4 * C * HW;
+            // the identity term (channel block 0) is prefetched into L2 now and loaded last
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(gb + (long long)min(c0 + i, C - 1) * HW + pix));
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
+            float ga[32], gn[32];
+            gather_tap(ga, gb, 0, P, h, w, inside, c0);
+            // one tap: wait for its accumulator, read this thread's 32 channels, start the
+            // next tap's gather, hand the buffer back, accumulate
+            auto step = [&](int u, float(&gcur)[32], float(&gnext)[32], bool load_next) {
+                const int i = tl * kTaps + u, buf = i % kDBufs;
+                if (!__all_sync(0xffffffffu, mbar_wait(&d_full[buf], (i / kDBufs) & 1, P.err, abort_v))) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                uint32_t v[32];
+                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * kN + c0;
+                DDPM_TMEM_LD_X16(ta, (v + 0));
+                DDPM_TMEM_LD_X16(ta + 16, (v + 16));
+                if (load_next) gather_tap(gnext, gb, u + 1, P, h, w, inside, c0);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&d_empty[buf]);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = fmaf(__uint_as_float(v[e]), gcur[e], acc[e]);
+            };
+            for (int u = 0; u + 1 < kTaps && ok; u += 2) {
+                step(u, ga, gn, true);
+                if (ok) step(u + 1, gn, ga, true);
+            }
+            if (ok) step(kTaps - 1, ga, gn, false);
+            if (!ok) break;
+            if (inside) {
+                const float* g0p = gb + (long long)c0 * HW + pix;
+                float* dxp = P.dx + ((long long)b * C + c0) * HW + pix;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (c0 + i < C) dxp[(long long)i * HW] = __ldg(g0p + (long long)i * HW) + acc[i];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool bwd_dx_tf32_shape_ok(const Dims& d) {
+    if (d.dtype != 0 || !(d.flags & kFlagTf32Backward) || (d.flags & kFlagCudaCores) || d.K != 3) return false;
+    if (d.C % 4 != 0 || d.C > 64 || d.W % 4 != 0) return false;   // 16-byte chunks, strides and TMA coordinates
+    if (4LL * d.C * d.HW >= (1LL << 31)) return false;
+    return dx_tf32_layout(d).stages > 0 && d.O <= (1LL << 30);
+}
+
+bool bwd_dx_tf32_eligible(const Dims& d, const void* g, const void* y, const void* w, const void* dx) {
+    if (!bwd_dx_tf32_shape_ok(d)) return false;
+    if ((uintptr_t)g % 16 || (uintptr_t)y % 16 || (uintptr_t)w % 16 || (uintptr_t)dx % 4) return false;
+    return bwdtc::encode_fn() != nullptr;
+}
+
+size_t bwd_dx_tf32_bytes(const Dims& d) { return (size_t)d.B * (size_t)d.C * (size_t)d.HW * sizeof(float); }
+
+cudaError_t launch_bwd_dx_tf32(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
+                               void* packed, cudaStream_t s) {
+    const DxTf32Layout L = dx_tf32_layout(d);
+    if (L.stages == 0 || (uintptr_t)packed % 16 != 0) return cudaErrorInvalidValue;
+    static int attr_done[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dx_tf32_kernel, L.bytes, attr_done);
+        if (e != cudaSuccess) return e;
+    }
+    auto enc = bwdtc::encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    float* yc = static_cast<float*>(packed);
+    const int nch4 = d.C / 4;
+
+    DxTf32Params P;
+    P.d = d;
+    P.tiles_w = (d.W + kTW - 1) / kTW;
+    P.tiles_per_img = ((d.H + kTH - 1) / kTH) * P.tiles_w;
+    P.n_tiles = d.B * P.tiles_per_img;
+    P.R = d.R();
+    P.WW = kTW + 2 * P.R;
+    P.WH = kTH + 2 * P.R;
+    P.npos = P.WW * P.WH;
+    P.nch4 = nch4;
+    P.nks = (d.C + 7) / 8;
+    P.stages = L.stages;
+    P.oyw = L.oyw;
+    P.ooh = L.ooh;
+    P.obt = L.obt;
+    P.g = static_cast<const float*>(g);
+    P.bias = static_cast<const float*>(bias);
+    P.dx = static_cast<float*>(dx);
+    P.err = device_error_word();
+    if (P.err == nullptr) return cudaErrorUnknown;
+
+    CUtensorMap tmW, tmY;
+    {
+        // W viewed as [3C (dc)][9 (k)][C (j)]: box {32 j, 1 k, 64 dc} = one K-atom of the rows (d*C + c, k)
+        const cuuint64_t dims[3] = {(cuuint64_t)d.C, 9, (cuuint64_t)(3 * d.C)};
+        const cuuint64_t str[2] = {(cuuint64_t)d.C * 4, (cuuint64_t)d.C * 9 * 4};
+        const cuuint32_t box[3] = {32, 1, 64};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(w), dims, str, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        // the packed copy [B][C/4][H][W*4] fp32: a window row of one chunk is one run of WW*16 bytes;
+        // positions outside the image (x < 0 or x >= W*4, rows outside) read as zeros
+        const cuuint64_t dims[4] = {(cuuint64_t)d.W * 4, (cuuint64_t)d.H, (cuuint64_t)nch4, (cuuint64_t)d.B};
+        const cuuint64_t str[3] = {(cuuint64_t)d.W * 16, (cuuint64_t)d.HW * 16, (cuuint64_t)d.HW * 16 * nch4};
+        const cuuint32_t box[4] = {(cuuint32_t)P.WW * 4, (cuuint32_t)P.WH, (cuuint32_t)nch4, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (P.WW * 4 > 256 || P.WH > 256 ||
+            enc(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, yc, dims, str, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+
+    // 1. the channel-chunked copy of y
+    const long long n_units = (long long)d.B * nch4 * (d.HW / 4);
+    long long blocks = (n_units + kPackThreads - 1) / kPackThreads;
+    const long long cap = (long long)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    trace_begin(s, kKPackYf32);
+    pack_y_f32_kernel<<<(unsigned)blocks, kPackThreads, 0, s>>>(static_cast<const float*>(y), yc, d.C, d.HW, n_units);
+    trace_end(s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    // 2. the shifted-GEMM dX
+    int grid = num_sms();
+    if (grid > P.n_tiles) grid = P.n_tiles;
+    trace_begin(s, kKBwdDxTf32);
+    bwd_dx_tf32_kernel<<<grid, kThreads, L.bytes, s>>>(tmW, tmY, P);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace ddpm

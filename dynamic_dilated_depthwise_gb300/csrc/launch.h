@@ -28,7 +28,9 @@ enum KernelId : int {
     kKFilterBwdDtaps = 14,
     kKForwardTf32 = 15,
     kKBwdDyTf32 = 16,
-    kKNumKernels = 17
+    kKPackYf32 = 17,
+    kKBwdDxTf32 = 18,
+    kKNumKernels = 19
 };
 
 // Tracing hooks around each launch (cheap no-ops while tracing is off).
@@ -135,6 +137,15 @@ bool bwd_dy_tf32_eligible(const Dims& d, const void* g, const void* x, const voi
 size_t bwd_dy_tf32_wt_bytes(const Dims& d);
 cudaError_t launch_bwd_dy_tf32(const Dims& d, const void* g, const void* x, const void* w, void* dy, void* wt,
                                cudaStream_t s);
+
+// dX of FP32 problems on TF32 tensor cores (DDPM_FLAG_TF32_BACKWARD): K = 3, C a multiple
+// of 4 up to 64, W a multiple of 4, halo radius <= 6.  The launch first writes a
+// channel-chunked copy of y into `packed` (bwd_dx_tf32_bytes(d) bytes, 16-byte aligned).
+bool bwd_dx_tf32_shape_ok(const Dims& d);   // the problem alone (sizes the workspace)
+bool bwd_dx_tf32_eligible(const Dims& d, const void* g, const void* y, const void* w, const void* dx);
+size_t bwd_dx_tf32_bytes(const Dims& d);
+cudaError_t launch_bwd_dx_tf32(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
+                               void* packed, cudaStream_t s);
 
 // dY on tcgen05 tensor cores (same shapes as the dW kernel).
 bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w);

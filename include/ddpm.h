@@ -69,9 +69,12 @@ typedef enum { DDPM_FLOAT32 = 0, DDPM_BFLOAT16 = 1 } ddpm_dtype;
  *   TF32 tensor cores (the page allows TF32 for FP32 backward reductions and
  *   recompute, never for the forward).  With it the dW/dbias partial sums run
  *   on tensor cores (TF32 operands, FP32 accumulation) for K = 3, C <= 64, W a
- *   multiple of 4, dilations <= 6 and 16-byte aligned tensors, and so does dY
+ *   multiple of 4, dilations <= 6 and 16-byte aligned tensors; so does dY
  *   where C is also a multiple of 16 and the workspace holds the rearranged
- *   weight (ddpm_backward_workspace_size counts it); dX stays IEEE FP32.
+ *   weight, and so does dX's recompute of the taps (T = bias + W y as a TF32
+ *   GEMM per tap, FP32 accumulation; the products T * grad and their sum stay
+ *   IEEE FP32) where C is a multiple of 4 and the workspace holds a
+ *   channel-chunked FP32 copy of y.  ddpm_backward_workspace_size counts both.
  *   Ignored for BF16 and under DDPM_FLAG_CUDA_CORES. */
 #define DDPM_FLAG_TF32_BACKWARD 0x1u
 /* DDPM_FLAG_CUDA_CORES: run the CUDA-core (FFMA) kernels even where a
@@ -151,10 +154,13 @@ DDPM_API ddpm_status ddpm_filter_pregenerated_backward(const ddpm_problem* probl
  * image size (7.2 MB for C = 64, K = 3).  For BF16 problems whose dX runs on the
  * packed tensor-core kernel, the returned size also covers channel-chunked
  * copies of y and of the three dilation blocks of grad (4 * B * C * H * W bf16
- * elements, which does grow with the image); for FP32 problems whose dY runs on
- * TF32 tensor cores, a rearranged copy of the weight (27 * C * C FP32 values).
- * ddpm_backward accepts any workspace of at least the partials' size and then
- * stages dX's operands inside the kernel and runs an FP32 dY on CUDA cores.
+ * elements, which does grow with the image); for FP32 problems whose dY and dX
+ * run on TF32 tensor cores, a rearranged copy of the weight (27 * C * C FP32
+ * values) and a channel-chunked copy of y (B * C * H * W FP32 values, which
+ * grows with the image).  ddpm_backward accepts any workspace of at least the
+ * partials' size; with less than the returned size a BF16 dX stages its
+ * operands inside the kernel, and an FP32 dY or dX that finds no room for its
+ * copy runs on CUDA cores.
  */
 DDPM_API ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* bytes);
 

@@ -441,7 +441,13 @@ TF32_SHAPES = [
     Problem(3, 8, 5, 68, 3, (1, 6, 2)),      # halo radius 6, several images
     Problem(2, 32, 9, 36, 3, (1, 6, 2)),     # TF32 dY: ragged 4 x 32 tiles, halo radius 6, two images
     Problem(1, 48, 6, 64, 3),                # TF32 dY with N = 48
+    Problem(1, 10, 6, 36, 3),                # C % 4 != 0: dX and dY stay IEEE FP32
+    Problem(2, 20, 19, 28, 3, (3, 1, 2)),    # TF32 dX: C % 8 == 4 (a zero chunk), ragged 16 x 8 tiles
 ]
+
+
+def _tf32_dx_applies(p):
+    return p.C % 4 == 0 and p.W % 4 == 0 and max(p.dilations) * (p.K // 2) <= 6
 
 
 @pytest.mark.parametrize("p", TF32_SHAPES, ids=_id)
@@ -453,6 +459,8 @@ def test_tf32_backward_matches_oracle(p):
     assert "bwd_dw_tf32" in names and "bwd_dw_partial_simt" not in names, names
     tf32_dy = p.C % 16 == 0
     assert ("bwd_dy_tf32" in names) == tf32_dy and ("bwd_dy_simt" in names) != tf32_dy, names
+    tf32_dx = _tf32_dx_applies(p)
+    assert ("bwd_dx_tf32" in names) == tf32_dx and ("bwd_dx_simt" in names) != tf32_dx, names
     got = run_backward(d, p, flags=flags)
     ieee = run_backward(d, p)
     torch.cuda.synchronize()
@@ -460,10 +468,36 @@ def test_tf32_backward_matches_oracle(p):
     for name, a, want in zip(("dx", "dy", "dW", "dbias"), got, ref):
         assert_grad_close(a, want, "float32", name)
         assert_grad_close(ieee[("dx", "dy", "dW", "dbias").index(name)], want, "float32", name + " (IEEE)")
-    # the flag leaves dX in IEEE FP32, and dY too where the TF32 dY kernel does not apply
-    assert torch.equal(got[0], ieee[0])
+    # where a TF32 kernel does not apply the flag leaves that gradient in IEEE FP32
+    if not tf32_dx:
+        assert torch.equal(got[0], ieee[0])
     if not tf32_dy:
         assert torch.equal(got[1], ieee[1])
+
+
+def test_tf32_backward_workspace_fallbacks():
+    """A workspace without room for the copy of y keeps dX on CUDA cores (dY still on
+    TF32); the partials alone keep both there.  Each result still matches the oracle."""
+    p = Problem(1, 32, 20, 40, 3)
+    h = make_inputs(p, 851, "float32")
+    d = _dev(h)
+    flags = binding.DDPM_FLAG_TF32_BACKWARD
+    prob = binding.make_problem(p.B, p.C, p.H, p.W, p.K, p.dilations, binding.DDPM_FLOAT32, flags)
+    full = binding.ddpm_backward_workspace_size(prob)
+    ymin = binding.ddpm_backward_workspace_min(prob)
+    wt = 27 * p.C * p.C * 4
+    dy_only = (ymin + 255) // 256 * 256 + wt
+    assert full >= dy_only + p.B * p.C * p.H * p.W * 4
+    ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=False)
+    for nbytes, want in ((full, {"bwd_dx_tf32", "bwd_dy_tf32"}), (dy_only, {"bwd_dx_simt", "bwd_dy_tf32"}),
+                         (ymin, {"bwd_dx_simt", "bwd_dy_simt"})):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        names = set(_traced_kernels(lambda: run_backward(d, p, flags=flags, workspace=ws)))
+        assert want <= names, (nbytes, names)
+        got = run_backward(d, p, flags=flags, workspace=ws)
+        torch.cuda.synchronize()
+        for name, a, r in zip(("dx", "dy", "dW", "dbias"), got, ref):
+            assert_grad_close(a, r, "float32", f"{name} (workspace {nbytes})")
 
 
 @pytest.mark.parametrize("p", TF32_SHAPES, ids=_id)
