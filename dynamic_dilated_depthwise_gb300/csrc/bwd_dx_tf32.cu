@@ -8,8 +8,9 @@
 // tensor cores (FP32 accumulation).
 //
 // Two launches.
-// pack_y_f32: y is copied once into a channel-chunked layout [B][C/4][H][W][4] -- the
-//   four channels of a chunk at one pixel in 16 contiguous bytes (HBM-bound).
+// pack_f32: y and the three dilation blocks of grad are copied once into a channel-chunked
+//   layout ([B][C/4][H][W][4] and [B][3][C/4][H][W][4]) -- the four channels of a chunk at
+//   one pixel in 16 contiguous bytes (HBM-bound).
 // bwd_dx_tf32: one shifted TF32 GEMM per tap.  A persistent CTA walks 16x8 pixel tiles
 //   (MMA M = 128, slot s = r*8 + c) with all channels (N = 64):
 //   - TMA brings the tile's y window [chunk][(16+2R) x (8+2R) positions][4] from the
@@ -26,8 +27,8 @@
 //   - D of each tap lands in one of eight TMEM buffers [128 x 64]; eight worker warps
 //     accumulate tap * grad in IEEE FP32.  Four-byte grad windows of all 64 channels do
 //     not fit in shared memory beside the y window, so each worker gathers its grad
-//     values from global memory (L2), one tap ahead of their use: a warp's 32 pixels of
-//     one channel are four 32-byte sectors.
+//     values from the chunked copy in global memory (L2), two taps ahead of their use:
+//     eight 16-byte loads per tap for its pixel's 32 channels.
 #include "bwd_tc_common.cuh"
 #include "tc.cuh"
 
@@ -58,7 +59,8 @@ struct DxTf32Params {
     int tiles_w, tiles_per_img, n_tiles;
     int R, WW, WH, npos, nch4, nks, stages;
     int oyw, ooh, obt;                     // shared-memory offsets from the aligned base
-    const float* g;                        // grad, NCHW [B][4C][H][W]
+    const float* g;                        // grad, NCHW [B][4C][H][W] (block 0 gives the identity term)
+    const float4* gc;                      // grad blocks 1..3, chunked [B][3][C/4][H*W] float4
     const float* bias;                     // may be null
     float* dx;
     unsigned int* err;
@@ -92,21 +94,25 @@ DxTf32Layout dx_tf32_layout(const Dims& d) {
 }
 
 // ----------------------------------------------------------------------------- pack
-// Thread = (b, chunk, 4-pixel group): four 16-byte channel rows in, four 16-byte
-// pixel rows out.  HW is a multiple of 4 (W is).
+// Thread = (tensor, b, chunk, 4-pixel group): four 16-byte channel rows in, four 16-byte
+// pixel rows out.  Units [0, n_y) copy y ([B][C/4] chunks), the rest the grad channels
+// C .. 4C-1 ([B][3C/4] chunks).  HW is a multiple of 4 (W is).
 __global__ void __launch_bounds__(kPackThreads)
-    pack_y_f32_kernel(const float* __restrict__ y, float* __restrict__ yc, int C, long long HW, long long n_units) {
-    const int nch4 = C / 4;
+    pack_f32_kernel(const float* __restrict__ y, const float* __restrict__ g, float* __restrict__ yc,
+                    float* __restrict__ gc, int C, long long HW, long long n_y, long long n_all) {
     const long long groups = HW / 4;
-    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < n_units;
+    for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < n_all;
          u += (long long)gridDim.x * blockDim.x) {
-        const long long p4 = u % groups, bc = u / groups;   // bc = b * nch4 + cb
+        const bool is_y = u < n_y;
+        const long long v = is_y ? u : u - n_y;
+        const int nch4 = is_y ? C / 4 : 3 * C / 4;
+        const long long p4 = v % groups, bc = v / groups;   // bc = b * nch4 + cb
         const long long b = bc / nch4, cb = bc % nch4;
-        const float* src = y + (b * C + cb * 4) * HW + p4 * 4;
+        const float* src = is_y ? y + (b * C + cb * 4) * HW + p4 * 4 : g + (b * 4 * C + C + cb * 4) * HW + p4 * 4;
         float4 in[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) in[e] = __ldg(reinterpret_cast<const float4*>(src + e * HW));
-        float4* dst = reinterpret_cast<float4*>(yc + (bc * HW + p4 * 4) * 4);
+        float4* dst = reinterpret_cast<float4*>((is_y ? yc : gc) + (bc * HW + p4 * 4) * 4);
         dst[0] = make_float4(in[0].x, in[1].x, in[2].x, in[3].x);
         dst[1] = make_float4(in[0].y, in[1].y, in[2].y, in[3].y);
         dst[2] = make_float4(in[0].z, in[1].z, in[2].z, in[3].z);
@@ -115,23 +121,20 @@ __global__ void __launch_bounds__(kPackThreads)
 }
 
 // ----------------------------------------------------------------------------- dX
-// The grad values of one tap for this thread's pixel and 32 channels (zero where the
-// source pixel lies outside the image or the channel beyond C).
-__device__ __forceinline__ void gather_tap(float (&g)[32], const float* gb, int u, const DxTf32Params& P, int h, int w,
-                                           bool inside, int c0) {
+// The grad values of one tap for this thread's pixel and its 32 channels, from the
+// chunked copy gci = [3][C/4][HW] float4 of this image (zero where the source pixel lies
+// outside the image or the chunk beyond C).
+__device__ __forceinline__ void gather_tap(float4 (&g)[8], const float4* gci, int u, const DxTf32Params& P, int h,
+                                           int w, bool inside, int cq0) {
     const int dd = u / 9, k = u - dd * 9;
     const int dil = dil_of(P.d, dd);
     const int sh = h - (k / 3 - 1) * dil, sw = w - (k % 3 - 1) * dil;
     const bool valid = inside && sh >= 0 && sh < P.d.H && sw >= 0 && sw < P.d.W;
-    if (valid) {
-        const float* p = gb + (long long)((1 + dd) * P.d.C + c0) * P.d.HW + (long long)sh * P.d.W + sw;
-        const int nc = P.d.C - c0;
+    const long long HW = P.d.HW;
+    const float4* p = gci + ((long long)dd * P.nch4 + cq0) * HW + (long long)sh * P.d.W + sw;
+    const int nq = P.nch4 - cq0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = i < nc ? __ldg(p + (long long)i * P.d.HW) : 0.0f;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = 0.0f;
-    }
+    for (int j = 0; j < 8; ++j) g[j] = (valid && j < nq) ? __ldg(p + j * HW) : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -246,6 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 || warp == kIssuer2) {
         // ------------------------------------------------------- MMA issuers: taps of parity `par`
+        // An issuing thread spends tens of cycles on every instruction between two MMAs,
+        // so the loop keeps them few: ring stage, buffer and tap advance by counters (no
+        // division), the descriptors are built once and each MMA adds a 32-bit offset to
+        // the low half of one, and the eight K steps of a tap are one unrolled burst.
         const int par = warp == 1 ? 0 : 1;
         if (lane == 0 && n_my > 0) {
             const uint32_t idesc = instr_desc(2, 0, 0, 128, kN);   // TF32, both operands K-major
@@ -254,37 +261,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t w_base = smem_desc(smem_u32(sm), 16, 1024, kSwizzle128B);
             const uint64_t oh_base = smem_desc(smem_u32(sm + P.ooh), 128, 0, kSwizzleNone);
             const uint64_t bt_base = smem_desc(smem_u32(sm + P.obt), 128, 512, kSwizzleNone);
+            const uint32_t a_hi = (uint32_t)(a_base >> 32), w_hi = (uint32_t)(w_base >> 32);
+            const uint32_t oh_hi = (uint32_t)(oh_base >> 32), bt_hi = (uint32_t)(bt_base >> 32);
+            const uint32_t astep = (2 * lbo_y) >> 4;              // one K step of A, descriptor units
+            const bool full_k = P.nks == 8;
             const int nks = P.nks;
+            int st = par, sph = 0;            // W ring stage of this issuer's next tap and its phase
+            int buf = par, bph = 0;           // TMEM buffer of this issuer's next tap and its phase
             bool ok = true;
             for (int tl = 0; tl < n_my && ok; ++tl) {
                 if (!mbar_wait(&yw_full, tl & 1, P.err, abort_v)) break;
                 tc_fence_after();
-                for (int u = 0; u < kTaps; ++u) {
-                    const int i = tl * kTaps + u;             // tap counter of this CTA
-                    if ((i & 1) != par) continue;
-                    const int dd = u / 9, k = u - dd * 9;
-                    const int st = i % S, sph = (i / S) & 1;
-                    const int buf = i % kDBufs, bph = (i / kDBufs) & 1;
+                // the first tap of tile tl for this issuer: (27 tl + u) % 2 == par
+                int u = par ^ (tl & 1), dd = 0, k = u;
+                for (; u < kTaps; u += 2) {
+                    const uint32_t a_lo = (uint32_t)a_base + (a_shift[u] >> 4);
+                    const uint32_t w_lo = (uint32_t)w_base + (uint32_t)((st * kWTile) >> 4);
+                    const uint32_t oh_lo = (uint32_t)oh_base + (uint32_t)(k * 32);
+                    const uint32_t bt_lo = (uint32_t)bt_base + (uint32_t)(dd * 256);
+                    const uint32_t dt = tmem + (uint32_t)(buf * kN);
                     if (!mbar_wait(&wt_full[st], sph, P.err, abort_v) ||
                         !mbar_wait(&d_empty[buf], bph ^ 1, P.err, abort_v)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a = desc_advance(a_base, a_shift[u]);
-                    const uint64_t b = desc_advance(w_base, (uint32_t)st * kWTile);
-                    const uint32_t dt = tmem + buf * kN;
+                    if (full_k) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        if (kk < nks)
-                            mma_tf32(dt, desc_advance(a, 2 * kk * lbo_y),
-                                     desc_advance(b, (uint32_t)((kk >> 2) * kWAtom + (kk & 3) * 32)), idesc,
-                                     kk > 0 ? 1u : 0u);
-                    mma_tf32(dt, desc_advance(oh_base, k * 512), desc_advance(bt_base, dd * 4096), idesc, 1u);
-                    mma_tf32(dt, desc_advance(oh_base, k * 512 + 256), desc_advance(bt_base, dd * 4096 + 256), idesc,
-                             1u);
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_tf32_lh(dt, a_lo + kk * astep, a_hi,
+                                        w_lo + (uint32_t)(((kk >> 2) * kWAtom + (kk & 3) * 32) >> 4), w_hi, idesc,
+                                        kk > 0 ? 1u : 0u);
+                    } else {
+                        for (int kk = 0; kk < nks; ++kk)
+                            mma_tf32_lh(dt, a_lo + kk * astep, a_hi,
+                                        w_lo + (uint32_t)(((kk >> 2) * kWAtom + (kk & 3) * 32) >> 4), w_hi, idesc,
+                                        kk > 0 ? 1u : 0u);
+                    }
+                    mma_tf32_lh(dt, oh_lo, oh_hi, bt_lo, bt_hi, idesc, 1u);
+                    mma_tf32_lh(dt, oh_lo + 16, oh_hi, bt_lo + 16, bt_hi, idesc, 1u);
                     mma_commit(&d_full[buf]);
                     mma_commit(&wt_empty[st]);
+                    st += 2;
+                    if (st >= S) {
+                        st -= S;
+                        sph ^= 1;
+                    }
+                    buf += 2;
+                    if (buf >= kDBufs) {
+                        buf -= kDBufs;
+                        bph ^= 1;
+                    }
+                    k += 2;
+                    if (k >= 9) {
+                        k -= 9;
+                        ++dd;
+                    }
                 }
                 if (ok) mma_commit(&yw_empty);
             }
@@ -299,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = q * 32 + lane;                    // slot == TMEM lane
         const int r = s >> 3, c = s & 7;
         const int c0 = hc * 32;
+        const long long gimg = 3LL * P.nch4 * HW;   // float4 per image of the chunked grad
         bool ok = true;
         for (int tl = 0; tl < n_my && ok; ++tl) {
             const int t = blockIdx.x + tl * gridDim.x;
@@ -307,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool inside = h < H && w < W;
             const long long pix = inside ? (long long)h * W + w : 0;
             const float* gb = P.g + (long long)b * 4 * C * HW;
+            const float4* gci = P.gc + (long long)b * gimg;
             // the identity term (channel block 0) is prefetched into L2 now and loaded last
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -314,11 +348,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             float acc[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
-            float ga[32], gn[32];
-            gather_tap(ga, gb, 0, P, h, w, inside, c0);
-            // one tap: wait for its accumulator, read this thread's 32 channels, start the
-            // next tap's gather, hand the buffer back, accumulate
-            auto step = [&](int u, float(&gcur)[32], float(&gnext)[32], bool load_next) {
+            // the grad of tap u sits in buffer u % 2; it is consumed after tap u's accumulator
+            // has been read and the buffer is refilled at once with tap u + 2, so every gather
+            // has two taps' time to arrive
+            float4 ga[8], gb2[8];
+            gather_tap(ga, gci, 0, P, h, w, inside, c0 / 4);
+            gather_tap(gb2, gci, 1, P, h, w, inside, c0 / 4);
+            auto step = [&](int u, float4(&g)[8]) {
                 const int i = tl * kTaps + u, buf = i % kDBufs;
                 if (!__all_sync(0xffffffffu, mbar_wait(&d_full[buf], (i / kDBufs) & 1, P.err, abort_v))) {
                     ok = false;
@@ -329,19 +365,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * kN + c0;
                 DDPM_TMEM_LD_X16(ta, (v + 0));
                 DDPM_TMEM_LD_X16(ta + 16, (v + 16));
-                if (load_next) gather_tap(gnext, gb, u + 1, P, h, w, inside, c0);
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&d_empty[buf]);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = fmaf(__uint_as_float(v[e]), gcur[e], acc[e]);
+                for (int j = 0; j < 8; ++j) {
+                    acc[4 * j + 0] = fmaf(__uint_as_float(v[4 * j + 0]), g[j].x, acc[4 * j + 0]);
+                    acc[4 * j + 1] = fmaf(__uint_as_float(v[4 * j + 1]), g[j].y, acc[4 * j + 1]);
+                    acc[4 * j + 2] = fmaf(__uint_as_float(v[4 * j + 2]), g[j].z, acc[4 * j + 2]);
+                    acc[4 * j + 3] = fmaf(__uint_as_float(v[4 * j + 3]), g[j].w, acc[4 * j + 3]);
+                }
+                if (u + 2 < kTaps) gather_tap(g, gci, u + 2, P, h, w, inside, c0 / 4);
             };
             for (int u = 0; u + 1 < kTaps && ok; u += 2) {
-                step(u, ga, gn, true);
-                if (ok) step(u + 1, gn, ga, true);
+                step(u, ga);
+                if (ok) step(u + 1, gb2);
             }
-            if (ok) step(kTaps - 1, ga, gn, false);
+            if (ok) step(kTaps - 1, ga);
             if (!ok) break;
             if (inside) {
                 const float* g0p = gb + (long long)c0 * HW + pix;
@@ -375,7 +416,7 @@ bool bwd_dx_tf32_eligible(const Dims& d, const void* g, const void* y, const voi
     return bwdtc::encode_fn() != nullptr;
 }
 
-size_t bwd_dx_tf32_bytes(const Dims& d) { return (size_t)d.B * (size_t)d.C * (size_t)d.HW * sizeof(float); }
+size_t bwd_dx_tf32_bytes(const Dims& d) { return (size_t)4 * d.B * (size_t)d.C * (size_t)d.HW * sizeof(float); }
 
 cudaError_t launch_bwd_dx_tf32(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
                                void* packed, cudaStream_t s) {
@@ -389,6 +430,7 @@ cudaError_t launch_bwd_dx_tf32(const Dims& d, const void* g, const void* y, cons
     auto enc = bwdtc::encode_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     float* yc = static_cast<float*>(packed);
+    float* gc = yc + (size_t)d.B * d.C * d.HW;
     const int nch4 = d.C / 4;
 
     DxTf32Params P;
@@ -407,6 +449,7 @@ cudaError_t launch_bwd_dx_tf32(const Dims& d, const void* g, const void* y, cons
     P.ooh = L.ooh;
     P.obt = L.obt;
     P.g = static_cast<const float*>(g);
+    P.gc = reinterpret_cast<const float4*>(gc);
     P.bias = static_cast<const float*>(bias);
     P.dx = static_cast<float*>(dx);
     P.err = device_error_word();
@@ -438,13 +481,15 @@ cudaError_t launch_bwd_dx_tf32(const Dims& d, const void* g, const void* y, cons
             return cudaErrorInvalidValue;
     }
 
-    // 1. the channel-chunked copy of y
-    const long long n_units = (long long)d.B * nch4 * (d.HW / 4);
-    long long blocks = (n_units + kPackThreads - 1) / kPackThreads;
+    // 1. the channel-chunked copies of y and of the three dilation blocks of grad
+    const long long n_y = (long long)d.B * nch4 * (d.HW / 4), n_all = 4 * n_y;
+    long long blocks = (n_all + kPackThreads - 1) / kPackThreads;
     const long long cap = (long long)num_sms() * 8;
     if (blocks > cap) blocks = cap;
-    trace_begin(s, kKPackYf32);
-    pack_y_f32_kernel<<<(unsigned)blocks, kPackThreads, 0, s>>>(static_cast<const float*>(y), yc, d.C, d.HW, n_units);
+    trace_begin(s, kKPackF32);
+    pack_f32_kernel<<<(unsigned)blocks, kPackThreads, 0, s>>>(static_cast<const float*>(y),
+                                                              static_cast<const float*>(g), yc, gc, d.C, d.HW, n_y,
+                                                              n_all);
     trace_end(s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -28,7 +28,7 @@ enum KernelId : int {
     kKFilterBwdDtaps = 14,
     kKForwardTf32 = 15,
     kKBwdDyTf32 = 16,
-    kKPackYf32 = 17,
+    kKPackF32 = 17,
     kKBwdDxTf32 = 18,
     kKNumKernels = 19
 };
@@ -139,8 +139,9 @@ cudaError_t launch_bwd_dy_tf32(const Dims& d, const void* g, const void* x, cons
                                cudaStream_t s);
 
 // dX of FP32 problems on TF32 tensor cores (DDPM_FLAG_TF32_BACKWARD): K = 3, C a multiple
-// of 4 up to 64, W a multiple of 4, halo radius <= 6.  The launch first writes a
-// channel-chunked copy of y into `packed` (bwd_dx_tf32_bytes(d) bytes, 16-byte aligned).
+// of 4 up to 64, W a multiple of 4, halo radius <= 6.  The launch first writes
+// channel-chunked copies of y and of grad's three dilation blocks into `packed`
+// (bwd_dx_tf32_bytes(d) bytes, 16-byte aligned).
 bool bwd_dx_tf32_shape_ok(const Dims& d);   // the problem alone (sizes the workspace)
 bool bwd_dx_tf32_eligible(const Dims& d, const void* g, const void* y, const void* w, const void* dx);
 size_t bwd_dx_tf32_bytes(const Dims& d);

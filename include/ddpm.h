@@ -73,8 +73,9 @@ typedef enum { DDPM_FLOAT32 = 0, DDPM_BFLOAT16 = 1 } ddpm_dtype;
  *   where C is also a multiple of 16 and the workspace holds the rearranged
  *   weight, and so does dX's recompute of the taps (T = bias + W y as a TF32
  *   GEMM per tap, FP32 accumulation; the products T * grad and their sum stay
- *   IEEE FP32) where C is a multiple of 4 and the workspace holds a
- *   channel-chunked FP32 copy of y.  ddpm_backward_workspace_size counts both.
+ *   IEEE FP32) where C is a multiple of 4 and the workspace holds
+ *   channel-chunked FP32 copies of y and of grad's three dilation blocks.
+ *   ddpm_backward_workspace_size counts both.
  *   Ignored for BF16 and under DDPM_FLAG_CUDA_CORES. */
 #define DDPM_FLAG_TF32_BACKWARD 0x1u
 /* DDPM_FLAG_CUDA_CORES: run the CUDA-core (FFMA) kernels even where a
@@ -156,8 +157,8 @@ DDPM_API ddpm_status ddpm_filter_pregenerated_backward(const ddpm_problem* probl
  * copies of y and of the three dilation blocks of grad (4 * B * C * H * W bf16
  * elements, which does grow with the image); for FP32 problems whose dY and dX
  * run on TF32 tensor cores, a rearranged copy of the weight (27 * C * C FP32
- * values) and a channel-chunked copy of y (B * C * H * W FP32 values, which
- * grows with the image).  ddpm_backward accepts any workspace of at least the
+ * values) and channel-chunked copies of y and of the three dilation blocks of
+ * grad (4 * B * C * H * W FP32 values, which grow with the image).  ddpm_backward accepts any workspace of at least the
  * partials' size; with less than the returned size a BF16 dX stages its
  * operands inside the kernel, and an FP32 dY or dX that finds no room for its
  * copy runs on CUDA cores.

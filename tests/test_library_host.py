@@ -169,15 +169,15 @@ def test_wait_probe_rejects_limits_out_of_range(lib):
 def test_fp32_tf32_workspace_adds_rearranged_weight(lib, C, tf32_dy):
     """FP32 problems with DDPM_FLAG_TF32_BACKWARD: where the TF32 dY kernel applies
     (C a multiple of 16), the workspace also holds the rearranged weight (27*C*C FP32);
-    where the TF32 dX applies (C a multiple of 4), it then holds, 256-byte aligned, a
-    channel-chunked FP32 copy of y (B*C*H*W values)."""
+    where the TF32 dX applies (C a multiple of 4), it then holds, 256-byte aligned,
+    channel-chunked FP32 copies of y and of grad's three dilation blocks (4*B*C*H*W values)."""
     p = _prob(B=1, C=C, H=64, W=64, K=3, flags=binding.DDPM_FLAG_TF32_BACKWARD)
     n = binding.ddpm_backward_workspace_size(p)
     parts = _partials_bytes(1, C, 64, 64, 3)
     up = lambda v: (v + 255) // 256 * 256
     wt = 27 * C * C * 4 if tf32_dy else 0
     if C % 4 == 0:
-        assert n == up(up(parts) + wt) + C * 64 * 64 * 4
+        assert n == up(up(parts) + wt) + 4 * C * 64 * 64 * 4
     elif tf32_dy:
         assert n == up(parts) + wt
     else:

@@ -487,7 +487,7 @@ def test_tf32_backward_workspace_fallbacks():
     ymin = binding.ddpm_backward_workspace_min(prob)
     wt = 27 * p.C * p.C * 4
     dy_only = (ymin + 255) // 256 * 256 + wt
-    assert full >= dy_only + p.B * p.C * p.H * p.W * 4
+    assert full >= dy_only + 4 * p.B * p.C * p.H * p.W * 4
     ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=False)
     for nbytes, want in ((full, {"bwd_dx_tf32", "bwd_dy_tf32"}), (dy_only, {"bwd_dx_simt", "bwd_dy_tf32"}),
                          (ymin, {"bwd_dx_simt", "bwd_dy_simt"})):
