@@ -456,43 +456,71 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     } else if (warp == 1 || warp == kPIssuer2) {
         // ------------------------------------------------------- MMA issuers: taps of parity `par`
+        // An issuing thread spends tens of cycles on every instruction between two MMAs, so
+        // the loop keeps them few: stage, buffer and tap advance by counters (no division),
+        // the descriptors are built once and each MMA adds a 32-bit offset to the low half
+        // of one, and the K steps of a tap are one unrolled burst.
         const int par = warp == 1 ? 0 : 1;
         if (lane == 0 && n_my > 0) {
-            // descriptors are built once; each MMA only moves a start address (desc_advance)
             const uint32_t idesc = instr_desc(1, 0, 0, 128, kPN);
             const uint32_t lbo_y = (uint32_t)P.npos * 16, sbo_y = (uint32_t)P.WW * 16;
             const uint64_t a_base = smem_desc(smem_u32(sm + P.oyw), lbo_y, sbo_y, kSwizzleNone);
             const uint64_t w_base = smem_desc(smem_u32(sm), 16, 1024, kSwizzle128B);
             const uint64_t oh_base = smem_desc(smem_u32(sm + P.ooh), 128, 0, kSwizzleNone);
             const uint64_t bt_base = smem_desc(smem_u32(sm + P.obt), 128, 256, kSwizzleNone);
+            const uint32_t a_hi = (uint32_t)(a_base >> 32), w_hi = (uint32_t)(w_base >> 32);
+            const uint32_t oh_hi = (uint32_t)(oh_base >> 32), bt_hi = (uint32_t)(bt_base >> 32);
+            const uint32_t astep = (2 * lbo_y) >> 4;              // one K step of A, descriptor units
             const int nks = P.nks;
+            const bool full_k = nks == 4;
+            int st = par, sph = 0;            // W ring stage of this issuer's next tap and its phase
+            int buf = par, bph = 0;           // TMEM buffer of this issuer's next tap and its phase
             bool ok = true;
             for (int tl = 0; tl < n_my && ok; ++tl) {
                 if (!mbar_wait(&yw_full, tl & 1, P.err, abort_v)) break;
                 tc_fence_after();
-                for (int u = 0; u < kPTaps; ++u) {
-                    const int i = tl * kPTaps + u;             // global tap counter of this CTA
-                    if ((i & 1) != par) continue;
-                    const int dd = u / 9, k = u - dd * 9;
-                    const int st = i % S, sph = (i / S) & 1;   // W ring stage and its phase parity
-                    const int buf = i % kPDBufs, bph = (i / kPDBufs) & 1;
+                // the first tap of tile tl for this issuer: (27 tl + u) % 2 == par
+                int u = par ^ (tl & 1), dd = 0, k = u;
+                for (; u < kPTaps; u += 2) {
+                    const uint32_t a_lo = (uint32_t)a_base + (a_shift[u] >> 4);
+                    const uint32_t w_lo = (uint32_t)w_base + (uint32_t)((st * kPWTile) >> 4);
+                    const uint32_t oh_lo = (uint32_t)oh_base + (uint32_t)(k * 16);
+                    const uint32_t bt_lo = (uint32_t)bt_base + (uint32_t)(dd * 128);
+                    const uint32_t dt = tmem + (uint32_t)(buf * kPN);
                     if (!mbar_wait(&wt_full[st], sph, P.err, abort_v) ||
                         !mbar_wait(&d_empty[buf], bph ^ 1, P.err, abort_v)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a = desc_advance(a_base, a_shift[dd * 9 + k]);
-                    const uint64_t b = desc_advance(w_base, (uint32_t)st * kPWTile);
-                    const uint32_t dt = tmem + buf * kPN;
+                    if (full_k) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        if (kk < nks)
-                            mma_f16(dt, desc_advance(a, 2 * kk * lbo_y), desc_advance(b, kk * 32), idesc,
-                                    kk > 0 ? 1u : 0u);
-                    mma_f16(dt, desc_advance(oh_base, k * 256), desc_advance(bt_base, dd * 2048), idesc, 1u);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f16_lh(dt, a_lo + kk * astep, a_hi, w_lo + (uint32_t)(kk * 2), w_hi, idesc,
+                                       kk > 0 ? 1u : 0u);
+                    } else {
+                        for (int kk = 0; kk < nks; ++kk)
+                            mma_f16_lh(dt, a_lo + kk * astep, a_hi, w_lo + (uint32_t)(kk * 2), w_hi, idesc,
+                                       kk > 0 ? 1u : 0u);
+                    }
+                    mma_f16_lh(dt, oh_lo, oh_hi, bt_lo, bt_hi, idesc, 1u);
                     mma_commit(&d_full[buf]);
                     mma_commit(&wt_empty[st]);
+                    st += 2;
+                    if (st >= S) {
+                        st -= S;
+                        sph ^= 1;
+                    }
+                    buf += 2;
+                    if (buf >= kPDBufs) {
+                        buf -= kPDBufs;
+                        bph ^= 1;
+                    }
+                    k += 2;
+                    if (k >= 9) {
+                        k -= 9;
+                        ++dd;
+                    }
                 }
                 if (ok) mma_commit(&yw_empty);
             }

@@ -341,10 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long pix = inside ? (long long)h * W + w : 0;
             const float* gb = P.g + (long long)b * 4 * C * HW;
             const float4* gci = P.gc + (long long)b * gimg;
-            // the identity term (channel block 0) is prefetched into L2 now and loaded last
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(gb + (long long)min(c0 + i, C - 1) * HW + pix));
+            // the identity term (channel block 0) is loaded after the gather (an L2 prefetch of
+            // it here cost the workers more at every tile change than it saved)
             float acc[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
