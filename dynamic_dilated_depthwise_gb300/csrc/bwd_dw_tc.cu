@@ -9,13 +9,14 @@
 //   ws[s][o][C] = sum_p dK[o, p]                                    (dbias)
 //
 // GB300 design.  A CTA owns a block of taps -- 14 channels of one dilation,
-// 126 taps, padded to the MMA M of 128 -- and one pixel split.  Per 2x64
+// 126 taps, for K = 3, or 5 channels, 125 taps, for K = 5, padded to the MMA M
+// of 128 -- and one pixel split.  Per 2x64
 // pixel tile:
 //   - one producer warp's TMA brings y [64 j x 128 px] (one 128-byte row per
 //     channel and tile row, 128B-swizzled: a K-major operand) into a 3-stage
 //     ring that the MMA releases;
-//   - another brings the block's 14 grad planes [14 x 128 px] and the matching
-//     x windows [14 x (2+2R) x 80 px], zero-filled outside the image, into a
+//   - another brings the block's grad planes [CB x 128 px] and the matching
+//     x windows [CB x (2+2R) x (64 + 2 halo) px], zero-filled outside the image, into a
 //     ring of 2-4 stages (as many as shared memory holds for the halo) that
 //     the formers release as soon as dK is formed;
 //   - eight warps form dK^T[o, px] (bwdtc::form_dk_tile) into a 128B-swizzled
@@ -46,21 +47,24 @@ constexpr int kYS = kDK + 2 * kDKBytes;              // y ring: stages x 2 halve
 constexpr int kYHalf = kNY * 128;                    // 10240
 constexpr int kYStage = 2 * kYHalf;                  // 20480
 constexpr int kXG = kYS + kYStages * kYStage;        // x/grad ring
-constexpr int kGStage = kCB * kPx * 2;               // grad planes of the block [14 x 128 px] bf16
+template <int K>
+__host__ __device__ constexpr int gstage_bytes() { return BwdGeom<K>::kCB * kPx * 2; }   // grad planes of the block [CB x 128 px] bf16
 constexpr int kSlack = 1024 + 128;                   // alignment slack + over-read margin
 static_assert(kYS % 1024 == 0 && kYStage % 1024 == 0 && kYHalf % 1024 == 0, "SW128 atoms need 1 KiB");
-static_assert(kXG % 128 == 0 && kGStage % 128 == 0, "TMA dst 128 B");
+static_assert(kXG % 128 == 0 && gstage_bytes<3>() % 128 == 0 && gstage_bytes<5>() % 128 == 0, "TMA dst 128 B");
 
 struct XgLayout {
     int stage_bytes;   // grad planes + x windows, rounded up to 128 B
     int stages;        // 0 when even two stages do not fit
 };
 
-// The x/grad stage holds the block's grad planes and its x windows [14 x (2+2R) x 80].
+// The x/grad stage holds the block's grad planes and its x windows [CB x (2+2R) x cols].
+template <int K>
 inline XgLayout xg_layout(int R) {
+    using G = BwdGeom<K>;
     XgLayout L;
-    const int xbytes = kCB * (kTH + 2 * R) * kWinCols * 2;
-    L.stage_bytes = (kGStage + xbytes + 127) / 128 * 128;
+    const int xbytes = G::kCB * (kTH + 2 * R) * G::kWinCols * 2;
+    L.stage_bytes = (gstage_bytes<K>() + xbytes + 127) / 128 * 128;
     int n = (kSmemCap - kSlack - kXG) / L.stage_bytes;
     L.stages = n > kMaxXgStages ? kMaxXgStages : (n < 2 ? 0 : n);
     return L;
@@ -69,11 +73,11 @@ inline XgLayout xg_layout(int R) {
 struct DwTcParams {
     Dims d;
     int tiles_w, tiles_per_img, n_tiles;
-    int n_cblk;        // ceil(C / 14) blocks of channels per dilation
+    int n_cblk;        // ceil(C / CB) blocks of channels per dilation
     int n_oblk;        // 3 * n_cblk
     int tiles_per_split;
     int R, WHx;        // halo radius, window rows (2 + 2R)
-    int xslot_bytes;   // WHx * 80 * 2
+    int xslot_bytes;   // WHx * window columns * 2
     int xg_stage, xg_stages;
     float* ws;         // [S][O][C+1]
     unsigned int* err;
@@ -84,10 +88,13 @@ struct DwTcParams {
 // The formers release the x/grad stage (xg_empty) as soon as dK^T is formed, and the
 // MMA releases the y stage and the dK^T buffer through commits, so the next windows
 // load while the tensor cores still read the previous tile.
+template <int K>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dw_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmG,
                      const __grid_constant__ CUtensorMap tmX, const DwTcParams P) {
     using namespace tc;
+    using G = BwdGeom<K>;
+    constexpr int kCB = G::kCB, kTaps = K * K, kGStage = gstage_bytes<K>();
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB-aligned base, derived by pointer arithmetic on the shared array so that every
     // access through it stays a shared-memory access (an integer round trip would make
@@ -113,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dd = ob / P.n_cblk;
     const int c_first = (ob % P.n_cblk) * kCB;
     const int nc = min(kCB, C - c_first);
-    const int nrows = nc * 9;
+    const int nrows = nc * kTaps;
     const int dil = dil_of(P.d, dd);
 
     if (threadIdx.x == 0) {
@@ -143,8 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t v = row == 0 ? 0x3F803F80u : 0u;  // bf16 pair (1.0, 1.0)
             reinterpret_cast<uint32_t*>(sm + kYS + st * kYStage + half * kYHalf + (64 + row) * 128)[word] = v;
         }
-        zero_dk_pad_rows(sm + kDK, et, 32 * kFormWarps);
-        zero_dk_pad_rows(sm + kDK + kDKBytes, et, 32 * kFormWarps);
+        zero_dk_pad_rows<K>(sm + kDK, et, 32 * kFormWarps);
+        zero_dk_pad_rows<K>(sm + kDK + kDKBytes, et, 32 * kFormWarps);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* st = sm + kXG + s * P.xg_stage;
                 mbar_arrive_expect_tx(&xg_full[s], bytes);
                 tma_load_4d(st, &tmG, &xg_full[s], w0, h0, (1 + dd) * C + c_first, b);
-                tma_load_4d(st + kGStage, &tmX, &xg_full[s], w0 - 8, h0 - P.R, c_first, b);
+                tma_load_4d(st + kGStage, &tmX, &xg_full[s], w0 - G::kHaloCols, h0 - P.R, c_first, b);
                 issued = i + 1;
             }
             // drain: every copy this thread started lands before its shared memory is released
@@ -242,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const uint8_t* st = sm + kXG + sx * P.xg_stage;
-            form_dk_tile(sm + kDK + s * kDKBytes, reinterpret_cast<const uint32_t*>(st + kGStage),
+            form_dk_tile<K>(sm + kDK + s * kDKBytes, reinterpret_cast<const uint32_t*>(st + kGStage),
                          reinterpret_cast<const bf16*>(st), kPx, nrows, slot_elems, P.R, dil, 0, et, 32 * kFormWarps);
             fence_proxy_async_smem();
             __syncwarp();
@@ -254,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue: this split's partial sums for the block of taps
         const int q = warp & 3, hc = (warp - 2) >> 2;
         const int row = q * 32 + lane;
-        const int rc = row / 9;
-        const long long o = (long long)(dd * C + c_first + rc) * 9 + (row - rc * 9);
+        const int rc = row / kTaps;
+        const long long o = (long long)(dd * C + c_first + rc) * kTaps + (row - rc * kTaps);
         float* wsrow = P.ws + ((long long)split * O + o) * (C + 1);
         uint32_t v[40];
         if (n_my > 0) {
@@ -290,14 +297,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+template <int K>
+cudaError_t launch_k(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S, cudaStream_t s) {
+    using G = BwdGeom<K>;
+    static int attr_done[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dw_tc_kernel<K>, kSmemCap, attr_done);
+        if (e != cudaSuccess) return e;
+    }
+    DwTcParams P;
+    P.d = d;
+    P.tiles_w = (d.W + kTW - 1) / kTW;
+    P.tiles_per_img = ((d.H + kTH - 1) / kTH) * P.tiles_w;
+    P.n_tiles = d.B * P.tiles_per_img;
+    P.n_cblk = (d.C + G::kCB - 1) / G::kCB;
+    P.n_oblk = 3 * P.n_cblk;
+    P.tiles_per_split = (P.n_tiles + S - 1) / S;
+    P.R = d.R();
+    P.WHx = kTH + 2 * P.R;
+    P.xslot_bytes = P.WHx * G::kWinCols * 2;
+    const XgLayout L = xg_layout<K>(P.R);
+    if (L.stages < 2) return cudaErrorInvalidValue;
+    P.xg_stage = L.stage_bytes;
+    P.xg_stages = L.stages;
+    const int smem_bytes = kXG + L.stages * L.stage_bytes + kSlack;
+    P.ws = ws;
+    P.err = device_error_word();
+    if (P.err == nullptr) return cudaErrorUnknown;
+    CUtensorMap tmY, tmG, tmX;
+    if (!encode_nchw(&tmY, y, d, d.C, kTW, 1, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_nchw(&tmG, g, d, 4 * d.C, kTW, kTH, G::kCB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_nchw(&tmX, x, d, d.C, G::kWinCols, (uint32_t)P.WHx, G::kCB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    trace_begin(s, kKBwdDwTc);
+    bwd_dw_tc_kernel<K><<<P.n_oblk * S, kThreads, smem_bytes, s>>>(tmY, tmG, tmX, P);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool bwd_dw_tc_eligible(const Dims& d, const void* g, const void* x, const void* y) {
-    return bwdtc::eligible(d, g, x, y) && xg_layout(d.R()).stages >= 2;
+    if (!bwdtc::eligible(d, g, x, y, true)) return false;
+    return (d.K == 3 ? xg_layout<3>(d.R()).stages : xg_layout<5>(d.R()).stages) >= 2;
 }
 
 int bwd_dw_tc_splits(const Dims& d, size_t workspace_bytes) {
-    const int n_oblk = 3 * ((d.C + kCB - 1) / kCB);
+    const int cb = d.K == 3 ? BwdGeom<3>::kCB : BwdGeom<5>::kCB;
+    const int n_oblk = 3 * ((d.C + cb - 1) / cb);
     const long long n_tiles = (long long)d.B * ((d.H + kTH - 1) / kTH) * ((d.W + kTW - 1) / kTW);
     int S = num_sms() / n_oblk;
     if (S < 1) S = 1;
@@ -310,39 +357,7 @@ int bwd_dw_tc_splits(const Dims& d, size_t workspace_bytes) {
 
 cudaError_t launch_bwd_dw_tc(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S,
                              cudaStream_t s) {
-    static int attr_done[64] = {};
-    {
-        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dw_tc_kernel, kSmemCap, attr_done);
-        if (e != cudaSuccess) return e;
-    }
-    DwTcParams P;
-    P.d = d;
-    P.tiles_w = (d.W + kTW - 1) / kTW;
-    P.tiles_per_img = ((d.H + kTH - 1) / kTH) * P.tiles_w;
-    P.n_tiles = d.B * P.tiles_per_img;
-    P.n_cblk = (d.C + kCB - 1) / kCB;
-    P.n_oblk = 3 * P.n_cblk;
-    P.tiles_per_split = (P.n_tiles + S - 1) / S;
-    P.R = d.R();
-    P.WHx = kTH + 2 * P.R;
-    P.xslot_bytes = P.WHx * kWinCols * 2;
-    const XgLayout L = xg_layout(P.R);
-    if (L.stages < 2) return cudaErrorInvalidValue;
-    P.xg_stage = L.stage_bytes;
-    P.xg_stages = L.stages;
-    const int smem_bytes = kXG + L.stages * L.stage_bytes + kSlack;
-    P.ws = ws;
-    P.err = device_error_word();
-    if (P.err == nullptr) return cudaErrorUnknown;
-    CUtensorMap tmY, tmG, tmX;
-    if (!encode_nchw(&tmY, y, d, d.C, kTW, 1, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_nchw(&tmG, g, d, 4 * d.C, kTW, kTH, kCB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_nchw(&tmX, x, d, d.C, kWinCols, (uint32_t)P.WHx, kCB, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    trace_begin(s, kKBwdDwTc);
-    bwd_dw_tc_kernel<<<P.n_oblk * S, kThreads, smem_bytes, s>>>(tmY, tmG, tmX, P);
-    trace_end(s);
-    return cudaGetLastError();
+    return d.K == 3 ? launch_k<3>(d, g, x, y, ws, S, s) : launch_k<5>(d, g, x, y, ws, S, s);
 }
 
 }  // namespace ddpm

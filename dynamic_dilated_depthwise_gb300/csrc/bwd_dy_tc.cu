@@ -7,10 +7,11 @@
 //
 // GB300 design.  Persistent CTAs walk super tiles of 8 rows x 64 columns (four
 // 2x64 sub-tiles, 512 pixels).  For each super tile the CTA visits every block
-// of taps (14 channels of one dilation, 126 taps); per block one producer
+// of taps (14 channels of one dilation, 126 taps, for K = 3; 5 channels, 125
+// taps, for K = 5); per block one producer
 // warp's TMA brings the block's W rows [128 o x 64 j] into a 3-stage ring that
-// the MMA releases, and another brings its grad planes [14 x 512 px] and x
-// windows [14 x (8+2R) x 80] into a 2-stage ring that the formers release once
+// the MMA releases, and another brings its grad planes [CB x 512 px] and x
+// windows [CB x (8+2R) x (64 + 2 halo)] into a 2-stage ring that the formers release once
 // the four sub-tiles are formed; per block:
 //   - eight warps form each sub-tile's dK^T tile (bwdtc::form_dk_tile);
 //   - one thread issues D_st[px, j] += dK[px, o] * W[o, j] (M = 128 pixels read
@@ -29,12 +30,11 @@ constexpr int kN = 64;            // MMA N: output channels j (zero padded beyon
 constexpr int kSub = 4;           // 2x64 sub-tiles per super tile
 constexpr int kSTH = kSub * kTH;  // 8 rows
 constexpr int kSPx = kSub * kPx;  // 512 pixels
-constexpr int kDyMaxR = 5;        // halo radius the window buffers hold
+constexpr int kDyMaxR = 5;        // K = 3: halo radius the window buffers hold (10 for K = 5)
 constexpr int kFormWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kWWarp = 2 + kFormWarps + kEpiWarps;   // warp of the W producer
 constexpr int kThreads = 32 * (3 + kFormWarps + kEpiWarps);
-constexpr int kWinRowsMax = kSTH + 2 * kDyMaxR;   // 18
 constexpr int kWStages = 3, kXgStages = 2;
 
 // shared memory (bytes from a 1024-aligned base)
@@ -42,11 +42,20 @@ constexpr int kDK = 0;                               // 2 x dK^T tiles
 constexpr int kWS = kDK + 2 * kDKBytes;              // W ring: stages x W block [128 o x 128 B] SW128
 constexpr int kWStage = kBlockRows * 128;            // 16384
 constexpr int kXG = kWS + kWStages * kWStage;        // x/grad ring
-constexpr int kGStage = kCB * kSPx * 2;              // grad planes [14 x 512 px] bf16
-constexpr int kXgStage = kGStage + kCB * kWinRowsMax * kWinCols * 2;   // + x windows [14 x rows x 80] bf16
-constexpr int kSmemBytes = kXG + kXgStages * kXgStage + 1024 + 128;   // + alignment slack + over-read margin
 static_assert(kWS % 1024 == 0 && kWStage % 1024 == 0, "SW128 atoms need 1 KiB");
-static_assert(kXG % 128 == 0 && kGStage % 128 == 0 && kXgStage % 128 == 0, "TMA dst 128 B");
+
+// The x/grad stage of kernel size K: grad planes [CB x 512 px] and x windows
+// [CB x (8 + 2 maxR) x cols], bf16.
+template <int K>
+struct DyLayout {
+    using G = BwdGeom<K>;
+    static constexpr int kMaxR = K == 3 ? kDyMaxR : 10;
+    static constexpr int kGStage = G::kCB * kSPx * 2;
+    static constexpr int kXgStage = kGStage + G::kCB * (kSTH + 2 * kMaxR) * G::kWinCols * 2;
+    static constexpr int kSmemBytes = kXG + kXgStages * kXgStage + 1024 + 128;   // + alignment slack + over-read margin
+    static_assert(kXG % 128 == 0 && kGStage % 128 == 0 && kXgStage % 128 == 0, "TMA dst 128 B");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
 
 struct DyTcParams {
     Dims d;
@@ -57,10 +66,14 @@ struct DyTcParams {
     unsigned int* err;
 };
 
+template <int K>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dy_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
                      const __grid_constant__ CUtensorMap tmX, const DyTcParams P) {
     using namespace tc;
+    using G = BwdGeom<K>;
+    using L = DyLayout<K>;
+    constexpr int kCB = G::kCB, kTaps = K * K, kGStage = L::kGStage, kXgStage = L::kXgStage;
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB-aligned base, derived by pointer arithmetic on the shared array so that every
     // access through it stays a shared-memory access (an integer round trip would make
@@ -98,8 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) tmem_alloc(&tmem_slot, 512);
     if (warp >= 2 && warp < 2 + kFormWarps) {
-        zero_dk_pad_rows(sm + kDK, threadIdx.x - 64, 32 * kFormWarps);
-        zero_dk_pad_rows(sm + kDK + kDKBytes, threadIdx.x - 64, 32 * kFormWarps);
+        zero_dk_pad_rows<K>(sm + kDK, threadIdx.x - 64, 32 * kFormWarps);
+        zero_dk_pad_rows<K>(sm + kDK + kDKBytes, threadIdx.x - 64, 32 * kFormWarps);
         tc::fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -129,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* st = sm + kXG + s * kXgStage;
                     mbar_arrive_expect_tx(&xg_full[s], bytes);
                     tma_load_4d(st, &tmG, &xg_full[s], w0, h0, (1 + dd) * C + c_first, b);
-                    tma_load_4d(st + kGStage, &tmX, &xg_full[s], w0 - 8, h0 - P.R, c_first, b);
+                    tma_load_4d(st + kGStage, &tmX, &xg_full[s], w0 - G::kHaloCols, h0 - P.R, c_first, b);
                     issued = i + 1;
                 }
             }
@@ -153,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int dd = ob / P.n_cblk, c_first = (ob % P.n_cblk) * kCB;
                     mbar_arrive_expect_tx(&w_full[s], kWStage);
-                    tma_load_2d(sm + kWS + s * kWStage, &tmW, &w_full[s], 0, (dd * C + c_first) * 9);
+                    tma_load_2d(sm + kWS + s * kWStage, &tmW, &w_full[s], 0, (dd * C + c_first) * kTaps);
                     issued = i + 1;
                 }
             }
@@ -216,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int dd = ob / P.n_cblk, c_first = (ob % P.n_cblk) * kCB;
-                const int nrows = min(kCB, C - c_first) * 9;
+                const int nrows = min(kCB, C - c_first) * kTaps;
                 const int dil = dil_of(P.d, dd);
                 const bf16* gs = reinterpret_cast<const bf16*>(sm + kXG + s * kXgStage);
                 const uint32_t* xs32 = reinterpret_cast<const uint32_t*>(sm + kXG + s * kXgStage + kGStage);
@@ -226,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    form_dk_tile(sm + kDK + db * kDKBytes, xs32, gs + st * kPx, kSPx, nrows, slot_elems, P.R, dil,
+                    form_dk_tile<K>(sm + kDK + db * kDKBytes, xs32, gs + st * kPx, kSPx, nrows, slot_elems, P.R, dil,
                                  st * kTH, et, 32 * kFormWarps);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -277,16 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-}  // namespace
-
-bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w) {
-    return bwdtc::eligible(d, g, x, w) && d.R() <= kDyMaxR;
-}
-
-cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
+template <int K>
+cudaError_t launch_k(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
+    using G = BwdGeom<K>;
+    using L = DyLayout<K>;
     static int attr_done[64] = {};
     {
-        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dy_tc_kernel, kSmemBytes, attr_done);
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dy_tc_kernel<K>, L::kSmemBytes, attr_done);
         if (e != cudaSuccess) return e;
     }
     DyTcParams P;
@@ -294,11 +304,11 @@ cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const 
     P.tiles_w = (d.W + kTW - 1) / kTW;
     P.tiles_per_img = ((d.H + kSTH - 1) / kSTH) * P.tiles_w;
     P.n_tiles = d.B * P.tiles_per_img;
-    P.n_cblk = (d.C + kCB - 1) / kCB;
+    P.n_cblk = (d.C + G::kCB - 1) / G::kCB;
     P.n_oblk = 3 * P.n_cblk;
     P.R = d.R();
     P.WHx = kSTH + 2 * P.R;
-    P.xslot_bytes = P.WHx * kWinCols * 2;
+    P.xslot_bytes = P.WHx * G::kWinCols * 2;
     P.dy = static_cast<bf16*>(dy);
     P.err = device_error_word();
     if (P.err == nullptr) return cudaErrorUnknown;
@@ -313,15 +323,25 @@ cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const 
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    if (!encode_nchw(&tmG, g, d, 4 * d.C, kTW, kSTH, kCB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_nchw(&tmX, x, d, d.C, kWinCols, (uint32_t)P.WHx, kCB, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_nchw(&tmG, g, d, 4 * d.C, kTW, kSTH, G::kCB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_nchw(&tmX, x, d, d.C, G::kWinCols, (uint32_t)P.WHx, G::kCB, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     int grid = num_sms();
     if (grid > P.n_tiles) grid = P.n_tiles;
     trace_begin(s, kKBwdDyTc);
-    bwd_dy_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmW, tmG, tmX, P);
+    bwd_dy_tc_kernel<K><<<grid, kThreads, L::kSmemBytes, s>>>(tmW, tmG, tmX, P);
     trace_end(s);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w) {
+    return bwdtc::eligible(d, g, x, w, true) && d.R() <= (d.K == 3 ? DyLayout<3>::kMaxR : DyLayout<5>::kMaxR);
+}
+
+cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
+    return d.K == 3 ? launch_k<3>(d, g, x, w, dy, s) : launch_k<5>(d, g, x, w, dy, s);
 }
 
 }  // namespace ddpm

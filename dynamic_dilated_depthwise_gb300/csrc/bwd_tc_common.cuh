@@ -3,9 +3,9 @@
 // Pixel tiles are 2 rows x 64 columns (128 pixels, m = r * 64 + c), so that
 // each 64-pixel half of a tile is one contiguous 128-byte row per channel:
 // the shape a 128B-swizzled TMA box delivers as an MMA operand atom.
-// Taps are processed in blocks of 14 channels of one dilation (126 taps,
-// padded to the MMA M / K of 128): row r of a block is tap
-// o = (d*C + c_first + r/9)*9 + r%9.
+// Taps are processed in blocks of channels of one dilation, padded to the MMA
+// M / K of 128: 14 channels (126 taps) for K = 3, 5 channels (125 taps) for
+// K = 5.  Row r of a block is tap o = (d*C + c_first + r/K^2)*K^2 + r%K^2.
 //
 // dK^T tiles ([128 taps x 128 pixels], bf16) live in shared memory in the
 // 128B-swizzled layout: pixel half h at +16 KiB * h, tap row r at
@@ -24,14 +24,25 @@ namespace bwdtc {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kCB = 14;            // channels per block of taps (126 rows)
+constexpr int kCB = 14;            // K = 3: channels per block of taps (126 rows)
 constexpr int kBlockRows = 128;    // MMA extent of a block of taps
 constexpr int kTH = 2, kTW = 64;   // pixel tile
 constexpr int kPx = kTH * kTW;     // 128
 constexpr int kSlots = 16;         // channel slots of a 16-channel TMA box
-constexpr int kMaxR = 8;           // halo radius supported
-constexpr int kWinCols = kTW + 16; // x window columns: origin w0 - 8 keeps TMA coordinates 16-byte aligned
+constexpr int kMaxR = 8;           // K = 3: halo radius supported
+constexpr int kWinCols = kTW + 16; // K = 3: x window columns; origin w0 - 8 keeps TMA coordinates 16-byte aligned
 constexpr int kDKBytes = kBlockRows * kPx * 2;  // 32 KiB
+
+// Per kernel size: channels per block of taps (CB * K^2 <= 128), the x window's
+// column halo left and right of the tile (a 16-byte TMA coordinate, >= the widest
+// horizontal tap reach), its width, and the largest halo radius the kernels take.
+template <int K> struct BwdGeom;
+template <> struct BwdGeom<3> {
+    static constexpr int kCB = 14, kHaloCols = 8, kWinCols = kTW + 16, kMaxR = 8;
+};
+template <> struct BwdGeom<5> {
+    static constexpr int kCB = 5, kHaloCols = 16, kWinCols = kTW + 32, kMaxR = 10;
+};
 
 // (a * b) for two bf16 pairs: the exact product rounded once to bf16 (nearest even).
 __device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
@@ -41,37 +52,38 @@ __device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
     return *reinterpret_cast<uint32_t*>(&z);
 }
 
-// Form one dK^T tile: dK[r, px] = grad_d[c, px] * x[c, px + off(d, k)], r = c_local*9 + k.
+// Form one dK^T tile: dK[r, px] = grad_d[c, px] * x[c, px + off(d, k)], r = c_local*K*K + k.
 //   dk        destination tile (32 KiB, swizzled as described above)
 //   xs32      x window of the block's channels: slot c_local, rows (tile rows + 2R),
-//             kWinCols columns, bf16, origin (h0 - R + row_off, w0 - 8)
+//             G::kWinCols columns, bf16, origin (h0 - R + row_off, w0 - G::kHaloCols)
 //   gs        grad planes of the block: slot c_local, the 128 pixels of this tile
 //             at gs + c_local * gstride
 //   row_off   first window row of this tile (tiles stacked in one window)
 //   tid/nthr  this thread among the forming threads
-// One work unit is (channel c_local, 8-pixel chunk) for all nine taps: the grad
-// chunk is loaded once, and each of the three window rows as three aligned
-// 16-byte vectors (elements c8 .. c8+23 of the row, i.e. columns -8 .. +15 around
-// the chunk) from which the three horizontal taps, shifted by compile-time
-// multiples of the dilation DIL <= 8, are cut with byte permutes.  A warp's 16-byte
-// loads and stores touch each bank once per eight threads, so they run without
-// shared-memory bank conflicts.  Rows of channels c_local >= nc are written as
-// zeros; rows 126 and 127 of the block are never written (the caller zeroes them
-// once).
-template <int DIL>
+// One work unit is (channel c_local, 8-pixel chunk) for all K*K taps: the grad
+// chunk is loaded once, and each of the K window rows as aligned 16-byte vectors
+// (elements c8 .. c8+8+2H-1 of the row, H = G::kHaloCols, i.e. columns -H .. 7+H
+// around the chunk) from which the K horizontal taps, shifted by compile-time
+// multiples of the dilation DIL, are cut with byte permutes.  A warp's 16-byte loads
+// and stores touch each bank once per eight threads, so they run without shared-memory
+// bank conflicts.  Rows of channels c_local >= nc are written as zeros; rows
+// CB*K*K .. 127 of the block are never written (the caller zeroes them once).
+template <int K, int DIL>
 __device__ __forceinline__ void form_dk_tile_dil(uint8_t* dk, const uint32_t* xs32, const bf16* gs, int gstride,
                                                  int nc, int slot_elems, int R, int row_off, int tid, int nthr) {
-    static_assert(DIL >= 1 && DIL <= 8, "the window holds 8 columns of halo");
+    using G = BwdGeom<K>;
+    constexpr int kH = G::kHaloCols, kNV = (8 + 2 * kH) / 8, kNW = 4 * kNV, r0 = K / 2;
+    static_assert(DIL >= 1 && r0 * DIL <= kH, "the window holds the taps' horizontal reach");
     const uint4* xs4 = reinterpret_cast<const uint4*>(xs32);
-    for (int u = tid; u < kCB * 16; u += nthr) {
+    for (int u = tid; u < G::kCB * 16; u += nthr) {
         const int cl = u >> 4, chunk = u & 15;
         const int tr = chunk >> 3, c8 = (chunk & 7) * 8;
         uint8_t* rowbase = dk + tr * 16384;
         const int sw = chunk & 7;
         if (cl >= nc) {
 #pragma unroll
-            for (int k = 0; k < 9; ++k) {
-                const int ol = cl * 9 + k;
+            for (int k = 0; k < K * K; ++k) {
+                const int ol = cl * K * K + k;
                 *reinterpret_cast<uint4*>(rowbase + (ol >> 3) * 1024 + (ol & 7) * 128 + ((sw ^ (ol & 7)) << 4)) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
@@ -79,20 +91,27 @@ __device__ __forceinline__ void form_dk_tile_dil(uint8_t* dk, const uint32_t* xs
         }
         const uint4 gv = *reinterpret_cast<const uint4*>(gs + cl * gstride + chunk * 8);
 #pragma unroll
-        for (int ky = 0; ky < 3; ++ky) {
-            const int e = cl * slot_elems + (row_off + tr + R + (ky - 1) * DIL) * kWinCols + c8;   // multiple of 8
-            const uint4 q0 = xs4[(e >> 3)], q1 = xs4[(e >> 3) + 1], q2 = xs4[(e >> 3) + 2];
-            const uint32_t w[12] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w, q2.x, q2.y, q2.z, q2.w};
+        for (int ky = 0; ky < K; ++ky) {
+            const int e = cl * slot_elems + (row_off + tr + R + (ky - r0) * DIL) * G::kWinCols + c8;   // multiple of 8
+            uint32_t w[kNW];
 #pragma unroll
-            for (int kx = 0; kx < 3; ++kx) {
-                const int off = 8 + (kx - 1) * DIL;              // element of tap kx's first pixel
+            for (int v = 0; v < kNV; ++v) {
+                const uint4 q = xs4[(e >> 3) + v];
+                w[4 * v + 0] = q.x;
+                w[4 * v + 1] = q.y;
+                w[4 * v + 2] = q.z;
+                w[4 * v + 3] = q.w;
+            }
+#pragma unroll
+            for (int kx = 0; kx < K; ++kx) {
+                const int off = kH + (kx - r0) * DIL;            // element of tap kx's first pixel
                 uint32_t a[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int wi = (off >> 1) + i;
-                    a[i] = (off & 1) ? __byte_perm(w[wi], w[(wi + 1) < 12 ? wi + 1 : 11], 0x5432) : w[wi];
+                    a[i] = (off & 1) ? __byte_perm(w[wi], w[(wi + 1) < kNW ? wi + 1 : kNW - 1], 0x5432) : w[wi];
                 }
-                const int ol = cl * 9 + ky * 3 + kx;
+                const int ol = cl * K * K + ky * K + kx;
                 uint4 v;
                 v.x = bf2_mul(gv.x, a[0]);
                 v.y = bf2_mul(gv.y, a[1]);
@@ -104,25 +123,28 @@ __device__ __forceinline__ void form_dk_tile_dil(uint8_t* dk, const uint32_t* xs
     }
 }
 
+template <int K>
 __device__ __forceinline__ void form_dk_tile(uint8_t* dk, const uint32_t* xs32, const bf16* gs, int gstride, int nrows,
                                              int slot_elems, int R, int dil, int row_off, int tid, int nthr) {
-    const int nc = nrows / 9;
+    const int nc = nrows / (K * K);
     switch (dil) {
-        case 1: form_dk_tile_dil<1>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
-        case 2: form_dk_tile_dil<2>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
-        case 3: form_dk_tile_dil<3>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
-        case 4: form_dk_tile_dil<4>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
-        case 5: form_dk_tile_dil<5>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
-        case 6: form_dk_tile_dil<6>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
-        case 7: form_dk_tile_dil<7>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
-        default: form_dk_tile_dil<8>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 1: form_dk_tile_dil<K, 1>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 2: form_dk_tile_dil<K, 2>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 3: form_dk_tile_dil<K, 3>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 4: form_dk_tile_dil<K, 4>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 5: form_dk_tile_dil<K, 5>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 6: form_dk_tile_dil<K, (K == 3 ? 6 : 5)>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        case 7: form_dk_tile_dil<K, (K == 3 ? 7 : 5)>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
+        default: form_dk_tile_dil<K, (K == 3 ? 8 : 5)>(dk, xs32, gs, gstride, nc, slot_elems, R, row_off, tid, nthr); break;
     }
 }
 
-// Zero the two padding rows (126, 127) of a dK^T tile.
+// Zero the padding rows (CB*K*K .. 127) of a dK^T tile.
+template <int K>
 __device__ __forceinline__ void zero_dk_pad_rows(uint8_t* dk, int tid, int nthr) {
-    for (int u = tid; u < 2 * 2 * 8; u += nthr) {      // 2 rows x 2 halves x 8 chunks
-        const int ol = 126 + (u >> 4), half = (u >> 3) & 1, c = u & 7;
+    constexpr int r0 = BwdGeom<K>::kCB * K * K, npad = kBlockRows - r0;
+    for (int u = tid; u < npad * 2 * 8; u += nthr) {   // pad rows x 2 halves x 8 chunks
+        const int ol = r0 + (u >> 4), half = (u >> 3) & 1, c = u & 7;
         *reinterpret_cast<uint4*>(dk + half * 16384 + (ol >> 3) * 1024 + (ol & 7) * 128 + ((c ^ (ol & 7)) << 4)) =
             make_uint4(0u, 0u, 0u, 0u);
     }
@@ -154,18 +176,20 @@ inline bool encode_nchw(CUtensorMap* m, const void* base, const Dims& d, int ch,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Shapes the tensor-core backward handles: bf16, K = 3, C a multiple of 8 up to 64,
-// W a multiple of 8 (16-byte TMA strides), halo radius <= 8, 16-byte aligned tensors.
-// shape_ok() is the part that depends on the problem alone.
-inline bool shape_ok(const Dims& d) {
-    if (d.dtype != 1 || d.K != 3 || (d.flags & kFlagCudaCores)) return false;
+// Shapes the tensor-core backward handles: bf16, K = 3 (K = 5 as well where k5 is
+// set: the dW and dY kernels), C a multiple of 8 up to 64, W a multiple of 8 (16-byte
+// TMA strides), the halo radius within the window (8 for K = 3, 10 for K = 5),
+// 16-byte aligned tensors.  shape_ok() is the part that depends on the problem alone.
+inline bool shape_ok(const Dims& d, bool k5 = false) {
+    if (d.dtype != 1 || (d.flags & kFlagCudaCores)) return false;
+    if (!(d.K == 3 || (k5 && d.K == 5))) return false;
     if (d.C > 64 || d.C % 8 != 0 || d.W % 8 != 0) return false;
-    if (d.R() > kMaxR) return false;
+    if (d.R() > (d.K == 3 ? BwdGeom<3>::kMaxR : BwdGeom<5>::kMaxR)) return false;
     return d.O <= (1LL << 30) && d.HW <= (1LL << 31) - 1024;
 }
 
-inline bool eligible(const Dims& d, const void* a, const void* b, const void* c) {
-    if (!shape_ok(d)) return false;
+inline bool eligible(const Dims& d, const void* a, const void* b, const void* c, bool k5 = false) {
+    if (!shape_ok(d, k5)) return false;
     if ((uintptr_t)a % 16 || (uintptr_t)b % 16 || (uintptr_t)c % 16) return false;
     return encode_fn() != nullptr;
 }
