@@ -95,7 +95,7 @@ def kernel_work(name: str, p, es: int, splits: int):
         return "hbm", 2 * P * 4 * C * es, "bytes"
     if name == "pack_f32":                 # y and grad blocks 1..3 read, their channel-chunked copies written
         return "hbm", 2 * P * 4 * C * es, "bytes"
-    if name in ("forward_tc", "bwd_dx_tc", "bwd_dx_tc_packed", "bwd_dy_tc", "bwd_dw_tc"):
+    if name in ("forward_tc", "bwd_dx_tc", "bwd_dx_tc_packed", "bwd_dx_gather", "bwd_dy_tc", "bwd_dw_tc"):
         return "tensor", gemm, "flops"
     if name == "bwd_dw_tf32":
         return "tensor_tf32", 2.0 * O * (C + 1) * P, "flops"
@@ -201,7 +201,8 @@ KERNEL_SOURCE = {"forward_tc": "forward_tc.cu", "pack_chunks": "bwd_dx_packed.cu
                  "filter_pregenerated_simt": "filter_simt.cu", "filter_bwd_dx": "filter_bwd_simt.cu",
                  "filter_bwd_dtaps": "filter_bwd_simt.cu", "bwd_dx_simt": "backward_simt.cu",
                  "bwd_dy_simt": "backward_simt.cu", "bwd_dw_partial_simt": "backward_simt.cu",
-                 "bwd_dy_tf32": "bwd_dy_tf32.cu", "bwd_dx_tf32": "bwd_dx_tf32.cu", "pack_f32": "bwd_dx_tf32.cu"}
+                 "bwd_dy_tf32": "bwd_dy_tf32.cu", "bwd_dx_tf32": "bwd_dx_tf32.cu", "pack_f32": "bwd_dx_tf32.cu",
+                 "bwd_dx_gather": "bwd_dx_gather.cu"}
 
 
 def kernel_source_digest(kernel: str) -> str:

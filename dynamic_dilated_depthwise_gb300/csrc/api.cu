@@ -213,7 +213,7 @@ ddpm_status ddpm_backward_workspace_size(const ddpm_problem* problem, size_t* by
     Dims d;
     DDPM_TRY(validate(problem, &d));
     if (bytes == nullptr) return DDPM_ERR_INVALID_ARGUMENT;
-    if (ddpm::bwd_dx_packed_shape_ok(d))
+    if (ddpm::bwd_dx_packed_shape_ok(d) || (d.K != 3 && ddpm::bwd_dx_gather_shape_ok(d)))
         *bytes = packed_offset(d) + ddpm::bwd_dx_packed_bytes(d);
     else if (ddpm::bwd_dx_tf32_shape_ok(d))
         *bytes = dx_tf32_offset(d) + ddpm::bwd_dx_tf32_bytes(d);
@@ -252,12 +252,15 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
         const size_t poff = packed_offset(d);
         const bool packed = ddpm::bwd_dx_packed_eligible(d, grad_out, y, weight) &&
                             workspace_bytes >= poff + ddpm::bwd_dx_packed_bytes(d);
+        // halos whose grad windows do not fit the packed kernel's shared memory (K = 5)
+        const bool gather = !packed && d.K != 3 && ddpm::bwd_dx_gather_eligible(d, grad_out, y, weight) &&
+                            workspace_bytes >= poff + ddpm::bwd_dx_packed_bytes(d);
         const bool dy_tf32 = ddpm::bwd_dy_tf32_eligible(d, grad_out, x, weight, dy) &&
                              workspace_bytes >= poff + ddpm::bwd_dy_tf32_wt_bytes(d);
         const size_t xoff = dx_tf32_offset(d);
         const bool dx_tf32 = ddpm::bwd_dx_tf32_eligible(d, grad_out, y, weight, dx) &&
                              workspace_bytes >= xoff + ddpm::bwd_dx_tf32_bytes(d);
-        const size_t part_bytes = (packed || dy_tf32 || dx_tf32) ? poff : workspace_bytes;
+        const size_t part_bytes = (packed || gather || dy_tf32 || dx_tf32) ? poff : workspace_bytes;
         // dX on the caller's stream, dY and dW (+ reduce) on the two side streams: the
         // pieces share only inputs, and each one's last partial wave of CTAs leaves SMs
         // that the others fill.  While kernels are traced the pieces run one after
@@ -277,6 +280,8 @@ ddpm_status ddpm_backward(const ddpm_problem* problem, const void* grad_out, con
             e = ddpm::launch_bwd_dx_packed(d, grad_out, y, weight, bias, dx, static_cast<char*>(workspace) + poff, s);
         else if (ddpm::bwd_dx_tc_eligible(d, grad_out, y, weight))
             e = ddpm::launch_bwd_dx_tc(d, grad_out, y, weight, bias, dx, s);
+        else if (gather)
+            e = ddpm::launch_bwd_dx_gather(d, grad_out, y, weight, bias, dx, static_cast<char*>(workspace) + poff, s);
         else if (dx_tf32)
             e = ddpm::launch_bwd_dx_tf32(d, grad_out, y, weight, bias, dx, static_cast<char*>(workspace) + xoff, s);
         else

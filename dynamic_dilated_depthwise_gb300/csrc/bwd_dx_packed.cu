@@ -645,20 +645,9 @@ bool bwd_dx_packed_eligible(const Dims& d, const void* g, const void* y, const v
 
 size_t bwd_dx_packed_bytes(const Dims& d) { return (size_t)4 * (size_t)d.B * (size_t)d.C * (size_t)d.HW * 2; }
 
-cudaError_t launch_bwd_dx_packed(const Dims& d, const void* g, const void* y, const void* w, const void* bias,
-                                 void* dx, void* packed, cudaStream_t s) {
-    const DxPackedLayout L = dx_packed_layout(d);
-    if (L.stages == 0) return cudaErrorInvalidValue;
-    static int attr_bytes[64] = {};
-    {
-        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dx_tc_packed_kernel, L.bytes, attr_bytes);
-        if (e != cudaSuccess) return e;
-    }
+cudaError_t launch_pack_chunks(const Dims& d, const void* g, const void* y, void* packed, cudaStream_t s) {
     bf16* yc = static_cast<bf16*>(packed);
-    bf16* gc = yc + (size_t)d.B * d.C * d.HW;
     const int nch = d.C / 8;
-
-    // 1. channel-chunked copies of y and of the three dilation blocks of grad
     const long long n_rows = 4LL * d.B * nch * (d.HW / 8);   // 16-byte pixel rows of the copies
     if (d.HW % kPkPx == 0 && n_rows <= INT_MAX && (uintptr_t)y % 16 == 0 && (uintptr_t)g % 16 == 0) {
         static int attr_pk[64] = {};
@@ -707,6 +696,28 @@ cudaError_t launch_bwd_dx_packed(const Dims& d, const void* g, const void* y, co
                                                                      n_y, n_all);
         trace_end(s);
         const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+
+    return cudaSuccess;
+}
+
+cudaError_t launch_bwd_dx_packed(const Dims& d, const void* g, const void* y, const void* w, const void* bias,
+                                 void* dx, void* packed, cudaStream_t s) {
+    const DxPackedLayout L = dx_packed_layout(d);
+    if (L.stages == 0) return cudaErrorInvalidValue;
+    static int attr_bytes[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dx_tc_packed_kernel, L.bytes, attr_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    bf16* yc = static_cast<bf16*>(packed);
+    bf16* gc = yc + (size_t)d.B * d.C * d.HW;
+    const int nch = d.C / 8;
+
+    // 1. channel-chunked copies of y and of the three dilation blocks of grad
+    {
+        const cudaError_t e = launch_pack_chunks(d, g, y, packed, s);
         if (e != cudaSuccess) return e;
     }
 

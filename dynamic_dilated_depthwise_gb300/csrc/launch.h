@@ -30,7 +30,8 @@ enum KernelId : int {
     kKBwdDyTf32 = 16,
     kKPackF32 = 17,
     kKBwdDxTf32 = 18,
-    kKNumKernels = 19
+    kKBwdDxGather = 19,
+    kKNumKernels = 20
 };
 
 // Tracing hooks around each launch (cheap no-ops while tracing is off).
@@ -123,6 +124,9 @@ cudaError_t launch_bwd_dx_tc(const Dims& d, const void* g, const void* y, const 
 // dX on tcgen05 tensor cores from channel-chunked copies of y and grad that the
 // launcher first writes into `packed` (bwd_dx_packed_bytes(d) bytes, 16-byte
 // aligned); the copies make the staging a plain TMA load (halo radius <= 6).
+// The copies alone: y into packed[0, B*C*H*W) and grad blocks 1..3 after it, bf16
+// [B][C/8][H][W][8] and [B][3][C/8][H][W][8] (C a multiple of 8, H*W of 8).
+cudaError_t launch_pack_chunks(const Dims& d, const void* g, const void* y, void* packed, cudaStream_t s);
 bool bwd_dx_packed_shape_ok(const Dims& d);   // the problem alone (sizes the workspace)
 bool bwd_dx_packed_eligible(const Dims& d, const void* g, const void* y, const void* w);
 size_t bwd_dx_packed_bytes(const Dims& d);
@@ -147,6 +151,14 @@ bool bwd_dx_tf32_eligible(const Dims& d, const void* g, const void* y, const voi
 size_t bwd_dx_tf32_bytes(const Dims& d);
 cudaError_t launch_bwd_dx_tf32(const Dims& d, const void* g, const void* y, const void* w, const void* bias, void* dx,
                                void* packed, cudaStream_t s);
+
+// bf16 dX on tcgen05 tensor cores from the same channel-chunked copies as the packed
+// dX (bwd_dx_packed_bytes(d) bytes in `packed`, written by the launch), with grad
+// gathered from L2: K = 3 or 5 (halo radius <= 10).  Taken for K = 5.
+bool bwd_dx_gather_shape_ok(const Dims& d);
+bool bwd_dx_gather_eligible(const Dims& d, const void* g, const void* y, const void* w);
+cudaError_t launch_bwd_dx_gather(const Dims& d, const void* g, const void* y, const void* w, const void* bias,
+                                 void* dx, void* packed, cudaStream_t s);
 
 // dY on tcgen05 tensor cores (same shapes as the dW kernel).
 bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w);

@@ -41,7 +41,7 @@ const char* const kNames[kKNumKernels] = {
     "filter_pregenerated_simt", "forward_simt", "forward_tc", "bwd_dx_simt", "bwd_dy_simt",
     "bwd_dw_partial_simt", "bwd_dw_reduce", "bwd_dx_tc", "bwd_dy_tc", "bwd_dw_tc",
     "pack_chunks", "bwd_dx_tc_packed", "bwd_dw_tf32", "filter_bwd_dx", "filter_bwd_dtaps", "forward_tf32",
-    "bwd_dy_tf32", "pack_f32", "bwd_dx_tf32",
+    "bwd_dy_tf32", "pack_f32", "bwd_dx_tf32", "bwd_dx_gather",
 };
 
 }  // namespace

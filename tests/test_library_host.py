@@ -127,7 +127,8 @@ def _partials_bytes(B, C, H, W, K):
     (2, 24, 16, 32, 3, (1, 3, 5), True),
     (2, 24, 15, 17, 3, (1, 3, 5), False),     # W not a multiple of 8: no tensor-core backward
     (1, 64, 64, 64, 3, (2, 4, 6), False),     # halo radius 6 with wide windows: dX tiles do not fit
-    (1, 64, 128, 128, 5, (1, 3, 5), False),   # K = 5: CUDA-core backward
+    (1, 64, 128, 128, 5, (1, 3, 5), True),    # K = 5: the same copies, for the dX that gathers grad from L2
+    (1, 64, 128, 128, 5, (1, 3, 6), False),   # K = 5, halo radius 12: CUDA-core backward
 ])
 def test_bf16_workspace_adds_packed_copies(lib, B, C, H, W, K, dil, packed):
     p = _prob(B=B, C=C, H=H, W=W, K=K, dilations=dil, dtype=binding.DDPM_BFLOAT16)
