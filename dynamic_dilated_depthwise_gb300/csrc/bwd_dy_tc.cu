@@ -27,9 +27,9 @@ namespace {
 using namespace bwdtc;
 
 constexpr int kN = 64;            // MMA N: output channels j (zero padded beyond C)
-constexpr int kSub = 4;           // 2x64 sub-tiles per super tile
-constexpr int kSTH = kSub * kTH;  // 8 rows
-constexpr int kSPx = kSub * kPx;  // 512 pixels
+// Sub-tiles of 2x64 per super tile: 4 (8 rows, 512 pixels), or 1 for images whose
+// 8-row super tiles would leave most SMs idle (the W block is then read per 128
+// pixels instead of per 512).
 constexpr int kDyMaxR = 5;        // K = 3: halo radius the window buffers hold (10 for K = 5)
 constexpr int kFormWarps = 8;
 constexpr int kEpiWarps = 4;
@@ -46,9 +46,10 @@ static_assert(kWS % 1024 == 0 && kWStage % 1024 == 0, "SW128 atoms need 1 KiB");
 
 // The x/grad stage of kernel size K: grad planes [CB x 512 px] and x windows
 // [CB x (8 + 2 maxR) x cols], bf16.
-template <int K>
+template <int K, int SUB>
 struct DyLayout {
     using G = BwdGeom<K>;
+    static constexpr int kSTH = SUB * kTH, kSPx = SUB * kPx;
     static constexpr int kMaxR = K == 3 ? kDyMaxR : 10;
     static constexpr int kGStage = G::kCB * kSPx * 2;
     static constexpr int kXgStage = kGStage + G::kCB * (kSTH + 2 * kMaxR) * G::kWinCols * 2;
@@ -66,14 +67,15 @@ struct DyTcParams {
     unsigned int* err;
 };
 
-template <int K>
+template <int K, int SUB>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dy_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
                      const __grid_constant__ CUtensorMap tmX, const DyTcParams P) {
     using namespace tc;
     using G = BwdGeom<K>;
-    using L = DyLayout<K>;
+    using L = DyLayout<K, SUB>;
     constexpr int kCB = G::kCB, kTaps = K * K, kGStage = L::kGStage, kXgStage = L::kXgStage;
+    constexpr int kSub = SUB, kSTH = L::kSTH, kSPx = L::kSPx;
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB-aligned base, derived by pointer arithmetic on the shared array so that every
     // access through it stays a shared-memory access (an integer round trip would make
@@ -290,13 +292,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int K>
+template <int K, int SUB>
 cudaError_t launch_k(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
     using G = BwdGeom<K>;
-    using L = DyLayout<K>;
+    using L = DyLayout<K, SUB>;
+    constexpr int kSTH = L::kSTH;
     static int attr_done[64] = {};
     {
-        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dy_tc_kernel<K>, L::kSmemBytes, attr_done);
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dy_tc_kernel<K, SUB>, L::kSmemBytes, attr_done);
         if (e != cudaSuccess) return e;
     }
     DyTcParams P;
@@ -329,7 +332,7 @@ cudaError_t launch_k(const Dims& d, const void* g, const void* x, const void* w,
     int grid = num_sms();
     if (grid > P.n_tiles) grid = P.n_tiles;
     trace_begin(s, kKBwdDyTc);
-    bwd_dy_tc_kernel<K><<<grid, kThreads, L::kSmemBytes, s>>>(tmW, tmG, tmX, P);
+    bwd_dy_tc_kernel<K, SUB><<<grid, kThreads, L::kSmemBytes, s>>>(tmW, tmG, tmX, P);
     trace_end(s);
     return cudaGetLastError();
 }
@@ -337,11 +340,15 @@ cudaError_t launch_k(const Dims& d, const void* g, const void* x, const void* w,
 }  // namespace
 
 bool bwd_dy_tc_eligible(const Dims& d, const void* g, const void* x, const void* w) {
-    return bwdtc::eligible(d, g, x, w, true) && d.R() <= (d.K == 3 ? DyLayout<3>::kMaxR : DyLayout<5>::kMaxR);
+    return bwdtc::eligible(d, g, x, w, true) &&
+           d.R() <= (d.K == 3 ? DyLayout<3, 4>::kMaxR : DyLayout<5, 4>::kMaxR);
 }
 
 cudaError_t launch_bwd_dy_tc(const Dims& d, const void* g, const void* x, const void* w, void* dy, cudaStream_t s) {
-    return d.K == 3 ? launch_k<3>(d, g, x, w, dy, s) : launch_k<5>(d, g, x, w, dy, s);
+    const long long super_tiles = (long long)d.B * ((d.H + 4 * kTH - 1) / (4 * kTH)) * ((d.W + kTW - 1) / kTW);
+    const bool small = super_tiles < num_sms() / 2;
+    if (d.K == 3) return small ? launch_k<3, 1>(d, g, x, w, dy, s) : launch_k<3, 4>(d, g, x, w, dy, s);
+    return small ? launch_k<5, 1>(d, g, x, w, dy, s) : launch_k<5, 4>(d, g, x, w, dy, s);
 }
 
 }  // namespace ddpm

@@ -303,7 +303,9 @@ def test_tf32x3_forward_without_bias_and_ineligible_shapes():
 
 # + H*W a multiple of 2048 with several images and fewer than eight channel chunks:
 # the persistent TMA pack
-TC_BWD_SHAPES = list(TC_SHAPES) + [Problem(2, 24, 32, 64, 3)]
+# + enough 8x64 super tiles (>= half the SMs) that dY keeps four sub-tiles per CTA, with
+# ragged rows and columns
+TC_BWD_SHAPES = list(TC_SHAPES) + [Problem(2, 24, 32, 64, 3), Problem(4, 16, 70, 136, 3)]
 
 
 @pytest.mark.parametrize("p", TC_BWD_SHAPES, ids=_id)
@@ -355,6 +357,7 @@ TC_BWD_K5_SHAPES = [
     Problem(2, 24, 10, 72, 5),               # ragged 64-column tiles, several images, a partial block
     Problem(1, 8, 6, 128, 5, (1, 2, 3)),     # other dilations, one full and one partial block
     Problem(1, 16, 3, 16, 5, (2, 4, 5)),     # image smaller than the halo
+    Problem(6, 8, 38, 136, 5),               # dY with four sub-tiles per CTA, ragged rows and columns
 ]
 
 
