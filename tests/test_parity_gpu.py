@@ -123,12 +123,15 @@ def test_backward_matches_oracle(p, dtype):
 
 
 # Shapes whose rows are whole 16-byte vectors (W % 8 == 0): the filter takes its tiled
-# shared-memory kernel.  Ragged 64-column and row tiles, halo radius 10 (K = 5) and 15
-# (K = 7), a 1-row image, and other dilations.
+# shared-memory kernel.  Ragged 64-column and row tiles,
+# halo radius 10 (K = 5), 15 (K = 7) and 16 (K = 3, the widest the x window takes), a
+# 1-row image, other dilations, and W a multiple of the FP32 vector only.
 FILTER_TILED = TC_SHAPES + [
     Problem(1, 8, 40, 72, 5),                # K = 5: halo radius 10
     Problem(1, 4, 19, 24, 7),                # K = 7: halo radius 15
     Problem(2, 6, 33, 64, 3, (2, 3, 4)),
+    Problem(1, 4, 40, 64, 3, (4, 8, 16)),    # K = 3: halo radius 16
+    Problem(2, 8, 10, 36, 3),                # W % 8 != 0: bf16 takes the per-element kernel
 ]
 
 
