@@ -10,13 +10,14 @@
 //
 // The FP32 counterpart of bwd_dw_tc.cu.  dK[o, p] = grad * x is formed in FP32 on
 // CUDA cores; the tensor cores read it (and y) as TF32 and accumulate in FP32.
-// A CTA owns a block of taps (14 channels of one dilation, 126 taps padded to
-// M = 128) and one pixel split; per 1x64 pixel tile:
+// A CTA owns a block of taps (14 channels of one dilation, 126 taps, for K = 3; 5
+// channels, 125 taps, for K = 5; padded to M = 128) and one pixel split; per 1x64
+// pixel tile:
 //   - one producer warp's TMA brings y [64 j x 64 px] FP32 as two 128-byte
 //     swizzled halves of 32 pixels (K-major operand) into a 2-stage ring the
 //     MMA releases;
-//   - another brings the block's 14 grad rows [14 x 64 px] and x windows
-//     [14 x (1+2R) x 80] (zero outside the image) into a 2-stage ring the
+//   - another brings the block's grad rows [CB x 64 px] and x windows
+//     [CB x (1+2R) x (64 + 2 halo)] (zero outside the image) into a 2-stage ring the
 //     formers release as soon as dK is formed;
 //   - eight warps form dK^T[o, px] into a 128B-swizzled K-major tile (32 KiB);
 //   - one thread issues D[o, n] += dK^T[o, px] * Y[n, px], kind::tf32, M = 128,
@@ -37,9 +38,14 @@ constexpr int kFormWarps = 8;
 constexpr int kThreads = 32 * (3 + kFormWarps);    // x/grad producer, MMA, formers, y producer
 constexpr int kYWarp = 2 + kFormWarps;
 constexpr int kYStages = 2, kXgStages = 2;
-constexpr int kMaxR32 = 6;                         // halo radius two x/grad stages hold
-constexpr int kWin32 = kTW32 + 16;                 // x window columns, origin w0 - 8 (32-byte aligned)
 constexpr int kSmemCap = 232448 - 1024;            // dynamic shared memory: the opt-in 227 KiB less the static part
+
+// Per kernel size: channels per block of taps, the x window's column halo (left and
+// right of the tile, a 32-byte TMA coordinate, >= the taps' horizontal reach), its
+// width, and the halo radius two x/grad stages hold.
+template <int K> struct Tf32Geom;
+template <> struct Tf32Geom<3> { static constexpr int CB = 14, HALO = 8, WIN = kTW32 + 16, MAXR = 6; };
+template <> struct Tf32Geom<5> { static constexpr int CB = 5, HALO = 16, WIN = kTW32 + 32, MAXR = 10; };
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr int kDK = 0;                             // 2 x dK^T tiles [128 taps x 64 px] FP32, 32 KiB each
@@ -48,44 +54,52 @@ constexpr int kYS = kDK + 2 * kDK32;               // y ring: stages x 2 halves 
 constexpr int kYHalf = kNY * 128;
 constexpr int kYStage = 2 * kYHalf;
 constexpr int kXG = kYS + kYStages * kYStage;      // x/grad ring
-constexpr int kGStage = kCB * kTW32 * 4;           // grad rows of the block [14 x 64 px] FP32
-constexpr int kXgMax = kGStage + kCB * (1 + 2 * kMaxR32) * kWin32 * 4;
-constexpr int kSmemBytes = kXG + kXgStages * kXgMax + 1024 + 128;   // + alignment slack + over-read margin
 static_assert(kDK32 == 32768 && kYS % 1024 == 0 && kYHalf % 1024 == 0, "SW128 atoms need 1 KiB");
-static_assert(kXG % 128 == 0 && kGStage % 128 == 0, "TMA dst 128 B");
-static_assert(kSmemBytes <= kSmemCap, "shared memory");
+
+template <int K>
+struct Tf32Layout {
+    using G = Tf32Geom<K>;
+    static constexpr int kGStage = G::CB * kTW32 * 4;   // grad rows of the block [CB x 64 px] FP32
+    static constexpr int kXgMax = kGStage + G::CB * (1 + 2 * G::MAXR) * G::WIN * 4;
+    static constexpr int kSmemBytes = kXG + kXgStages * kXgMax + 1024 + 128;   // + alignment slack + over-read margin
+    static_assert(kXG % 128 == 0 && kGStage % 128 == 0, "TMA dst 128 B");
+    static_assert(kSmemBytes <= kSmemCap, "shared memory");
+};
 
 struct DwTf32Params {
     Dims d;
     int tiles_w, tiles_per_img, n_tiles;
     int n_cblk, n_oblk, tiles_per_split;
     int R, WHx;            // halo radius, window rows (1 + 2R)
-    int xslot;             // bytes of one channel's x window: WHx * 80 * 4
+    int xslot;             // bytes of one channel's x window: WHx * window columns * 4
     int xg_stage;          // bytes of one x/grad stage, a multiple of 128
     float* ws;             // [S][O][C+1]
     unsigned int* err;
 };
 
-// Form one dK^T tile in FP32: dK[r, px] = grad_d[c, px] * x[c, px + off(d, k)], r = c*9 + k.
+// Form one dK^T tile in FP32: dK[r, px] = grad_d[c, px] * x[c, px + off(d, k)], r = c*K*K + k.
 // Layout: pixel half h (px / 32) at +16 KiB * h, tap row r at (r/8)*1024 + (r%8)*128,
 // 16-byte chunk (px%32)/4 XOR (r%8).  Work unit = (channel, 4-pixel chunk j): the
-// grad chunk is one 16-byte load; each of the three window rows gives the five
-// aligned vectors of window columns 4j .. 4j+19 (the chunk sits at columns
-// 4j+8 .. 4j+11), from which the three horizontal taps are taken at compile-time
-// offsets 8 + (kx-1)*DIL.  A warp's loads and stores touch each bank once per eight
-// threads.  Rows of channels >= nc are written as zeros.
-template <int DIL>
+// grad chunk is one 16-byte load; each of the K window rows gives the aligned vectors
+// of window columns 4j .. 4j+3+2H (H = the window's column halo; the chunk sits at
+// columns 4j+H .. 4j+H+3), from which the K horizontal taps are taken at compile-time
+// offsets H + (kx-r)*DIL; only the vectors the taps reach are loaded.  A warp's loads
+// and stores touch each bank once per eight threads.  Rows of channels >= nc are
+// written as zeros.
+template <int K, int DIL>
 __device__ __forceinline__ void form_dk_f32_dil(uint8_t* dk, const float* xs, const float* gs, int nc, int xslot_f,
                                                 int R, int tid, int nthr) {
-    static_assert(DIL >= 1 && DIL <= 8, "the window holds 8 columns of halo");
-    for (int u = tid; u < kCB * 16; u += nthr) {
+    using G = Tf32Geom<K>;
+    constexpr int kH = G::HALO, kNV = (4 + 2 * kH) / 4, r0 = K / 2;
+    static_assert(DIL >= 1 && r0 * DIL <= kH, "the window holds the taps' horizontal reach");
+    for (int u = tid; u < G::CB * 16; u += nthr) {
         const int cl = u >> 4, j = u & 15;
         uint8_t* colbase = dk + (j >> 3) * 16384;
         const int sw = j & 7;
         if (cl >= nc) {
 #pragma unroll
-            for (int k = 0; k < 9; ++k) {
-                const int r = cl * 9 + k;
+            for (int k = 0; k < K * K; ++k) {
+                const int r = cl * K * K + k;
                 *reinterpret_cast<float4*>(colbase + (r >> 3) * 1024 + (r & 7) * 128 + ((sw ^ (r & 7)) << 4)) =
                     make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -94,13 +108,13 @@ __device__ __forceinline__ void form_dk_f32_dil(uint8_t* dk, const float* xs, co
         const float4 gv = *reinterpret_cast<const float4*>(gs + cl * kTW32 + j * 4);
         const float g[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
-        for (int ky = 0; ky < 3; ++ky) {
-            const float* row = xs + cl * xslot_f + (R + (ky - 1) * DIL) * kWin32 + j * 4;
-            float w[20];
+        for (int ky = 0; ky < K; ++ky) {
+            const float* row = xs + cl * xslot_f + (R + (ky - r0) * DIL) * G::WIN + j * 4;
+            float w[4 * kNV];
 #pragma unroll
-            for (int v = 0; v < 5; ++v) {
-                // only the vectors the three taps reach are loaded (compile-time indices)
-                if (v * 4 + 3 >= 8 - DIL && v * 4 <= 11 + DIL) {
+            for (int v = 0; v < kNV; ++v) {
+                // only the vectors the K taps reach are loaded (compile-time indices)
+                if (v * 4 + 3 >= kH - r0 * DIL && v * 4 <= kH + 3 + r0 * DIL) {
                     const float4 q = *reinterpret_cast<const float4*>(row + v * 4);
                     w[v * 4 + 0] = q.x;
                     w[v * 4 + 1] = q.y;
@@ -109,9 +123,9 @@ __device__ __forceinline__ void form_dk_f32_dil(uint8_t* dk, const float* xs, co
                 }
             }
 #pragma unroll
-            for (int kx = 0; kx < 3; ++kx) {
-                const int off = 8 + (kx - 1) * DIL;
-                const int r = cl * 9 + ky * 3 + kx;
+            for (int kx = 0; kx < K; ++kx) {
+                const int off = kH + (kx - r0) * DIL;
+                const int r = cl * K * K + ky * K + kx;
                 float4 o;
                 o.x = g[0] * w[off + 0];
                 o.y = g[1] * w[off + 1];
@@ -123,31 +137,37 @@ __device__ __forceinline__ void form_dk_f32_dil(uint8_t* dk, const float* xs, co
     }
 }
 
+template <int K>
 __device__ __forceinline__ void form_dk_f32(uint8_t* dk, const float* xs, const float* gs, int nc, int xslot_f, int R,
                                             int dil, int tid, int nthr) {
     switch (dil) {
-        case 1: form_dk_f32_dil<1>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
-        case 2: form_dk_f32_dil<2>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
-        case 3: form_dk_f32_dil<3>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
-        case 4: form_dk_f32_dil<4>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
-        case 5: form_dk_f32_dil<5>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
-        default: form_dk_f32_dil<6>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
+        case 1: form_dk_f32_dil<K, 1>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
+        case 2: form_dk_f32_dil<K, 2>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
+        case 3: form_dk_f32_dil<K, 3>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
+        case 4: form_dk_f32_dil<K, 4>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
+        case 5: form_dk_f32_dil<K, 5>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
+        default: form_dk_f32_dil<K, (K == 3 ? 6 : 5)>(dk, xs, gs, nc, xslot_f, R, tid, nthr); break;
     }
 }
 
-// Zero the two padding rows (126, 127) of an FP32 dK^T tile.
+// Zero the padding rows (CB*K*K .. 127) of an FP32 dK^T tile.
+template <int K>
 __device__ __forceinline__ void zero_pad_rows_f32(uint8_t* dk, int tid, int nthr) {
-    for (int u = tid; u < 2 * 2 * 8; u += nthr) {      // 2 rows x 2 halves x 8 chunks
-        const int r = 126 + (u >> 4), half = (u >> 3) & 1, c = u & 7;
+    constexpr int r0 = Tf32Geom<K>::CB * K * K, npad = kBlockRows - r0;
+    for (int u = tid; u < npad * 2 * 8; u += nthr) {   // pad rows x 2 halves x 8 chunks
+        const int r = r0 + (u >> 4), half = (u >> 3) & 1, c = u & 7;
         *reinterpret_cast<float4*>(dk + half * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)) =
             make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
+template <int K>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dw_tf32_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmG,
                        const __grid_constant__ CUtensorMap tmX, const DwTf32Params P) {
     using namespace tc;
+    using G = Tf32Geom<K>;
+    constexpr int kCB = G::CB, kTaps = K * K, kGStage = Tf32Layout<K>::kGStage;
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB-aligned base, derived by pointer arithmetic on the shared array so that every
     // access through it stays a shared-memory access
@@ -171,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int dd = ob / P.n_cblk;
     const int c_first = (ob % P.n_cblk) * kCB;
     const int nc = min(kCB, C - c_first);
-    const int nrows = nc * 9;
+    const int nrows = nc * kTaps;
     const int dil = dil_of(P.d, dd);
 
     if (threadIdx.x == 0) {
@@ -201,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t v = row == 0 ? 0x3F800000u : 0u;   // FP32 1.0
             reinterpret_cast<uint32_t*>(sm + kYS + st * kYStage + half * kYHalf + (64 + row) * 128)[word] = v;
         }
-        zero_pad_rows_f32(sm + kDK, et, 32 * kFormWarps);
-        zero_pad_rows_f32(sm + kDK + kDK32, et, 32 * kFormWarps);
+        zero_pad_rows_f32<K>(sm + kDK, et, 32 * kFormWarps);
+        zero_pad_rows_f32<K>(sm + kDK + kDK32, et, 32 * kFormWarps);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -226,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* st = sm + kXG + s * P.xg_stage;
                 mbar_arrive_expect_tx(&xg_full[s], bytes);
                 tma_load_4d(st, &tmG, &xg_full[s], w0, h0, (1 + dd) * C + c_first, b);
-                tma_load_4d(st + kGStage, &tmX, &xg_full[s], w0 - 8, h0 - P.R, c_first, b);
+                tma_load_4d(st + kGStage, &tmX, &xg_full[s], w0 - G::HALO, h0 - P.R, c_first, b);
                 issued = i + 1;
             }
             // drain: every copy this thread started lands before its shared memory is released
@@ -298,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const uint8_t* st = sm + kXG + sx * P.xg_stage;
-            form_dk_f32(sm + kDK + s * kDK32, reinterpret_cast<const float*>(st + kGStage),
+            form_dk_f32<K>(sm + kDK + s * kDK32, reinterpret_cast<const float*>(st + kGStage),
                         reinterpret_cast<const float*>(st), nc, P.xslot / 4, P.R, dil, et, 32 * kFormWarps);
             fence_proxy_async_smem();
             __syncwarp();
@@ -310,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // epilogue: this split's partial sums for the block of taps
         const int q = warp & 3, hc = (warp - 2) >> 2;
         const int row = q * 32 + lane;
-        const int rc = row / 9;
-        const long long o = (long long)(dd * C + c_first + rc) * 9 + (row - rc * 9);
+        const int rc = row / kTaps;
+        const long long o = (long long)(dd * C + c_first + rc) * kTaps + (row - rc * kTaps);
         float* wsrow = P.ws + ((long long)split * O + o) * (C + 1);
         uint32_t v[40];
         if (n_my > 0) {
@@ -358,20 +378,58 @@ bool encode_nchw_f32(CUtensorMap* m, const void* base, const Dims& d, int ch, ui
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int K>
+cudaError_t launch_k(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S, cudaStream_t s) {
+    using G = Tf32Geom<K>;
+    using L = Tf32Layout<K>;
+    static int attr_done[64] = {};
+    {
+        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dw_tf32_kernel<K>, L::kSmemBytes, attr_done);
+        if (e != cudaSuccess) return e;
+    }
+    DwTf32Params P;
+    P.d = d;
+    P.tiles_w = (d.W + kTW32 - 1) / kTW32;
+    P.tiles_per_img = d.H * P.tiles_w;
+    P.n_tiles = d.B * P.tiles_per_img;
+    P.n_cblk = (d.C + G::CB - 1) / G::CB;
+    P.n_oblk = 3 * P.n_cblk;
+    P.tiles_per_split = (P.n_tiles + S - 1) / S;
+    P.R = d.R();
+    P.WHx = 1 + 2 * P.R;
+    P.xslot = P.WHx * G::WIN * 4;
+    P.xg_stage = (L::kGStage + G::CB * P.xslot + 127) / 128 * 128;
+    P.ws = ws;
+    P.err = device_error_word();
+    if (P.err == nullptr) return cudaErrorUnknown;
+    CUtensorMap tmY, tmG, tmX;
+    if (!encode_nchw_f32(&tmY, y, d, d.C, 32, 1, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_nchw_f32(&tmG, g, d, 4 * d.C, kTW32, 1, G::CB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_nchw_f32(&tmX, x, d, d.C, G::WIN, (uint32_t)P.WHx, G::CB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    trace_begin(s, kKBwdDwTf32);
+    bwd_dw_tf32_kernel<K><<<P.n_oblk * S, kThreads, L::kSmemBytes, s>>>(tmY, tmG, tmX, P);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
-// FP32 problems that asked for TF32 backward contractions, K = 3, C <= 64, W a
-// multiple of 4 (16-byte TMA strides), halo radius <= 6, 16-byte aligned tensors.
+// FP32 problems that asked for TF32 backward contractions, K = 3 (halo radius <= 6) or
+// 5 (halo radius <= 10), C <= 64, W a multiple of 4 (16-byte TMA strides), 16-byte
+// aligned tensors.
 bool bwd_dw_tf32_eligible(const Dims& d, const void* g, const void* x, const void* y) {
-    if (d.dtype != 0 || !(d.flags & kFlagTf32Backward) || (d.flags & kFlagCudaCores) || d.K != 3) return false;
-    if (d.C > 64 || d.W % 4 != 0 || d.R() > kMaxR32) return false;
+    if (d.dtype != 0 || !(d.flags & kFlagTf32Backward) || (d.flags & kFlagCudaCores)) return false;
+    if (!(d.K == 3 || d.K == 5)) return false;
+    if (d.C > 64 || d.W % 4 != 0 || d.R() > (d.K == 3 ? Tf32Geom<3>::MAXR : Tf32Geom<5>::MAXR)) return false;
     if (d.O > (1LL << 30) || d.HW > (1LL << 31) - 1024) return false;
     if ((uintptr_t)g % 16 || (uintptr_t)x % 16 || (uintptr_t)y % 16) return false;
     return encode_fn() != nullptr;
 }
 
 int bwd_dw_tf32_splits(const Dims& d, size_t workspace_bytes) {
-    const int n_oblk = 3 * ((d.C + kCB - 1) / kCB);
+    const int cb = d.K == 3 ? Tf32Geom<3>::CB : Tf32Geom<5>::CB;
+    const int n_oblk = 3 * ((d.C + cb - 1) / cb);
     const long long n_tiles = (long long)d.B * d.H * ((d.W + kTW32 - 1) / kTW32);
     int S = num_sms() / n_oblk;
     if (S < 1) S = 1;
@@ -384,35 +442,7 @@ int bwd_dw_tf32_splits(const Dims& d, size_t workspace_bytes) {
 
 cudaError_t launch_bwd_dw_tf32(const Dims& d, const void* g, const void* x, const void* y, float* ws, int S,
                                cudaStream_t s) {
-    static int attr_done[64] = {};
-    {
-        const cudaError_t e = set_max_dynamic_smem((const void*)bwd_dw_tf32_kernel, kSmemBytes, attr_done);
-        if (e != cudaSuccess) return e;
-    }
-    DwTf32Params P;
-    P.d = d;
-    P.tiles_w = (d.W + kTW32 - 1) / kTW32;
-    P.tiles_per_img = d.H * P.tiles_w;
-    P.n_tiles = d.B * P.tiles_per_img;
-    P.n_cblk = (d.C + kCB - 1) / kCB;
-    P.n_oblk = 3 * P.n_cblk;
-    P.tiles_per_split = (P.n_tiles + S - 1) / S;
-    P.R = d.R();
-    P.WHx = 1 + 2 * P.R;
-    P.xslot = P.WHx * kWin32 * 4;
-    P.xg_stage = (kGStage + kCB * P.xslot + 127) / 128 * 128;
-    P.ws = ws;
-    P.err = device_error_word();
-    if (P.err == nullptr) return cudaErrorUnknown;
-    CUtensorMap tmY, tmG, tmX;
-    if (!encode_nchw_f32(&tmY, y, d, d.C, 32, 1, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_nchw_f32(&tmG, g, d, 4 * d.C, kTW32, 1, kCB, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_nchw_f32(&tmX, x, d, d.C, kWin32, (uint32_t)P.WHx, kCB, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    trace_begin(s, kKBwdDwTf32);
-    bwd_dw_tf32_kernel<<<P.n_oblk * S, kThreads, kSmemBytes, s>>>(tmY, tmG, tmX, P);
-    trace_end(s);
-    return cudaGetLastError();
+    return d.K == 3 ? launch_k<3>(d, g, x, y, ws, S, s) : launch_k<5>(d, g, x, y, ws, S, s);
 }
 
 }  // namespace ddpm

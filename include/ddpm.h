@@ -68,8 +68,9 @@ typedef enum { DDPM_FLOAT32 = 0, DDPM_BFLOAT16 = 1 } ddpm_dtype;
  * DDPM_FLAG_TF32_BACKWARD: FP32 problems may run the backward contractions on
  *   TF32 tensor cores (the page allows TF32 for FP32 backward reductions and
  *   recompute, never for the forward).  With it the dW/dbias partial sums run
- *   on tensor cores (TF32 operands, FP32 accumulation) for K = 3, C <= 64, W a
- *   multiple of 4, dilations <= 6 and 16-byte aligned tensors; so does dY
+ *   on tensor cores (TF32 operands, FP32 accumulation) for C <= 64, W a
+ *   multiple of 4, 16-byte aligned tensors and K = 3 with dilations <= 6 or
+ *   K = 5 with dilations <= 5.  For K = 3 so does dY
  *   where C is also a multiple of 16 and the workspace holds the rearranged
  *   weight, and so does dX's recompute of the taps (T = bias + W y as a TF32
  *   GEMM per tap, FP32 accumulation; the products T * grad and their sum stay

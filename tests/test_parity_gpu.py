@@ -481,7 +481,7 @@ def test_filter_backward_full_size(name, dtype):
 
 # --------------------------------------------- FP32 backward, TF32 dW / dbias --
 
-# Shapes the TF32 dW kernel takes (FP32, K = 3, C <= 64, W % 4 == 0, dilations <= 6):
+# Shapes the TF32 dW kernel takes (FP32, K = 3, C <= 64, W % 4 == 0, dilations <= 6; K = 5 below):
 # ragged 64-pixel row tiles, partial blocks of 14 channels, other dilations, several images.
 TF32_SHAPES = [
     Problem(1, 16, 9, 132, 3),               # three tiles per row, the last 4 pixels wide
@@ -556,6 +556,46 @@ def test_tf32_backward_integer_bit_exact(p):
     h = make_integer_inputs(p, 13, "float32")
     d = _dev(h)
     dx, dy, dw, db = run_backward(d, p, flags=binding.DDPM_FLAG_TF32_BACKWARD)
+    torch.cuda.synchronize()
+    rdx, rdy, rdw, rdb = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations,
+                                         bf16=False)
+    np.testing.assert_array_equal(to64(dw), rdw)
+    np.testing.assert_array_equal(to64(db), rdb)
+    np.testing.assert_array_equal(to64(dx), rdx)
+    np.testing.assert_array_equal(to64(dy), rdy)
+
+
+# K = 5: the TF32 dW kernel takes blocks of 5 channels (125 taps of the 128 MMA rows) and
+# 96-column x windows (halo radius <= 10); dX and dY stay IEEE FP32 on CUDA cores.
+TF32_DW_K5_SHAPES = [
+    Problem(1, 10, 12, 72, 5),               # two channel blocks, a ragged 8-pixel tile
+    Problem(2, 64, 9, 64, 5),                # C = 64: 13 blocks, the last holds 4 channels
+    Problem(1, 12, 23, 36, 5, (1, 5, 3)),    # halo radius 10 (dilation 5), a short tile
+    Problem(1, 7, 6, 132, 5, (2, 3, 4)),     # odd C, three tiles per row, radius 8
+]
+
+
+@pytest.mark.parametrize("p", TF32_DW_K5_SHAPES, ids=_id)
+def test_tf32_backward_k5_matches_oracle(p):
+    h = make_inputs(p, 852, "float32")
+    d = _dev(h)
+    flags = binding.DDPM_FLAG_TF32_BACKWARD
+    names = _traced_kernels(lambda: run_backward(d, p, flags=flags))
+    assert "bwd_dw_tf32" in names and "bwd_dw_partial_simt" not in names, names
+    assert "bwd_dx_simt" in names and "bwd_dy_simt" in names, names
+    got = run_backward(d, p, flags=flags)
+    ieee = run_backward(d, p)
+    torch.cuda.synchronize()
+    ref = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations, bf16=False)
+    for name, a, want in zip(("dx", "dy", "dW", "dbias"), got, ref):
+        assert_grad_close(a, want, "float32", name)
+    assert torch.equal(got[0], ieee[0]) and torch.equal(got[1], ieee[1])
+
+
+@pytest.mark.parametrize("p", TF32_DW_K5_SHAPES, ids=_id)
+def test_tf32_backward_k5_integer_bit_exact(p):
+    h = make_integer_inputs(p, 14, "float32")
+    dx, dy, dw, db = run_backward(_dev(h), p, flags=binding.DDPM_FLAG_TF32_BACKWARD)
     torch.cuda.synchronize()
     rdx, rdy, rdw, rdb = oracle.backward(h["grad_out"], h["x"], h["y"], h["weight"], h["bias"], p.K, p.dilations,
                                          bf16=False)
