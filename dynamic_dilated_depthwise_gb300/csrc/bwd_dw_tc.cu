@@ -19,10 +19,15 @@
 //     x windows [CB x (2+2R) x (64 + 2 halo) px], zero-filled outside the image, into a
 //     ring of 2-4 stages (as many as shared memory holds for the halo) that
 //     the formers release as soon as dK is formed;
-//   - eight warps form dK^T[o, px] (bwdtc::form_dk_tile) into a 128B-swizzled
-//     K-major operand;
+//   - two groups of eight warps form dK^T[o, px] (bwdtc::form_dk_tile) into a
+//     128B-swizzled K-major operand, even tiles in one group and buffer, odd
+//     tiles in the other: one group's formation of a tile is a short chain of
+//     shared-memory loads and stores per thread, so two tiles in flight keep the
+//     formers' loads overlapped;
 //   - one thread issues D[o, n] += dK^T[o, px] * Y[n, px] with N = 80 rows: the
-//     64 y channels plus a constant ones row (row 64) that yields dbias.
+//     64 y channels plus a constant ones row (row 64) that yields dbias; the
+//     descriptors are built once and each MMA adds 32-bit offsets to their low
+//     halves.
 // The accumulator stays in TMEM for the whole split and is written once.
 #include "bwd_tc_common.cuh"
 #include "tc.cuh"
@@ -33,7 +38,8 @@ namespace {
 using namespace bwdtc;
 
 constexpr int kNY = 80;           // MMA N: 64 y channels + ones row + 15 zero rows
-constexpr int kFormWarps = 8;
+constexpr int kGroupWarps = 8;                     // warps of one former group
+constexpr int kFormWarps = 2 * kGroupWarps;        // two groups: even and odd tiles
 constexpr int kThreads = 32 * (3 + kFormWarps);   // x/grad producer, MMA, formers, y producer
 constexpr int kYWarp = 2 + kFormWarps;             // warp of the y producer
 constexpr int kYStages = 3;
@@ -100,7 +106,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // access through it stays a shared-memory access (an integer round trip would make
     // them generic loads and stores with 64-bit addresses)
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t y_full[kYStages], y_empty[kYStages], xg_full[kMaxXgStages], xg_empty[kMaxXgStages];
+    // xg_full has one barrier per stage and former group: a parity wait is only sound
+    // for a waiter that has seen the barrier's previous phase, and the two groups take
+    // turns on the shared stages
+    __shared__ uint64_t y_full[kYStages], y_empty[kYStages], xg_full[2][kMaxXgStages], xg_empty[kMaxXgStages];
     __shared__ uint64_t dk_full[2], dk_empty[2], acc_done, mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
@@ -115,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_end = min(t_begin + P.tiles_per_split, P.n_tiles);
     const int n_my = max(0, t_end - t_begin);
     const int NX = P.xg_stages;
+    const int NL = (NX & 1) ? 2 * NX : NX;   // tiles between two uses of one (stage, group) barrier
 
     // this block of taps: dilation dd, channels [c_first, c_first + nc)
     const int dd = ob / P.n_cblk;
@@ -130,11 +140,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&y_empty[s], 1);
         }
         for (int s = 0; s < NX; ++s) {
-            mbar_init(&xg_full[s], 1);
-            mbar_init(&xg_empty[s], kFormWarps);
+            mbar_init(&xg_full[0][s], 1);
+            mbar_init(&xg_full[1][s], 1);
+            mbar_init(&xg_empty[s], kGroupWarps);   // the group that formed the tile
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&dk_full[s], kFormWarps);
+            mbar_init(&dk_full[s], kGroupWarps);
             mbar_init(&dk_empty[s], 1);
         }
         mbar_init(&acc_done, 1);
@@ -173,15 +184,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
                 const int h0 = (ti / P.tiles_w) * kTH, w0 = (ti % P.tiles_w) * kTW;
                 uint8_t* st = sm + kXG + s * P.xg_stage;
-                mbar_arrive_expect_tx(&xg_full[s], bytes);
-                tma_load_4d(st, &tmG, &xg_full[s], w0, h0, (1 + dd) * C + c_first, b);
-                tma_load_4d(st + kGStage, &tmX, &xg_full[s], w0 - G::kHaloCols, h0 - P.R, c_first, b);
+                uint64_t* full = &xg_full[i & 1][s];
+                mbar_arrive_expect_tx(full, bytes);
+                tma_load_4d(st, &tmG, full, w0, h0, (1 + dd) * C + c_first, b);
+                tma_load_4d(st + kGStage, &tmX, full, w0 - G::kHaloCols, h0 - P.R, c_first, b);
                 issued = i + 1;
             }
             // drain: every copy this thread started lands before its shared memory is released
             int never = 0;
             for (int i = issued > NX ? issued - NX : 0; i < issued; ++i)
-                mbar_wait(&xg_full[i % NX], (i / NX) & 1, P.err, &never);
+                mbar_wait(&xg_full[i & 1][i % NX], (i / NL) & 1, P.err, &never);
         }
     } else if (warp == kYWarp) {
         // ------------------------------------------------------- y producer
@@ -211,25 +223,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             // descriptors are built once; each MMA only moves a start address (desc_advance)
             const uint64_t dk_base = smem_desc(smem_u32(sm + kDK), 16, 1024, kSwizzle128B);
             const uint64_t y_base = smem_desc(smem_u32(sm + kYS), 16, 1024, kSwizzle128B);
+            const uint32_t dk_hi = (uint32_t)(dk_base >> 32), y_hi = (uint32_t)(y_base >> 32);
             bool ok = true;
+            int sy = 0, yph = 0;   // y ring stage and phase, stepped by a counter
             for (int i = 0; i < n_my && ok; ++i) {
                 const int s = i & 1, ph = (i >> 1) & 1;
-                const int sy = i % kYStages, yph = (i / kYStages) & 1;
                 if (!mbar_wait(&dk_full[s], ph, P.err, abort_v) || !mbar_wait(&y_full[sy], yph, P.err, abort_v)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t da = desc_advance(dk_base, (uint32_t)s * kDKBytes);
-                const uint64_t ya = desc_advance(y_base, (uint32_t)sy * kYStage);
+                const uint32_t da = (uint32_t)dk_base + (uint32_t)((s * kDKBytes) >> 4);
+                const uint32_t ya = (uint32_t)y_base + (uint32_t)((sy * kYStage) >> 4);
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_f16(tmem, desc_advance(da, half * 16384 + kk * 32), desc_advance(ya, half * kYHalf + kk * 32),
-                                idesc, (i > 0 || half > 0 || kk > 0) ? 1u : 0u);
+                        mma_f16_lh(tmem, da + (uint32_t)((half * 16384 + kk * 32) >> 4), dk_hi,
+                                   ya + (uint32_t)((half * kYHalf + kk * 32) >> 4), y_hi, idesc,
+                                   (i > 0 || half > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&dk_empty[s]);
                 mma_commit(&y_empty[sy]);
+                if (++sy == kYStages) {
+                    sy = 0;
+                    yph ^= 1;
+                }
             }
             if (ok) mma_commit(&acc_done);
             mma_commit(&mma_done);
@@ -238,19 +256,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------- dK formers + epilogue
-        const int et = threadIdx.x - 64;
+        // group grp forms tiles grp, grp + 2, ... into dK^T buffer grp
+        const int grp = (warp - 2) / kGroupWarps;
+        const int et = threadIdx.x - 64 - grp * 32 * kGroupWarps;
         const int slot_elems = P.xslot_bytes / 2;
         bool ok = true;
-        for (int i = 0; i < n_my && ok; ++i) {
+        for (int i = grp; i < n_my && ok; i += 2) {
             const int s = i & 1, ph = (i >> 1) & 1;
-            const int sx = i % NX, xph = (i / NX) & 1;
-            if (!mbar_wait(&xg_full[sx], xph, P.err, abort_v) || !mbar_wait(&dk_empty[s], ph ^ 1, P.err, abort_v)) {
+            const int sx = i % NX, xph = (i / NL) & 1;
+            if (!mbar_wait(&xg_full[grp][sx], xph, P.err, abort_v) || !mbar_wait(&dk_empty[s], ph ^ 1, P.err, abort_v)) {
                 ok = false;
                 break;
             }
             const uint8_t* st = sm + kXG + sx * P.xg_stage;
             form_dk_tile<K>(sm + kDK + s * kDKBytes, reinterpret_cast<const uint32_t*>(st + kGStage),
-                         reinterpret_cast<const bf16*>(st), kPx, nrows, slot_elems, P.R, dil, 0, et, 32 * kFormWarps);
+                         reinterpret_cast<const bf16*>(st), kPx, nrows, slot_elems, P.R, dil, 0, et, 32 * kGroupWarps);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -258,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&xg_empty[sx]);
             }
         }
-        // epilogue: this split's partial sums for the block of taps
+        // epilogue (group 0): this split's partial sums for the block of taps
+        if (grp != 0) ok = false;
         const int q = warp & 3, hc = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         const int rc = row / kTaps;
