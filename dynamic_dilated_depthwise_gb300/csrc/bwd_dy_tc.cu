@@ -13,7 +13,11 @@
 // the MMA releases, and another brings its grad planes [CB x 512 px] and x
 // windows [CB x (8+2R) x (64 + 2 halo)] into a 2-stage ring that the formers release once
 // the four sub-tiles are formed; per block:
-//   - eight warps form each sub-tile's dK^T tile (bwdtc::form_dk_tile);
+//   - two groups of eight warps form the sub-tiles' dK^T tiles
+//     (bwdtc::form_dk_tile), alternate sub-tiles in alternate buffers, so that
+//     two formations are in flight (each is a short chain of shared-memory
+//     loads and stores per thread); with one sub-tile per block the groups
+//     take alternate blocks, and each x/grad stage serves one group;
 //   - one thread issues D_st[px, j] += dK[px, o] * W[o, j] (M = 128 pixels read
 //     MN-major from the dK^T tile, N = 64, K = 128 taps in eight K=16 steps).
 // Four accumulators [128 px x 64 j] fp32 per super tile, double-buffered, fill
@@ -31,7 +35,8 @@ constexpr int kN = 64;            // MMA N: output channels j (zero padded beyon
 // 8-row super tiles would leave most SMs idle (the W block is then read per 128
 // pixels instead of per 512).
 constexpr int kDyMaxR = 5;        // K = 3: halo radius the window buffers hold (10 for K = 5)
-constexpr int kFormWarps = 8;
+constexpr int kGroupWarps = 8;    // warps of one former group
+constexpr int kFormWarps = 2 * kGroupWarps;
 constexpr int kEpiWarps = 4;
 constexpr int kWWarp = 2 + kFormWarps + kEpiWarps;   // warp of the W producer
 constexpr int kThreads = 32 * (3 + kFormWarps + kEpiWarps);
@@ -100,10 +105,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kXgStages; ++s) {
             mbar_init(&xg_full[s], 1);
-            mbar_init(&xg_empty[s], kFormWarps);
+            mbar_init(&xg_empty[s], kSub > 1 ? kFormWarps : kGroupWarps);   // the groups that read the block
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&dk_full[s], kFormWarps);
+            mbar_init(&dk_full[s], kGroupWarps);
             mbar_init(&dk_empty[s], 1);
             mbar_init(&acc_full[s], 1);
             mbar_init(&acc_empty[s], kEpiWarps);
@@ -183,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // descriptors are built once; each MMA only moves a start address (desc_advance)
             const uint64_t dk_base = smem_desc(smem_u32(sm + kDK), 16384, 1024, kSwizzle128B);
             const uint64_t w_base = smem_desc(smem_u32(sm + kWS), 8192, 1024, kSwizzle128B);
+            const uint32_t dk_hi = (uint32_t)(dk_base >> 32), w_hi = (uint32_t)(w_base >> 32);
             bool ok = true;
             for (int tl = 0; tl < n_my && ok; ++tl) {
                 const int tb = tl & 1, tph = (tl >> 1) & 1;
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint64_t wa = desc_advance(w_base, (uint32_t)s * kWStage);
+                    const uint32_t wa = (uint32_t)w_base + (uint32_t)((s * kWStage) >> 4);
                     for (int st = 0; st < kSub; ++st) {
                         const int kd = i * kSub + st, db = kd & 1;
                         if (!mbar_wait(&dk_full[db], (kd >> 1) & 1, P.err, abort_v)) {
@@ -202,12 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t da = desc_advance(dk_base, (uint32_t)db * kDKBytes);
+                        const uint32_t da = (uint32_t)dk_base + (uint32_t)((db * kDKBytes) >> 4);
                         const uint32_t dt = tmem + (tb * kSub + st) * kN;
 #pragma unroll
                         for (int kk = 0; kk < kBlockRows / 16; ++kk)
-                            mma_f16(dt, desc_advance(da, kk * 2048), desc_advance(wa, kk * 2048), idesc,
-                                    (ob > 0 || kk > 0) ? 1u : 0u);
+                            mma_f16_lh(dt, da + (uint32_t)(kk * 128), dk_hi, wa + (uint32_t)(kk * 128), w_hi, idesc,
+                                       (ob > 0 || kk > 0) ? 1u : 0u);
                         mma_commit(&dk_empty[db]);
                     }
                     mma_commit(&w_empty[s]);
@@ -220,12 +226,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 2 + kFormWarps) {
         // ------------------------------------------------------- dK formers
-        const int et = threadIdx.x - 64;
+        // group grp forms the sub-tiles kd with kd % 2 == grp into dK^T buffer grp
+        const int grp = (warp - 2) / kGroupWarps;
+        const int et = threadIdx.x - 64 - grp * 32 * kGroupWarps;
         const int slot_elems = P.xslot_bytes / 2;
         bool ok = true;
         for (int tl = 0; tl < n_my && ok; ++tl) {
             for (int ob = 0; ob < NB && ok; ++ob) {
                 const int i = tl * NB + ob, s = i % kXgStages, ph = (i / kXgStages) & 1;
+                if (kSub == 1 && (i & 1) != grp) continue;   // the other group's block
                 if (!mbar_wait(&xg_full[s], ph, P.err, abort_v)) {
                     ok = false;
                     break;
@@ -235,14 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int dil = dil_of(P.d, dd);
                 const bf16* gs = reinterpret_cast<const bf16*>(sm + kXG + s * kXgStage);
                 const uint32_t* xs32 = reinterpret_cast<const uint32_t*>(sm + kXG + s * kXgStage + kGStage);
-                for (int st = 0; st < kSub; ++st) {
+                for (int st = kSub > 1 ? grp : 0; st < kSub; st += 2) {
                     const int kd = i * kSub + st, db = kd & 1;
                     if (!mbar_wait(&dk_empty[db], ((kd >> 1) & 1) ^ 1, P.err, abort_v)) {
                         ok = false;
                         break;
                     }
                     form_dk_tile<K>(sm + kDK + db * kDKBytes, xs32, gs + st * kPx, kSPx, nrows, slot_elems, P.R, dil,
-                                 st * kTH, et, 32 * kFormWarps);
+                                 st * kTH, et, 32 * kGroupWarps);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&dk_full[db]);
@@ -264,19 +273,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
             const int h0 = (ti / P.tiles_w) * kSTH, w0 = (ti % P.tiles_w) * kTW;
             for (int st = 0; st < kSub; ++st) {
-                uint32_t v[64];
-                const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (tb * kSub + st) * kN;
-                DDPM_TMEM_LD_X16(ta, (v + 0));
-                DDPM_TMEM_LD_X16(ta + 16, (v + 16));
-                DDPM_TMEM_LD_X16(ta + 32, (v + 32));
-                DDPM_TMEM_LD_X16(ta + 48, (v + 48));
-                tmem_ld_wait();
                 const int h = h0 + st * kTH + tr, w = w0 + tcol;
-                if (h < P.d.H && w < P.d.W) {
-                    bf16* out = P.dy + (long long)b * C * P.d.HW + (long long)h * P.d.W + w;
+                bf16* out = P.dy + (long long)b * C * P.d.HW + (long long)h * P.d.W + w;
 #pragma unroll
-                    for (int j = 0; j < kN; ++j)
-                        if (j < C) out[(long long)j * P.d.HW] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                for (int jh = 0; jh < kN; jh += 32) {   // 32 columns at a time (register budget)
+                    uint32_t v[32];
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (tb * kSub + st) * kN + jh;
+                    DDPM_TMEM_LD_X16(ta, (v + 0));
+                    DDPM_TMEM_LD_X16(ta + 16, (v + 16));
+                    tmem_ld_wait();
+                    if (h < P.d.H && w < P.d.W) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (jh + j < C)
+                                out[(long long)(jh + j) * P.d.HW] = __float2bfloat16_rn(__uint_as_float(v[j]));
+                    }
                 }
             }
             tc_fence_before();
