@@ -148,6 +148,31 @@ __device__ __forceinline__ void lds_slots(uint32_t addr, unsigned short* v, std:
     ((v[I] = tc::lds_u16<I * SLOT>(addr)), ...);
 }
 
+// The constant MMA operands of a CTA: a ones column (A, [128 x 16]) and the bias column of
+// each dilation (B, [N x 16]), K = 16, no swizzle.  In the core-matrix layout row r's k = 0..7
+// sit at (r/8)*256 + (r%8)*16 and k = 8..15 128 bytes further; one thread per row writes both
+// 16-byte halves, and each bias value is one load (a loop of dependent cold loads here cost
+// microseconds).  Kept out of line: it runs once per CTA and leaves the epilogue's registers alone.
+template <int K>
+__device__ __noinline__ void fill_const_operands(uint8_t* sm, const bf16* bias, int C, int c0, int et) {
+    using L = FwdLayout<K>;
+    constexpr int kN = L::kN, kTaps = L::kTaps, kCG = L::kCG, nthr = 32 * L::kEpiWarps;
+    for (int m = et; m < kTile; m += nthr) {
+        uint8_t* r = sm + L::kSOnes + (m / 8) * 256 + (m % 8) * 16;
+        *reinterpret_cast<uint4*>(r) = make_uint4(0x3F80u, 0u, 0u, 0u);   // bf16 1.0 in column 0
+        *reinterpret_cast<uint4*>(r + 128) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int i = et; i < 3 * kN; i += nthr) {
+        const int dd = i / kN, n = i - dd * kN;
+        // columns n < CG*K*K are this group's taps (o < O: C is a multiple of CG), the rest padding
+        uint32_t v = 0u;
+        if (bias != nullptr && n < kCG * kTaps) v = __bfloat16_as_ushort(bias[(dd * C + c0) * kTaps + n]);
+        uint8_t* r = sm + L::kSBias + dd * kN * 32 + (n / 8) * 256 + (n % 8) * 16;
+        *reinterpret_cast<uint4*>(r) = make_uint4(v, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(r + 128) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 template <int K>
 __global__ void __launch_bounds__(FwdLayout<K>::kThreads, FwdLayout<K>::kCtasPerSm)
     forward_tc_kernel(const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmW,
@@ -197,20 +222,7 @@ __global__ void __launch_bounds__(FwdLayout<K>::kThreads, FwdLayout<K>::kCtasPer
     if (warp == 1) tmem_alloc(&tmem_slot, kTmemCols);
     if (warp >= kEpi0) {
         // constant MMA operands: a ones column (A) and the bias column (B), K = 16, no swizzle
-        const int et = threadIdx.x - 32 * kEpi0;
-        for (int i = et; i < kTile * 16; i += 32 * kEpiWarps) {
-            const int m = i / 16, k = i % 16;
-            *reinterpret_cast<bf16*>(sm + kSOnes + (m / 8) * 256 + (k / 8) * 128 + (m % 8) * 16 + (k % 8) * 2) =
-                __float2bfloat16(k == 0 ? 1.0f : 0.0f);
-        }
-        for (int i = et; i < 3 * kN * 16; i += 32 * kEpiWarps) {
-            const int dd = i / (kN * 16), rem = i % (kN * 16), n = rem / 16, k = rem % 16;
-            const long long o = (long long)(dd * C + c0) * kTaps + n;
-            bf16 v = __float2bfloat16(0.0f);
-            if (k == 0 && P.bias != nullptr && o < P.d.O) v = P.bias[o];
-            *reinterpret_cast<bf16*>(sm + kSBias + dd * kN * 32 + (n / 8) * 256 + (k / 8) * 128 + (n % 8) * 16 +
-                                     (k % 8) * 2) = v;
-        }
+        fill_const_operands<K>(sm, P.bias, C, c0, threadIdx.x - 32 * kEpi0);
         fence_proxy_async_smem();
     }
     tc_fence_before();
