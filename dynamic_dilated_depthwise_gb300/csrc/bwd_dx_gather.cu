@@ -178,17 +178,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int k = i / (kNBias * 128), g = (i / 64) % (2 * kNBias), e = i & 7;
             oh[i] = (g * 8 + e == k) ? (unsigned short)0x3F80u : (unsigned short)0u;
         }
-        unsigned short* bt = reinterpret_cast<unsigned short*>(sm + P.obt);
-        for (int i = et; i < F::kBiasTab / 2; i += nt) {    // [d][c/8][k-group][c%8][e], k = group*8 + e
-            const int per_d = 8 * kNBias * 128;
-            const int dd = i / per_d, r = i % per_d;
-            const int c = (r / (kNBias * 128)) * 8 + ((r >> 3) & 7), k = ((r / 64) % (2 * kNBias)) * 8 + (r & 7);
-            unsigned short v = 0;
-            if (P.bias != nullptr && c < C && k < kKK) {
-                const bf16 bb = P.bias[((long long)dd * C + c) * kKK + k];
-                v = *reinterpret_cast<const unsigned short*>(&bb);
+        // bias table [d][c/8][k-group g][c%8][e], k = g*8 + e: one thread per (d, c) loads the
+        // channel's K*K taps (independent loads, one latency) and writes its 16-byte chunks
+        for (int i = et; i < 3 * 64; i += nt) {
+            const int dd = i >> 6, c = i & 63;
+            unsigned short b[16 * kNBias];
+#pragma unroll
+            for (int k = 0; k < 16 * kNBias; ++k) b[k] = 0;
+            if (P.bias != nullptr && c < C) {
+                const unsigned short* bp =
+                    reinterpret_cast<const unsigned short*>(P.bias) + ((long long)dd * C + c) * kKK;
+#pragma unroll
+                for (int k = 0; k < kKK; ++k) b[k] = bp[k];
             }
-            bt[i] = v;
+            uint8_t* ch = sm + P.obt + (dd * 8 * kNBias * 128 + (c >> 3) * (kNBias * 128) + (c & 7) * 8) * 2;
+#pragma unroll
+            for (int g = 0; g < 2 * kNBias; ++g) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) w[e] = (uint32_t)b[g * 8 + 2 * e] | ((uint32_t)b[g * 8 + 2 * e + 1] << 16);
+                *reinterpret_cast<uint4*>(ch + g * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
         const int nzero = (2 * P.nks - P.nch) * P.npos;     // chunk nch when C/8 is odd
         for (int i = et; i < nzero; i += nt)

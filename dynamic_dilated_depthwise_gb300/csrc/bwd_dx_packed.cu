@@ -363,16 +363,23 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int k = i >> 7, kc = (i >> 6) & 1, e = i & 7;
             oh[i] = (kc * 8 + e == k) ? (unsigned short)0x3F80u : (unsigned short)0u;
         }
-        unsigned short* bt = reinterpret_cast<unsigned short*>(sm + P.obt);
-        for (int i = et; i < kPBiasTab / 2; i += nt) {      // [d][c/8][chunk kc][c%8][e], k = kc*8 + e
-            const int dd = i >> 10, r = i & 1023;
-            const int c = (r >> 7) * 8 + ((r >> 3) & 7), k = ((r >> 6) & 1) * 8 + (r & 7);
-            unsigned short v = 0;
-            if (P.bias != nullptr && c < C && k < 9) {
-                const bf16 bb = P.bias[((long long)dd * C + c) * 9 + k];
-                v = *reinterpret_cast<const unsigned short*>(&bb);
+        // bias table [d][c/8][chunk kc][c%8][e], k = kc*8 + e: one thread per (d, c) loads the
+        // channel's nine taps (independent loads, one latency) and writes its two 16-byte chunks
+        for (int i = et; i < 3 * 64; i += nt) {
+            const int dd = i >> 6, c = i & 63;
+            uint32_t v[5] = {0u, 0u, 0u, 0u, 0u};
+            if (P.bias != nullptr && c < C) {
+                const unsigned short* bp = reinterpret_cast<const unsigned short*>(P.bias) + ((long long)dd * C + c) * 9;
+                unsigned short b[9];
+#pragma unroll
+                for (int k = 0; k < 9; ++k) b[k] = bp[k];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[k] = (uint32_t)b[2 * k] | ((uint32_t)b[2 * k + 1] << 16);
+                v[4] = b[8];
             }
-            bt[i] = v;
+            uint8_t* ch = sm + P.obt + (dd * 1024 + (c >> 3) * 128 + (c & 7) * 8) * 2;
+            *reinterpret_cast<uint4*>(ch) = make_uint4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<uint4*>(ch + 128) = make_uint4(v[4], 0u, 0u, 0u);
         }
         const int nzero = (2 * P.nks - P.nch) * P.npos;     // chunk nch when C/8 is odd
         for (int i = et; i < nzero; i += nt)

@@ -54,7 +54,10 @@ constexpr int kYW = kRaw + 2 * kRawStage;             // 10 chunks x positions x
 constexpr int kYWBytes = 10 * kMaxPos * 16;           // 89600
 constexpr int kGW = kYW + kYWBytes;                   // [position][64] bf16, 16-byte chunks swizzled
 constexpr int kGWBytes = kMaxPos * 128;               // 71680
-constexpr int kSmemBytes = kGW + kGWBytes + 1024;
+constexpr int kBC = kGW + kGWBytes;                   // copy of the bias [3 d][64 c][9 k] bf16
+constexpr int kBCBytes = 3 * 64 * 9 * 2;              // 3456
+constexpr int kSmemBytes = kBC + kBCBytes + 1024;
+static_assert(kSmemBytes <= 232448 - 1024, "shared memory");
 static_assert(kWTStage % 1024 == 0, "W tap tiles need 1 KiB alignment");
 static_assert(kRaw % 128 == 0 && kRawStage % 128 == 0 && kYW % 16 == 0 && kGW % 16 == 0, "staging alignment");
 
@@ -115,6 +118,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(&tmem_slot, 512);
+    {
+        // the bias into shared memory once ([d][c][k], zero for c >= C): the W producer writes
+        // each tap's bias tile from there, with no global load on its per-tap path.  All of a
+        // thread's loads are issued before its stores.
+        constexpr int kN = 3 * 64 * 9, kPer = (kN + kThreads - 1) / kThreads;
+        unsigned short v[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = threadIdx.x + j * kThreads;
+            const int dd = i / 576, c = (i / 9) % 64, k = i % 9;
+            v[j] = (i < kN && P.bias != nullptr && c < C)
+                       ? reinterpret_cast<const unsigned short*>(P.bias)[((long long)dd * C + c) * 9 + k]
+                       : (unsigned short)0;
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = threadIdx.x + j * kThreads;
+            if (i < kN) reinterpret_cast<unsigned short*>(sm + kBC)[i] = v[j];
+        }
+    }
     if (warp >= 2 && warp < kRawWarp) {
         // constant chunks 8 (ones column) and 9 (zeros) of the y window: the bias K-step
         const int et = threadIdx.x - 64;
@@ -148,12 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* bt = sm + kWT + st * kWTStage + 8192;
                 for (int rr = 0; rr < 2; ++rr) {
                     const int c = 2 * lane + rr;
-                    const long long o = (long long)(dd * C + c) * 9 + k;
-                    uint32_t bv = 0u;
-                    if (P.bias != nullptr && c < C) {
-                        const bf16 b = P.bias[o];
-                        bv = (uint32_t)(*reinterpret_cast<const unsigned short*>(&b));
-                    }
+                    const uint32_t bv = reinterpret_cast<const unsigned short*>(sm + kBC)[(dd * 64 + c) * 9 + k];
                     *reinterpret_cast<uint4*>(bt + (c / 8) * 256 + (c % 8) * 16) = make_uint4(bv, 0u, 0u, 0u);
                     *reinterpret_cast<uint4*>(bt + (c / 8) * 256 + 128 + (c % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }

@@ -186,11 +186,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int k = i >> 7, g = (i >> 5) & 3, e = i & 3;
             oh[i] = (g * 4 + e == k) ? 1.0f : 0.0f;
         }
-        float* bt = reinterpret_cast<float*>(sm + P.obt);
-        for (int i = et; i < kBiasTab / 4; i += nt) {       // [d][c/8][k/4][c%8][k%4]
-            const int dd = i >> 10, r = i & 1023;
-            const int c = (r >> 7) * 8 + ((r >> 2) & 7), k = ((r >> 5) & 3) * 4 + (r & 3);
-            bt[i] = (P.bias != nullptr && c < C && k < 9) ? P.bias[((long long)dd * C + c) * 9 + k] : 0.0f;
+        // bias table [d][c/8][k/4][c%8][k%4]: one thread per (d, c) loads the channel's nine taps
+        // (independent loads, one latency) and writes its four 16-byte chunks
+        for (int i = et; i < 3 * 64; i += nt) {
+            const int dd = i >> 6, c = i & 63;
+            float b[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) b[k] = 0.0f;
+            if (P.bias != nullptr && c < C) {
+                const float* bp = P.bias + ((long long)dd * C + c) * 9;
+#pragma unroll
+                for (int k = 0; k < 9; ++k) b[k] = bp[k];
+            }
+            float* ch = reinterpret_cast<float*>(sm + P.obt) + dd * 1024 + (c >> 3) * 128 + (c & 7) * 4;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<float4*>(ch + g * 32) = make_float4(b[4 * g], b[4 * g + 1], b[4 * g + 2], b[4 * g + 3]);
         }
         const int nzero = (2 * P.nks - P.nch4) * P.npos;    // chunk nch4 when C/4 is odd
         for (int i = et; i < nzero; i += nt)
