@@ -13,14 +13,15 @@
 //     consecutive slots are eight consecutive positions of one window row, so
 //     the A operand of tap (dy, dx) is the same window at a start offset of
 //     ((R-dy)*WW + (R-dx)) * 16 bytes (row-group stride WW * 16);
-//   - two constant chunks (a ones column and zeros) make a fifth K=16 step
-//     that adds the bias, whose B tile the producer writes per tap;
+//   - a fifth K=16 step adds the bias: A is a constant 8-row ones column read
+//     by every row group (row-group stride 0), B the bias tile the producer
+//     writes per tap;
 //   - the producer brings W's rows of tap (d, k) for all channels by TMA
-//     (a 3-D view of W: [dc][k][j]) into a 4-stage ring;
+//     (a 3-D view of W: [dc][k][j]) into a 3-stage ring;
 //   - D of each tap lands in one of eight TMEM buffers [128 x 64];
 //   - a second producer warp streams the raw windows -- 8-channel chunks
 //     [8 ch][16+2R rows][24 cols] of y and of each dilation's grad planes --
-//     by TMA through a 2-stage ring; eight worker warps transpose each chunk
+//     by TMA through a 4-stage ring; eight worker warps transpose each chunk
 //     into the K-major y window or the position-major grad window, then per
 //     tap round the taps to bf16 and accumulate tap * grad at the gathered
 //     position.
@@ -40,7 +41,8 @@ constexpr int kTaps = 27;
 constexpr int kWorkWarps = 8;
 constexpr int kThreads = 32 * (3 + kWorkWarps);   // W producer, MMA, 8 workers, raw producer
 constexpr int kRawWarp = 2 + kWorkWarps;
-constexpr int kStages = 4;
+constexpr int kStages = 3;               // W ring
+constexpr int kRawStages = 4;            // raw chunk ring
 constexpr int kDBufs = 8;
 constexpr int kRawCols = 24;              // raw window columns: origin w0 - 8 keeps TMA 16-byte aligned
 constexpr int kRawStage = 8 * (kDxTH + 2 * kDxMaxR) * kRawCols * 2;   // 10752
@@ -49,17 +51,19 @@ constexpr int kChunks = 8 + 3 * 8;        // raw chunks per tile: y, then grad o
 // shared memory (bytes from a 1024-aligned base)
 constexpr int kWTStage = 8192 + 2048;                 // W tap tile (SW128, 64 rows) + bias tile
 constexpr int kWT = 0;
-constexpr int kRaw = kWT + kStages * kWTStage;        // 2 x raw chunk [8 ch][rows][24] bf16
-constexpr int kYW = kRaw + 2 * kRawStage;             // 10 chunks x positions x 16 B
-constexpr int kYWBytes = 10 * kMaxPos * 16;           // 89600
+constexpr int kRaw = kWT + kStages * kWTStage;        // raw chunk ring [8 ch][rows][24] bf16
+constexpr int kYW = kRaw + kRawStages * kRawStage;    // 8 chunks x positions x 16 B
+constexpr int kYWBytes = 8 * kMaxPos * 16;            // 71680
 constexpr int kGW = kYW + kYWBytes;                   // [position][64] bf16, 16-byte chunks swizzled
 constexpr int kGWBytes = kMaxPos * 128;               // 71680
 constexpr int kBC = kGW + kGWBytes;                   // copy of the bias [3 d][64 c][9 k] bf16
 constexpr int kBCBytes = 3 * 64 * 9 * 2;              // 3456
-constexpr int kSmemBytes = kBC + kBCBytes + 1024;
+constexpr int kOnes = kBC + kBCBytes;                 // bias K-step A: [8 rows][16 k], column 0 ones
+constexpr int kSmemBytes = kOnes + 256 + 1024;
 static_assert(kSmemBytes <= 232448 - 1024, "shared memory");
+static_assert(kRaw % 128 == 0 && kRawStage % 128 == 0 && kYW % 16 == 0 && kGW % 16 == 0 && kOnes % 16 == 0,
+              "staging alignment");
 static_assert(kWTStage % 1024 == 0, "W tap tiles need 1 KiB alignment");
-static_assert(kRaw % 128 == 0 && kRawStage % 128 == 0 && kYW % 16 == 0 && kGW % 16 == 0, "staging alignment");
 
 struct DxTcParams {
     Dims d;
@@ -74,6 +78,26 @@ struct DxTcParams {
 
 __device__ __forceinline__ void work_bar() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kWorkWarps) : "memory"); }
 
+// Window positions per worker thread: every position of the window at one pass.
+constexpr int kPosPerThread = (kMaxPos + 32 * kWorkWarps - 1) / (32 * kWorkWarps);   // 3
+
+// The eight channels of a raw chunk [8 ch][rows][kRawCols] at this thread's window positions
+// et, et + 256, ... as bf16 pairs; every load is issued before any result is used (one
+// shared-memory latency instead of one per position).  Positions beyond the window read
+// position 0 (inside the chunk) and are not stored.
+__device__ __forceinline__ void gather_positions(uint32_t (&pk)[kPosPerThread][4], const unsigned short* raw, int et,
+                                                 int npos, int WW, int R, int rplane) {
+#pragma unroll
+    for (int u = 0; u < kPosPerThread; ++u) {
+        int pos = et + u * 32 * kWorkWarps;
+        if (pos >= npos) pos = 0;
+        const int row = pos / WW, re = row * kRawCols + (pos - row * WW) + (8 - R);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            pk[u][e] = (uint32_t)raw[(2 * e) * rplane + re] | ((uint32_t)raw[(2 * e + 1) * rplane + re] << 16);
+    }
+}
+
 // bf16 (nearest even) of an fp32 value, returned as fp32
 __device__ __forceinline__ float round_bf16(float t) { return __bfloat162float(__float2bfloat16_rn(t)); }
 
@@ -87,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // them generic loads and stores with 64-bit addresses)
     uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ uint64_t wt_full[kStages], wt_empty[kStages], d_full[kDBufs], d_empty[kDBufs], yw_full, yw_empty,
-        raw_full[2], raw_empty[2], mma_done;
+        raw_full[kRawStages], raw_empty[kRawStages], mma_done;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     volatile int* abort_v = &abort_flag;
@@ -110,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&yw_full, kWorkWarps);
         mbar_init(&yw_empty, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kRawStages; ++i) {
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], kWorkWarps);
         }
@@ -139,12 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (warp >= 2 && warp < kRawWarp) {
-        // constant chunks 8 (ones column) and 9 (zeros) of the y window: the bias K-step
+        // the bias K-step's A operand: one 8-row core-matrix pair (k = 0..7, then 8..15 at +128)
+        // with a one in column 0, read by every row group (stride 0)
         const int et = threadIdx.x - 64;
-        for (int p = et; p < 2 * npos; p += 32 * kWorkWarps) {
-            const uint4 v = p < npos ? make_uint4(0x3F80u, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(sm + kYW + (8 * npos + p) * 16) = v;
-        }
+        if (et < 16)
+            *reinterpret_cast<uint4*>(sm + kOnes + et * 16) =
+                et < 8 ? make_uint4(0x3F80u, 0u, 0u, 0u) : make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -199,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t y_base = smem_desc(smem_u32(sm + kYW), lbo_y, sbo_y, kSwizzleNone);
             const uint64_t w_base = smem_desc(smem_u32(sm + kWT), 16, 1024, kSwizzle128B);
             const uint64_t bias_base = smem_desc(smem_u32(sm + kWT + 8192), 128, 256, kSwizzleNone);
+            const uint64_t ones = smem_desc(smem_u32(sm + kOnes), 128, 0, kSwizzleNone);
             bool ok = true;
             for (int tl = 0; tl < n_my && ok; ++tl) {
                 if (!mbar_wait(&yw_full, tl & 1, P.err, abort_v)) break;
@@ -220,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_f16(dt, desc_advance(ya, 2 * kk * lbo_y), desc_advance(wt, kk * 32), idesc, kk > 0);
-                    mma_f16(dt, desc_advance(ya, 8 * lbo_y), desc_advance(bias_base, (uint32_t)st * kWTStage), idesc, 1);
+                    mma_f16(dt, ones, desc_advance(bias_base, (uint32_t)st * kWTStage), idesc, 1);
                     mma_commit(&d_full[buf]);
                     mma_commit(&wt_empty[st]);
                 }
@@ -243,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = t / P.tiles_per_img, ti = t % P.tiles_per_img;
                 const int h0 = (ti / P.tiles_w) * kDxTH, w0 = (ti % P.tiles_w) * kDxTW;
                 for (int idx = 0; idx < kChunks; ++idx) {
-                    const int i = tl * kChunks + idx, rs = i & 1;
-                    if (!mbar_wait(&raw_empty[rs], ((i >> 1) & 1) ^ 1, P.err, abort_v)) {
+                    const int i = tl * kChunks + idx, rs = i % kRawStages;
+                    if (!mbar_wait(&raw_empty[rs], ((i / kRawStages) & 1) ^ 1, P.err, abort_v)) {
                         ok = false;
                         break;
                     }
@@ -260,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             int never = 0;
-            for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-                mbar_wait(&raw_full[i & 1], (i >> 1) & 1, P.err, &never);
+            for (int i = issued > kRawStages ? issued - kRawStages : 0; i < issued; ++i)
+                mbar_wait(&raw_full[i % kRawStages], (i / kRawStages) & 1, P.err, &never);
         }
     } else {
         // ------------------------------------------------------- workers
@@ -280,19 +305,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // y window: [chunk][position][8 channels] from the raw chunks (zero outside the image / beyond C)
             if (!mbar_wait(&yw_empty, (tl & 1) ^ 1, P.err, abort_v)) break;
             for (int jc = 0; jc < 8 && ok; ++jc) {
-                const int i = tl * kChunks + jc, rs = i & 1;
-                if (!mbar_wait(&raw_full[rs], (i >> 1) & 1, P.err, abort_v)) {
+                const int i = tl * kChunks + jc, rs = i % kRawStages;
+                if (!mbar_wait(&raw_full[rs], (i / kRawStages) & 1, P.err, abort_v)) {
                     ok = false;
                     break;
                 }
                 const unsigned short* raw = reinterpret_cast<const unsigned short*>(sm + kRaw + rs * kRawStage);
-                for (int pos = et; pos < npos; pos += 32 * kWorkWarps) {
-                    const int row = pos / WW, re = row * kRawCols + (pos - row * WW) + (8 - R);
-                    uint32_t pk[4];
+                uint32_t pk[kPosPerThread][4];
+                gather_positions(pk, raw, et, npos, WW, R, rplane);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        pk[e] = (uint32_t)raw[(2 * e) * rplane + re] | ((uint32_t)raw[(2 * e + 1) * rplane + re] << 16);
-                    *reinterpret_cast<uint4*>(ywp + (jc * npos + pos) * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                for (int u = 0; u < kPosPerThread; ++u) {
+                    const int pos = et + u * 32 * kWorkWarps;
+                    if (pos < npos)
+                        *reinterpret_cast<uint4*>(ywp + (jc * npos + pos) * 16) =
+                            make_uint4(pk[u][0], pk[u][1], pk[u][2], pk[u][3]);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&raw_empty[rs]);
@@ -302,39 +328,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&yw_full);
 
-            // dx = grad (channel block 0) + the gathered sum: the accumulators start from the
-            // identity term, loaded now so that its latency hides behind the gather
+            // dx = grad (channel block 0) + the gathered sum.  The identity term is only
+            // prefetched into L2 here and loaded after the taps: a load still in flight would
+            // hold up the next mbarrier wait (its acquire orders it after the load).  Addresses
+            // are clamped into the tensor (validity is applied at the store).
             const int h = h0 + r, w = w0 + c;
             const bool inside = h < H && w < W;
             const long long pix = inside ? (long long)h * W + w : 0;
-            float acc[32];
-            {
-                const bf16* g0p = P.g + (long long)b * 4 * C * HW + pix;
+            const bf16* g0p = P.g + (long long)b * 4 * C * HW + pix;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int ch = hc * 32 + i;
-                    acc[i] = (inside && ch < C) ? __bfloat162float(__ldg(g0p + (long long)ch * HW)) : 0.0f;
-                }
-            }
+            for (int i = 0; i < 32; ++i)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(g0p + (long long)min(hc * 32 + i, C - 1) * HW));
+            float acc[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
             for (int dd = 0; dd < 3 && ok; ++dd) {
                 const int dil = dil_of(P.d, dd);
                 // grad window of dilation dd: [position][64 channels] bf16, 16-byte chunks rotated by position
                 work_bar();
                 for (int jc = 0; jc < 8 && ok; ++jc) {
-                    const int i = tl * kChunks + 8 + dd * 8 + jc, rs = i & 1;
-                    if (!mbar_wait(&raw_full[rs], (i >> 1) & 1, P.err, abort_v)) {
+                    const int i = tl * kChunks + 8 + dd * 8 + jc, rs = i % kRawStages;
+                    if (!mbar_wait(&raw_full[rs], (i / kRawStages) & 1, P.err, abort_v)) {
                         ok = false;
                         break;
                     }
                     const unsigned short* raw = reinterpret_cast<const unsigned short*>(sm + kRaw + rs * kRawStage);
-                    for (int pos = et; pos < npos; pos += 32 * kWorkWarps) {
-                        const int row = pos / WW, re = row * kRawCols + (pos - row * WW) + (8 - R);
-                        uint32_t pk[4];
+                    uint32_t pk[kPosPerThread][4];
+                    gather_positions(pk, raw, et, npos, WW, R, rplane);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            pk[e] = (uint32_t)raw[(2 * e) * rplane + re] | ((uint32_t)raw[(2 * e + 1) * rplane + re] << 16);
-                        *reinterpret_cast<uint4*>(gwp + pos * 128 + ((jc ^ (pos & 7)) << 4)) =
-                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    for (int u = 0; u < kPosPerThread; ++u) {
+                        const int pos = et + u * 32 * kWorkWarps;
+                        if (pos < npos)
+                            *reinterpret_cast<uint4*>(gwp + pos * 128 + ((jc ^ (pos & 7)) << 4)) =
+                                make_uint4(pk[u][0], pk[u][1], pk[u][2], pk[u][3]);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&raw_empty[rs]);
@@ -375,10 +401,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if (inside) {
                 bf16* dxp = P.dx + (long long)b * C * HW + pix;
+                // a base the compiler cannot match with the prefetch's: otherwise it keeps the 32
+                // prefetched addresses live across the taps
+                const bf16* g0q = g0p;
+                asm volatile("" : "+l"(g0q));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int ch = hc * 32 + i;
-                    if (ch < C) dxp[(long long)ch * HW] = __float2bfloat16_rn(acc[i]);
+                for (int hh = 0; hh < 32; hh += 16) {   // 16 channels at a time (register budget)
+                    float g0[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        g0[i] = __bfloat162float(__ldg(g0q + (long long)min(hc * 32 + hh + i, C - 1) * HW));
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int ch = hc * 32 + hh + i;
+                        if (ch < C) dxp[(long long)ch * HW] = __float2bfloat16_rn(g0[i] + acc[hh + i]);
+                    }
                 }
             }
         }
