@@ -98,8 +98,23 @@ __device__ __forceinline__ void gather_positions(uint32_t (&pk)[kPosPerThread][4
     }
 }
 
-// bf16 (nearest even) of an fp32 value, returned as fp32
-__device__ __forceinline__ float round_bf16(float t) { return __bfloat162float(__float2bfloat16_rn(t)); }
+// bf16x2 of two fp32 values (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// a0 += lo(t) * lo(g), a1 += hi(t) * hi(g): bf16 operands, FP32 accumulate, one rounding
+__device__ __forceinline__ void fma2_bf16_f32(float& a0, float& a1, uint32_t t, uint32_t g) {
+    asm("{\n\t.reg .b16 tl, th, gl, gh;\n\t"
+        "mov.b32 {tl, th}, %2;\n\t"
+        "mov.b32 {gl, gh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, tl, gl, %0;\n\t"
+        "fma.rn.f32.bf16 %1, th, gh, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(t), "r"(g));
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dx_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
@@ -390,10 +405,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
                         for (int f = 0; f < 4; ++f) {
-                            const float g0 = __uint_as_float(gw[f] << 16), g1 = __uint_as_float(gw[f] & 0xFFFF0000u);
+                            // the tap rounded to bf16, times grad: exact product, FP32 accumulate
                             const int ci = e * 8 + 2 * f;
-                            acc[ci] = fmaf(round_bf16(__uint_as_float(v[ci])), g0, acc[ci]);
-                            acc[ci + 1] = fmaf(round_bf16(__uint_as_float(v[ci + 1])), g1, acc[ci + 1]);
+                            fma2_bf16_f32(acc[ci], acc[ci + 1],
+                                          pack_bf16x2(__uint_as_float(v[ci]), __uint_as_float(v[ci + 1])), gw[f]);
                         }
                     }
                 }
