@@ -20,7 +20,8 @@
 //     (a 3-D view of W: [dc][k][j]) into a 3-stage ring;
 //   - D of each tap lands in one of eight TMEM buffers [128 x 64];
 //   - a second producer warp streams the raw windows -- 8-channel chunks
-//     [8 ch][16+2R rows][24 cols] of y and of each dilation's grad planes --
+//     [8 ch][16+2R rows][24 cols] of y and of each dilation's grad planes, then
+//     the tile's own grad block 0 (the identity term) as two [32 ch][16][8] chunks --
 //     by TMA through a 4-stage ring; eight worker warps transpose each chunk
 //     into the K-major y window or the position-major grad window, then per
 //     tap round the taps to bf16 and accumulate tap * grad at the gathered
@@ -46,7 +47,12 @@ constexpr int kRawStages = 4;            // raw chunk ring
 constexpr int kDBufs = 8;
 constexpr int kRawCols = 24;              // raw window columns: origin w0 - 8 keeps TMA 16-byte aligned
 constexpr int kRawStage = 8 * (kDxTH + 2 * kDxMaxR) * kRawCols * 2;   // 10752
-constexpr int kChunks = 8 + 3 * 8;        // raw chunks per tile: y, then grad of each dilation
+// raw chunks per tile: y, the grad of each dilation, then the identity term (grad block 0 of
+// the tile itself, [32 ch][16 rows][8 cols] per chunk)
+constexpr int kChunks = 8 + 3 * 8 + 2;
+constexpr int kIdChunk = 8 + 3 * 8;
+constexpr int kIdBytes = 32 * kDxTH * kDxTW * 2;      // 8192
+static_assert(kIdBytes <= 8 * (kDxTH + 2 * kDxMaxR) * kRawCols * 2, "an identity chunk fits a raw stage");
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr int kWTStage = 8192 + 2048;                 // W tap tile (SW128, 64 rows) + bias tile
@@ -118,7 +124,8 @@ __device__ __forceinline__ void fma2_bf16_f32(float& a0, float& a1, uint32_t t, 
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dx_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmY,
-                     const __grid_constant__ CUtensorMap tmG, const DxTcParams P) {
+                     const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmI,
+                     const DxTcParams P) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
     // 1 KiB-aligned base, derived by pointer arithmetic on the shared array so that every
@@ -275,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tmY);
             prefetch_tmap(&tmG);
+            prefetch_tmap(&tmI);
             const uint32_t raw_bytes = 8u * (uint32_t)P.WH * kRawCols * 2;
             int issued = 0;
             bool ok = true;
@@ -289,12 +297,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     uint8_t* dst = sm + kRaw + rs * kRawStage;
-                    mbar_arrive_expect_tx(&raw_full[rs], raw_bytes);
+                    mbar_arrive_expect_tx(&raw_full[rs], idx < kIdChunk ? raw_bytes : (uint32_t)kIdBytes);
                     if (idx < 8) {
                         tma_load_4d(dst, &tmY, &raw_full[rs], w0 - 8, h0 - R, idx * 8, b);
                     } else {
                         const int dd = (idx - 8) / 8, jc = (idx - 8) % 8;
-                        tma_load_4d(dst, &tmG, &raw_full[rs], w0 - 8, h0 - R, (1 + dd) * C + jc * 8, b);
+                        if (idx < kIdChunk)
+                            tma_load_4d(dst, &tmG, &raw_full[rs], w0 - 8, h0 - R, (1 + dd) * C + jc * 8, b);
+                        else
+                            tma_load_4d(dst, &tmI, &raw_full[rs], w0, h0, (idx - kIdChunk) * 32, b);
                     }
                     issued = i + 1;
                 }
@@ -343,17 +354,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&yw_full);
 
-            // dx = grad (channel block 0) + the gathered sum.  The identity term is only
-            // prefetched into L2 here and loaded after the taps: a load still in flight would
-            // hold up the next mbarrier wait (its acquire orders it after the load).  Addresses
-            // are clamped into the tensor (validity is applied at the store).
+            // dx = grad (channel block 0) + the gathered sum; the identity term arrives as the
+            // tile's last two raw chunks
             const int h = h0 + r, w = w0 + c;
             const bool inside = h < H && w < W;
             const long long pix = inside ? (long long)h * W + w : 0;
-            const bf16* g0p = P.g + (long long)b * 4 * C * HW + pix;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(g0p + (long long)min(hc * 32 + i, C - 1) * HW));
             float acc[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.0f;
@@ -414,25 +419,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
-            if (inside) {
+            // the identity term: chunk kIdChunk + hc holds this thread's 32 channels, [ch][row][col]
+            for (int j = 0; j < 2 && ok; ++j) {
+                const int i = tl * kChunks + kIdChunk + j, rs = i % kRawStages;
+                if (!mbar_wait(&raw_full[rs], (i / kRawStages) & 1, P.err, abort_v)) ok = false;
+            }
+            if (!ok) break;
+            {
+                const unsigned short* id = reinterpret_cast<const unsigned short*>(
+                    sm + kRaw + ((tl * kChunks + kIdChunk + hc) % kRawStages) * kRawStage);
                 bf16* dxp = P.dx + (long long)b * C * HW + pix;
-                // a base the compiler cannot match with the prefetch's: otherwise it keeps the 32
-                // prefetched addresses live across the taps
-                const bf16* g0q = g0p;
-                asm volatile("" : "+l"(g0q));
 #pragma unroll
-                for (int hh = 0; hh < 32; hh += 16) {   // 16 channels at a time (register budget)
-                    float g0[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        g0[i] = __bfloat162float(__ldg(g0q + (long long)min(hc * 32 + hh + i, C - 1) * HW));
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int ch = hc * 32 + hh + i;
-                        if (ch < C) dxp[(long long)ch * HW] = __float2bfloat16_rn(g0[i] + acc[hh + i]);
-                    }
+                for (int i = 0; i < 32; ++i) {
+                    const int ch = hc * 32 + i;
+                    const float g0 = __uint_as_float((uint32_t)id[(i * kDxTH + r) * kDxTW + c] << 16);
+                    if (inside && ch < C) dxp[(long long)ch * HW] = __float2bfloat16_rn(g0 + acc[i]);
                 }
             }
+            __syncwarp();
+            if (lane == 0)
+                for (int j = 0; j < 2; ++j) mbar_arrive(&raw_empty[(tl * kChunks + kIdChunk + j) % kRawStages]);
         }
     }
     tc_fence_before();
@@ -483,14 +489,15 @@ cudaError_t launch_bwd_dx_tc(const Dims& d, const void* g, const void* y, const 
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    CUtensorMap tmY, tmG;
+    CUtensorMap tmY, tmG, tmI;
     if (!encode_nchw(&tmY, y, d, d.C, kRawCols, (uint32_t)P.WH, 8, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_nchw(&tmG, g, d, 4 * d.C, kRawCols, (uint32_t)P.WH, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !encode_nchw(&tmG, g, d, 4 * d.C, kRawCols, (uint32_t)P.WH, 8, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_nchw(&tmI, g, d, 4 * d.C, kDxTW, kDxTH, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     int grid = num_sms();
     if (grid > P.n_tiles) grid = P.n_tiles;
     trace_begin(s, kKBwdDxTc);
-    bwd_dx_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmW, tmY, tmG, P);
+    bwd_dx_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmW, tmY, tmG, tmI, P);
     trace_end(s);
     return cudaGetLastError();
 }
