@@ -341,19 +341,24 @@ __global__ void __launch_bounds__(FwdLayout<K>::kThreads, FwdLayout<K>::kCtasPer
         // this thread's first staging element of block 0
         const uint32_t st0 = smem_u32(sm + kSStage) + (uint32_t)cl0 * ch_stride + (uint32_t)(in_tile ? s : 0) * 2;
         int buf = 0, bph = 0;
-        // hand staging block blk of tile tcd to the TMA: called by every epilogue thread after
-        // writing its values, the same number of times by all of them even after a failed
-        // wait (the named barrier has no time limit); the leader first makes sure the block
-        // written next is no longer being read by the store issued three blocks ago
+        // hand staging blocks blk and blk+1 of tile tcd to the TMA (twice per tile: blocks 0, 1
+        // after the first dilation, 2, 3 after the last): called by every epilogue thread after
+        // writing its values, the same number of times by all of them even after a failed wait
+        // (the named barrier has no time limit).  Before the barrier the leader waits until the
+        // previous pair's stores have read their blocks, so that past the barrier every thread
+        // may write the blocks that pair used (the next pair's writes come after it).
         bool ok = true;
-        auto flush_block = [&](int blk, const TileCoord& tcd) {
+        auto flush_pair = [&](int blk, const TileCoord& tcd) {
             fence_proxy_async_smem();
-            if (leader) bulk_wait_read<2>();
+            if (leader) bulk_wait_read<0>();
             epi_bar<32 * kEpiWarps>();
             if (leader && ok) {
-                const int cbase = (blk == 0 ? 0 : blk * C) + c0;
-                const uint8_t* src = sm + kSStage + blk * kStageBlk;
-                tma_store_4d(&tmO, src, tcd.w0, tcd.h0, cbase, tcd.b);
+#pragma unroll
+                for (int bb = 0; bb < 2; ++bb) {
+                    const int cbase = (blk + bb == 0 ? 0 : (blk + bb) * C) + c0;
+                    const uint8_t* src = sm + kSStage + (blk + bb) * kStageBlk;
+                    tma_store_4d(&tmO, src, tcd.w0, tcd.h0, cbase, tcd.b);
+                }
                 bulk_commit();
             }
         };
@@ -372,11 +377,10 @@ __global__ void __launch_bounds__(FwdLayout<K>::kThreads, FwdLayout<K>::kCtasPer
                 for (int c = 0; c < kCPT; ++c)
                     asm volatile("st.shared.u16 [%0], %1;" ::"r"(st0 + c * ch_stride), "h"(v[c]) : "memory");
             }
-            flush_block(0, tcd);
             for (int dd = 0; dd < 3; ++dd) {
                 if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar_acc_full[dd], i & 1, P.err, abort_v));
                 if (!ok) {
-                    flush_block(1 + dd, tcd);
+                    if (dd != 1) flush_pair(dd, tcd);
                     continue;
                 }
                 tc_fence_after();
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(FwdLayout<K>::kThreads, FwdLayout<K>::kCtasPer
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar_raw_empty[buf]);
                 }
-                flush_block(1 + dd, tcd);
+                if (dd != 1) flush_pair(dd, tcd);   // blocks 0, 1 after dilation 0; 2, 3 after dilation 2
             }
             if (++buf == kRawBufs) {
                 buf = 0;
