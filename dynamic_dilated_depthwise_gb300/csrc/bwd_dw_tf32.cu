@@ -19,7 +19,7 @@
 //   - another brings the block's grad rows [CB x 64 px] and x windows
 //     [CB x (1+2R) x (64 + 2 halo)] (zero outside the image) into a 2-stage ring the
 //     formers release as soon as dK is formed;
-//   - eight warps form dK^T[o, px] into a 128B-swizzled K-major tile (32 KiB);
+//   - two groups of eight warps (even and odd tiles) form dK^T[o, px] into a 128B-swizzled K-major tile (32 KiB);
 //   - one thread issues D[o, n] += dK^T[o, px] * Y[n, px], kind::tf32, M = 128,
 //     N = 80 (64 y channels, a ones row for dbias, 15 zero rows), K = 8 per
 //     instruction: eight instructions per tile.
@@ -34,10 +34,14 @@ using namespace bwdtc;
 
 constexpr int kTW32 = 64;                          // pixels of a tile (one image row)
 constexpr int kNY = 80;                            // MMA N: 64 y channels + ones row + 15 zero rows
-constexpr int kFormWarps = 8;
+constexpr int kGroupWarps = 8;                     // warps of one former group
+constexpr int kFormWarps = 2 * kGroupWarps;        // two groups: even and odd tiles
 constexpr int kThreads = 32 * (3 + kFormWarps);    // x/grad producer, MMA, formers, y producer
 constexpr int kYWarp = 2 + kFormWarps;
 constexpr int kYStages = 2, kXgStages = 2;
+// tile i uses x/grad stage i % 2 and is formed by group i % 2: each stage serves one group,
+// so each group waits on a barrier whose previous phase it has seen itself
+static_assert(kXgStages == 2, "one x/grad stage per former group");
 constexpr int kSmemCap = 232448 - 1024;            // dynamic shared memory: the opt-in 227 KiB less the static part
 
 // Per kernel size: channels per block of taps, the x window's column halo (left and
@@ -202,10 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kXgStages; ++s) {
             mbar_init(&xg_full[s], 1);
-            mbar_init(&xg_empty[s], kFormWarps);
+            mbar_init(&xg_empty[s], kGroupWarps);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&dk_full[s], kFormWarps);
+            mbar_init(&dk_full[s], kGroupWarps);
             mbar_init(&dk_empty[s], 1);
         }
         mbar_init(&acc_done, 1);
@@ -308,9 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------- dK formers + epilogue
-        const int et = threadIdx.x - 64;
+        // group grp forms tiles grp, grp + 2, ... into dK^T buffer grp
+        const int grp = (warp - 2) / kGroupWarps;
+        const int et = threadIdx.x - 64 - grp * 32 * kGroupWarps;
         bool ok = true;
-        for (int i = 0; i < n_my && ok; ++i) {
+        for (int i = grp; i < n_my && ok; i += 2) {
             const int s = i & 1, ph = (i >> 1) & 1;
             const int sx = i % kXgStages, xph = (i / kXgStages) & 1;
             if (!mbar_wait(&xg_full[sx], xph, P.err, abort_v) || !mbar_wait(&dk_empty[s], ph ^ 1, P.err, abort_v)) {
@@ -319,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const uint8_t* st = sm + kXG + sx * P.xg_stage;
             form_dk_f32<K>(sm + kDK + s * kDK32, reinterpret_cast<const float*>(st + kGStage),
-                        reinterpret_cast<const float*>(st), nc, P.xslot / 4, P.R, dil, et, 32 * kFormWarps);
+                        reinterpret_cast<const float*>(st), nc, P.xslot / 4, P.R, dil, et, 32 * kGroupWarps);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -327,7 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&xg_empty[sx]);
             }
         }
-        // epilogue: this split's partial sums for the block of taps
+        // epilogue (group 0): this split's partial sums for the block of taps
+        if (grp != 0) ok = false;
         const int q = warp & 3, hc = (warp - 2) >> 2;
         const int row = q * 32 + lane;
         const int rc = row / kTaps;
