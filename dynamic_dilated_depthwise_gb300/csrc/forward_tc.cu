@@ -323,8 +323,8 @@ __global__ void __launch_bounds__(FwdLayout<K>::kThreads, FwdLayout<K>::kCtasPer
     } else {
         // ------------------------------------------------------- epilogue
         // Results go to a staging block [8 ch][TH][TW] per output block (x, d1, d3, d5),
-        // which one thread writes out with TMA stores once every epilogue warp has filled it;
-        // the stores clip pixels outside the image.
+        // which one thread writes out with TMA stores, two blocks at a time once every
+        // epilogue warp has filled them; the stores clip pixels outside the image.
         const int ew = warp - kEpi0;
         const int q = warp & 3;          // TMEM lane quadrant this warp may access
         const int cl0 = (ew >> 2) * kCPT;   // first local channel of this thread
